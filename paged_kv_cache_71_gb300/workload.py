@@ -1,0 +1,368 @@
+"""Seeded synthetic workloads for paged decode attention, and the host block allocator.
+
+This module builds inputs only.  It holds none of the attention arithmetic:
+it draws lengths and values from seeded generators, hands out physical
+blocks the way a serving engine's block manager does, and records where
+each new token must be written.  Both the CUDA path and the CPU oracle
+consume what it produces; neither is imported here.
+
+Block manager semantics follow the allocator simulation in "3.3 批处理与
+内存管理" (Batching and Memory Management, llm-learning-path), section
+"代码": a free list popped from its tail, one reference count per physical
+block, prefill allocates ceil(n / S) blocks, a decode append allocates a
+new block when the last one is full, and a write into a shared (refcount >
+1) partial block first moves the sequence onto a private copy
+("共享与写时复制", copy-on-write).  The copy of the data itself is the
+``copy_blocks`` kernel's job; the allocator records the (src, dst) pair.
+
+Value distributions (all seeded with ``numpy.random.default_rng``):
+Q, K, V ~ N(0, 1) drawn in float32 and rounded once to the storage dtype;
+FP8 E4M3 caches hold random codes (uniform sign and mantissa, exponent
+field uniform in [4, 10]) with a per-tensor scale of 0.25, so that no
+quantiser is involved in making them.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+# ---------------------------------------------------------------- block manager
+
+
+class BlockAllocator:
+    """Host-side paged-KV block manager (free list + refcounts + copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        self.block_size = int(block_size)
+        self.num_blocks = int(num_blocks)
+        self.free = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        assert sorted(self.free) == list(range(num_blocks))
+        self.ref = [0] * num_blocks
+        self.tables: dict = {}
+        self.lens: dict = {}
+        self.pending_copies: list[tuple[int, int]] = []
+
+    def _take(self) -> int:
+        if not self.free:
+            raise MemoryError("KV pool exhausted: the scheduler must preempt (swap out or recompute)")
+        b = self.free.pop()
+        self.ref[b] = 1
+        return b
+
+    def blocks_needed(self, n_tokens: int) -> int:
+        return -(-int(n_tokens) // self.block_size)
+
+    def add_seq(self, sid, n_tokens: int) -> None:
+        """Prefill: allocate ceil(n / S) blocks for n tokens."""
+        self.tables[sid] = [self._take() for _ in range(self.blocks_needed(n_tokens))]
+        self.lens[sid] = int(n_tokens)
+
+    def append_token(self, sid) -> int:
+        """Decode append: returns the slot (block * S + offset) of the new token."""
+        table, n = self.tables[sid], self.lens[sid]
+        if n % self.block_size == 0:
+            table.append(self._take())
+        elif self.ref[table[-1]] > 1:
+            src = table[-1]
+            self.ref[src] -= 1
+            table[-1] = self._take()
+            self.pending_copies.append((src, table[-1]))
+        self.lens[sid] = n + 1
+        return self.slot_of(sid, n)
+
+    def fork(self, parent, child) -> None:
+        """Parallel sampling / beam fork: the child shares every block of the parent."""
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        for b in self.tables[child]:
+            self.ref[b] += 1
+
+    def free_seq(self, sid) -> None:
+        for b in self.tables.pop(sid):
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        del self.lens[sid]
+
+    def slot_of(self, sid, pos: int) -> int:
+        """Flattened cache slot of logical position ``pos``: block * S + offset."""
+        S = self.block_size
+        return self.tables[sid][pos // S] * S + pos % S
+
+    def take_copies(self) -> list[tuple[int, int]]:
+        out, self.pending_copies = self.pending_copies, []
+        return out
+
+    def padded_tables(self, sids, width: int | None = None) -> np.ndarray:
+        width = width or max(len(self.tables[s]) for s in sids)
+        bt = np.full((len(sids), width), -1, dtype=np.int32)
+        for i, s in enumerate(sids):
+            t = self.tables[s]
+            bt[i, : len(t)] = t
+        return bt
+
+
+# ---------------------------------------------------------------- value generation
+
+DTYPES = ("f32", "bf16", "e4m3")
+_ELEM = {"f32": 4, "bf16": 2, "e4m3": 1}
+FP8_SCALE = 0.25
+
+
+def elem_size(dtype: str) -> int:
+    return _ELEM[dtype]
+
+
+def _normal_f32(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.standard_normal(size=shape, dtype=np.float32)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest even) and return the bit patterns."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _fill_chunk(base: int, c: int, a: int, b: int, dtype: str, out: np.ndarray) -> None:
+    sub = np.random.default_rng([base, c])
+    v = _normal_f32(sub, b - a)
+    out[a:b] = v if dtype == "f32" else to_bf16_bits(v)
+
+
+def random_values(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
+    """N(0,1) values stored as float32 / bf16 bits (uint16) / random E4M3 codes (uint8).
+
+    Large arrays are drawn in fixed-size chunks, each from its own generator
+    seeded by (a draw of ``rng``, chunk index), on a thread pool: the result
+    depends only on ``rng``'s state, not on the number of threads."""
+    shape = tuple(int(s) for s in shape)
+    n = int(np.prod(shape)) if shape else 1
+    if dtype == "e4m3":
+        sign = rng.integers(0, 2, size=n, dtype=np.uint8)
+        expo = rng.integers(4, 11, size=n, dtype=np.uint8)
+        mant = rng.integers(0, 8, size=n, dtype=np.uint8)
+        return ((sign << 7) | (expo << 3) | mant).astype(np.uint8).reshape(shape)
+    out = np.empty(n, dtype=np.float32 if dtype == "f32" else np.uint16)
+    if n <= chunk:
+        v = _normal_f32(rng, n)
+        out[:] = v if dtype == "f32" else to_bf16_bits(v)
+        return out.reshape(shape)
+    base = int(rng.integers(0, 2**63 - 1))
+    spans = [(c, a, min(n, a + chunk)) for c, a in enumerate(range(0, n, chunk))]
+    workers = max(1, min(len(spans), os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda t: _fill_chunk(base, t[0], t[1], t[2], dtype, out), spans))
+    return out.reshape(shape)
+
+
+# ---------------------------------------------------------------- configurations
+
+
+@dataclass
+class PrefillChunk:
+    q: np.ndarray              # [NQ, Hq, D] in q dtype
+    q_start: int               # position of the chunk's first query token
+    kv_len: int                # keys visible to the last query (q_start + NQ)
+    block_table: np.ndarray    # int32 [blocks] of the chunk's sequence
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    kv_dtype: str
+    q_dtype: str
+    k_scale: float
+    v_scale: float
+    q: np.ndarray                     # [B, Hq, D]
+    k_cache: np.ndarray               # [NB, S, Hkv, D]
+    v_cache: np.ndarray
+    block_tables: np.ndarray          # int32 [B, MB], -1 padded
+    context_lens: np.ndarray          # int32 [B], includes this step's token
+    k_new: np.ndarray                 # [T, Hkv, D] in q dtype (the projection's output dtype)
+    v_new: np.ndarray
+    slot_mapping: np.ndarray          # int64 [T]
+    copy_pairs: np.ndarray            # int64 [N, 2] (src, dst), may be empty
+    prefill: PrefillChunk | None = None
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.head_dim))
+
+
+CONFIG_NAMES = ("tiny", "llama2_7b", "llama3_8b_gqa", "prefix_shared", "llama70b_mixed_bf16",
+                "llama70b_mixed_fp8")
+
+CONFIG_SEEDS = {"tiny": 7100, "llama2_7b": 7101, "llama3_8b_gqa": 7102, "prefix_shared": 7103,
+                "llama70b_mixed_bf16": 7104, "llama70b_mixed_fp8": 7104}
+
+
+def _pool_size(total_blocks: int, slack: float = 0.05) -> int:
+    return int(total_blocks + max(1, int(np.ceil(total_blocks * slack))))
+
+
+def _cache_and_q(rng, NB, S, Hkv, D, B, Hq, kv_dtype, q_dtype):
+    k_cache = random_values(rng, (NB, S, Hkv, D), kv_dtype)
+    v_cache = random_values(rng, (NB, S, Hkv, D), kv_dtype)
+    q = random_values(rng, (B, Hq, D), q_dtype)
+    return k_cache, v_cache, q
+
+
+def _decode_batch(name, lens, Hq, Hkv, D, S, kv_dtype, q_dtype, seed, exact_pool=None):
+    """B independent sequences: prefill L-1 tokens, then append this step's token."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int64)
+    need = int(sum(-(-int(L) // S) for L in lens))
+    NB = exact_pool or _pool_size(need)
+    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    slots = []
+    for s, L in enumerate(lens):
+        alloc.add_seq(s, int(L) - 1)
+        slots.append(alloc.append_token(s))
+    sids = list(range(len(lens)))
+    k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, len(lens), Hq, kv_dtype, q_dtype)
+    k_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
+    v_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
+    scale = FP8_SCALE if kv_dtype == "e4m3" else 1.0
+    return Workload(name, seed, Hq, Hkv, D, S, kv_dtype, q_dtype, scale, scale, q, k_cache, v_cache,
+                    alloc.padded_tables(sids), lens.astype(np.int32), k_new, v_new,
+                    np.array(slots, dtype=np.int64), np.zeros((0, 2), dtype=np.int64),
+                    notes={"pool_blocks": NB, "used_blocks": need})
+
+
+def tiny(seed: int = CONFIG_SEEDS["tiny"]) -> Workload:
+    """4 sequences {10, 6, 33, 1}, S=4, 32 permuted physical blocks, 4 q / 2 kv heads, D=64, fp32.
+    The 4 new tokens land at positions {9, 5, 32, 0}."""
+    return _decode_batch("tiny", [10, 6, 33, 1], 4, 2, 64, 4, "f32", "f32", seed, exact_pool=32)
+
+
+def llama2_7b(seed: int = CONFIG_SEEDS["llama2_7b"]) -> Workload:
+    """Batch 64, 32 q = 32 kv heads, D=128, bf16, S=16, lengths uniform in [128, 4096]."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(128, 4097, size=64)
+    return _decode_batch("llama2_7b", lens, 32, 32, 128, 16, "bf16", "bf16", seed + 1000)
+
+
+def lognormal_lengths(rng, n, median=1024.0, sigma=1.0, lo=16, hi=8192) -> np.ndarray:
+    return np.clip(np.round(np.exp(rng.normal(np.log(median), sigma, size=n))), lo, hi).astype(np.int64)
+
+
+def llama3_8b_gqa(seed: int = CONFIG_SEEDS["llama3_8b_gqa"], batch: int = 256) -> Workload:
+    """Batch 256, 32 q / 8 kv heads, D=128, bf16, S=16, lengths lognormal (median 1024,
+    sigma 1) clipped to [16, 8192]; plus the cache write of the 256 new tokens."""
+    rng = np.random.default_rng(seed)
+    lens = lognormal_lengths(rng, batch)
+    return _decode_batch("llama3_8b_gqa", lens, 32, 8, 128, 16, "bf16", "bf16", seed + 1000)
+
+
+def prefix_shared(seed: int = CONFIG_SEEDS["prefix_shared"], batch: int = 128, prefix: int = 800,
+                  private: int = 205, cow_parent_len: int = 805) -> Workload:
+    """128 sequences share an 800-token prefix (the same 50 physical blocks, refcount 128) and
+    then hold 205 private tokens each (L = 1005).  A fork of a parent whose last block is
+    partial (805 tokens, 5 in block 50) into 128 children makes every child's first append
+    copy that block: 128 (src, dst) pairs for copy_blocks, then each child writes its token
+    at offset 5 of its copy; the parent keeps the original."""
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D = 16, 32, 8, 128
+    need = (prefix // S) + batch * (-(-(prefix + private) // S) - prefix // S) \
+        + (-(-cow_parent_len // S)) + batch
+    NB = _pool_size(need)
+    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc.add_seq("prefix", prefix)
+    for s in range(batch):
+        alloc.fork("prefix", s)
+    alloc.free_seq("prefix")
+    slots = []
+    for s in range(batch):
+        for _ in range(private - 1):
+            alloc.append_token(s)
+        slots.append(alloc.append_token(s))
+    alloc.add_seq("cow_parent", cow_parent_len)
+    cow_children = [("cow", c) for c in range(batch)]
+    for c in cow_children:
+        alloc.fork("cow_parent", c)
+    for c in cow_children:
+        slots.append(alloc.append_token(c))
+    pairs = np.array(alloc.take_copies(), dtype=np.int64).reshape(-1, 2)
+    sids = list(range(batch))
+    k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, batch, Hq, "bf16", "bf16")
+    T = len(slots)
+    k_new = random_values(rng, (T, Hkv, D), "bf16")
+    v_new = random_values(rng, (T, Hkv, D), "bf16")
+    lens = np.array([alloc.lens[s] for s in sids], dtype=np.int32)
+    shared = alloc.tables[0][: prefix // S]
+    return Workload("prefix_shared", seed, Hq, Hkv, D, S, "bf16", "bf16", 1.0, 1.0, q, k_cache, v_cache,
+                    alloc.padded_tables(sids), lens, k_new, v_new, np.array(slots, dtype=np.int64), pairs,
+                    notes={"pool_blocks": NB, "shared_blocks": list(map(int, shared)),
+                           "shared_refcount": alloc.ref[shared[0]],
+                           "cow_parent_table": list(map(int, alloc.tables["cow_parent"])),
+                           "cow_child_tables": [list(map(int, alloc.tables[c])) for c in cow_children],
+                           "cow_child_len": alloc.lens[cow_children[0]],
+                           "num_decode_tokens": batch})
+
+
+def llama70b_mixed(kv_dtype: str = "bf16", seed: int = CONFIG_SEEDS["llama70b_mixed_bf16"],
+                   batch: int = 48, chunk: int = 512, prefix: int = 8192) -> Workload:
+    """64 q / 8 kv heads, D=128, S=16: 48 decode sequences with lengths uniform in
+    [4096, 32768] plus one chunked-prefill chunk of 512 query tokens at positions
+    8192..8703 over an 8192-token paged prefix (the chunk's own K/V is written first,
+    so 8704 keys are cached).  KV in bf16 or FP8 E4M3 with a per-tensor scale."""
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, D = 16, 64, 8, 128
+    lens = rng.integers(4096, 32769, size=batch)
+    need = int(sum(-(-int(L) // S) for L in lens)) + (-(-(prefix + chunk) // S))
+    NB = _pool_size(need)
+    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    slots = []
+    for s, L in enumerate(lens):
+        alloc.add_seq(s, int(L) - 1)
+        slots.append(alloc.append_token(s))
+    alloc.add_seq("chunked", prefix)
+    for _ in range(chunk):
+        slots.append(alloc.append_token("chunked"))
+    sids = list(range(batch))
+    k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, batch, Hq, kv_dtype, "bf16")
+    T = len(slots)
+    k_new = random_values(rng, (T, Hkv, D), "bf16")
+    v_new = random_values(rng, (T, Hkv, D), "bf16")
+    q_chunk = random_values(rng, (chunk, Hq, D), "bf16")
+    pf = PrefillChunk(q_chunk, prefix, prefix + chunk, np.array(alloc.tables["chunked"], dtype=np.int32))
+    scale = FP8_SCALE if kv_dtype == "e4m3" else 1.0
+    name = "llama70b_mixed_" + ("fp8" if kv_dtype == "e4m3" else "bf16")
+    return Workload(name, seed, Hq, Hkv, D, S, kv_dtype, "bf16", scale, scale, q, k_cache, v_cache,
+                    alloc.padded_tables(sids), lens.astype(np.int32), k_new, v_new,
+                    np.array(slots, dtype=np.int64), np.zeros((0, 2), dtype=np.int64), prefill=pf,
+                    notes={"pool_blocks": NB, "num_decode_tokens": batch})
+
+
+def make(name: str, **kw) -> Workload:
+    if name == "tiny":
+        return tiny(**kw)
+    if name == "llama2_7b":
+        return llama2_7b(**kw)
+    if name == "llama3_8b_gqa":
+        return llama3_8b_gqa(**kw)
+    if name == "prefix_shared":
+        return prefix_shared(**kw)
+    if name == "llama70b_mixed_bf16":
+        return llama70b_mixed("bf16", **kw)
+    if name == "llama70b_mixed_fp8":
+        return llama70b_mixed("e4m3", seed=CONFIG_SEEDS["llama70b_mixed_fp8"], **kw)
+    raise KeyError(name)
