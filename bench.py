@@ -1,0 +1,344 @@
+"""Benchmark of the paged decode step on GB300.
+
+One step = the whole hot path for one batch: the cache write of the step's
+new tokens (reshape_and_cache), copy-on-write block copies when the batch
+has any, and paged decode attention over every sequence.  Default workload:
+the Llama-3-8B GQA batch (256 sequences, 32 q / 8 kv heads, head_dim 128,
+bf16 KV, 16-token blocks, lognormal lengths) -- one layer.
+
+Prints ONE JSON line (rank 0).  `value` is sequence-steps per second per
+layer over all ranks, with inputs resident in HBM; `e2e` repeats the
+measurement through the C ABI with host buffers (the step's inputs copied
+in and the output copied out inside the timed region); `roofline` rates the
+decode kernel's algorithmic bytes per launch against the measured HBM copy
+bandwidth; `cpu_baseline` times the fp64 oracle on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn KV GB/s & % of GB300 HBM peak; seq-steps/sec per layer"
+UNIT = "seq-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- byte accounting
+
+def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, dtype_bytes: int) -> int:
+    """K and V bytes one token occupies: 2 x layers x kv heads x head_dim x element size."""
+    return 2 * n_layers * n_kv_heads * head_dim * dtype_bytes
+
+
+def decode_algorithmic_bytes(w) -> int:
+    """Bytes one decode launch must touch at least: every sequence's K and V once per KV head,
+    the queries, the outputs, the block-table entries it reads and the context lengths."""
+    from paged_kv_cache_71_gb300.workload import elem_size
+    L = w.context_lens.astype(np.int64)
+    kv = int(L.sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, elem_size(w.kv_dtype))
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * elem_size(w.q_dtype)
+    table = int(((L + w.block_size - 1) // w.block_size).sum()) * 4
+    return kv + qo + table + 4 * w.num_seqs
+
+
+def write_bytes(w) -> int:
+    from paged_kv_cache_71_gb300.workload import elem_size
+    T = len(w.slot_mapping)
+    row = w.num_kv_heads * w.head_dim
+    return 2 * T * row * (elem_size(w.q_dtype) + elem_size(w.kv_dtype)) + 8 * T
+
+
+# ---------------------------------------------------------------- environment helpers
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(w, steps: int = 1, max_seconds: float = 20.0) -> dict:
+    """fp64 oracle on the host cores: the step's cache write and decode over the whole batch,
+    repeated up to `steps` times or until `max_seconds` pass."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3}[w.kv_dtype]
+    done, t0 = 0, time.perf_counter()
+    while done < steps:
+        oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc, cache_dtype=cache_dt,
+                                 k_scale=w.k_scale, v_scale=w.v_scale)
+        oracle.paged_attention_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, cache_dtype=cache_dt,
+                                      k_scale=w.k_scale, v_scale=w.v_scale, threads=threads)
+        done += 1
+        if time.perf_counter() - t0 > max_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": w.num_seqs * done / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} full step(s) of the {w.name} batch ({w.num_seqs} sequences), fp64, "
+                      f"{dt:.1f} s", "seconds": dt, "steps": done}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama3_8b_gqa")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_env()
+    import torch
+    from paged_kv_cache_71_gb300 import workload as wl
+
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
+
+    # every rank serves its own batch (sequences shard across GPUs; no exchange)
+    w = wl.make(args.config, seed=wl.CONFIG_SEEDS[args.config] + 1000 * rank) if args.config != "llama70b_mixed_fp8" \
+        else wl.make(args.config)
+    st = DeviceStep(w, num_splits=args.num_splits)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 2 + (1 if st.copy_pairs is not None else 0)
+
+    def step():
+        st.write(stream)
+        st.attend(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if st.device_error():
+        raise RuntimeError(f"device error {st.device_error():#x}")
+
+    # ---- device-resident timing: events around each step and around each decode launch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        st.write(stream)
+        ev[i][1].record(stream)
+        st.attend(stream)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * w.num_seqs / (ms_per_step / 1e3)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(st, k).cpu().pin_memory() for k in
+                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+        out_host = torch.empty_like(st.out, device="cpu").pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                getattr(st, k).copy_(t, non_blocking=True)
+            step()
+            out_host.copy_(st.out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / args.steps
+        if dist:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": ws * w.num_seqs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    peak, peak_src = measured_peaks()
+    alg = decode_algorithmic_bytes(w)
+    dec_avg = float(np.mean(decode_ms))
+    achieved = alg / (dec_avg / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
+            "kernel": "paged_decode_kernel", "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, steps=3, max_seconds=20.0)
+        cpu.pop("seconds", None)
+        cpu.pop("steps", None)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                       "kv_dtype": w.kv_dtype, "mean_context": float(w.context_lens.mean()),
+                       "num_splits": args.num_splits, "parallelism": f"replicas{ws}",
+                       "l2": f"inputs larger than L2: {alg / 1e9:.2f} GB of K/V read per step"},
+            "kv_gbps": round(achieved, 1), "pct_of_hbm_peak": round(100 * achieved / peak, 2),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "kernels": {"paged_decode_us": round(dec_avg * 1e3, 2),
+                        "reshape_and_cache_us": round(float(np.mean(write_ms)) * 1e3, 2),
+                        "write_bytes": write_bytes(w)},
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args, ws, rank):
+    """The oracle, as it stands, timed on the host cores on the same workload (rank 0 only)."""
+    if rank != 0:
+        return
+    from paged_kv_cache_71_gb300 import workload as wl
+    w = wl.make(args.config)
+    time_oracle(w, steps=1, max_seconds=5.0)  # warm the library and caches
+    per = []
+    for _ in range(args.warmup):
+        time_oracle(w, steps=1, max_seconds=60.0)
+    for _ in range(args.steps):
+        r = time_oracle(w, steps=1, max_seconds=60.0)
+        per.append(r["seconds"])
+    ms = 1e3 * float(np.mean(per))
+    value = w.num_seqs / (ms / 1e3)
+    cores = r["cores"]
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                       "kv_dtype": w.kv_dtype},
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step = the full {w.name} batch ({w.num_seqs} sequences): cache "
+                                       f"write + fp64 decode"},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache library (GB300 / sm_103a).
+ *
+ * One shared library, libpkv.so, with hand-written CUDA kernels for the
+ * decode step of a paged KV cache.  Every entry point:
+ *   - takes plain pointers and sizes (no framework types);
+ *   - expects DEVICE pointers for every tensor argument unless stated,
+ *     owned by the caller; the library never allocates, frees or
+ *     synchronises device memory;
+ *   - enqueues its work on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns after enqueueing;
+ *   - validates shapes, dtypes and alignment on the host before launching
+ *     and returns a status code; a failed check launches nothing;
+ *   - reports data-dependent range errors found on the device (bad block
+ *     ids, slots beyond the pool, bad lengths, a timed-out wait) by OR-ing
+ *     PKV_DEVERR_* bits into `*device_error` (device memory, nullable), and
+ *     skips the offending item.  It never traps.
+ *
+ * Layouts (row-major, innermost last):
+ *   K / V cache, per layer:  [num_blocks][block_size][num_kv_heads][head_dim]
+ *     -- the per-block layout [block_size, n_kv_heads, head_dim] of the
+ *        KVBlock definition in "大模型推理的KV Cache优化全解" (block structure
+ *        section), one layer at a time, K and V in separate tensors.
+ *   block_tables: int32 [num_seqs][max_blocks_per_seq]; entry j of row s is
+ *     the physical block holding tokens [j*S, (j+1)*S) of sequence s
+ *     ("3.3 批处理与内存管理", section "PagedAttention：块表", equation:
+ *     physical block = table[p / S], offset = p % S).  Entries past a
+ *     sequence's last block are never read.
+ *   context_lens: int32 [num_seqs]; tokens in each sequence, INCLUDING the
+ *     token written by this step's reshape_and_cache.
+ *   slot_mapping: int64 [num_tokens]; slot = block * S + offset; a negative
+ *     slot marks a padding token that is skipped.
+ *   q / out (decode): [num_seqs][num_q_heads][head_dim].
+ *   GQA: query head hq reads KV head hq / G, G = num_q_heads / num_kv_heads.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: dtype combo, head_dim, block_size, G */
+    PKV_ERR_OUT_OF_RANGE = 3,  /* a host-checkable index or size beyond its limit */
+    PKV_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned */
+    PKV_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
+} pkv_status;
+
+typedef enum {
+    PKV_F32 = 0,
+    PKV_BF16 = 1,
+    PKV_FP8_E4M3 = 2   /* OCP E4M3 (bias 7, max 448, no inf), per-tensor scale */
+} pkv_dtype;
+
+/* Bits OR-ed into *device_error by the kernels. */
+#define PKV_DEVERR_BAD_SLOT 0x1     /* slot >= num_blocks * block_size */
+#define PKV_DEVERR_BAD_BLOCK 0x2    /* block id < 0 or >= num_blocks where one must be read */
+#define PKV_DEVERR_BAD_LENGTH 0x4   /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEVERR_TIMEOUT 0x8      /* a bounded wait on an async copy gave up */
+
+/* Description of one layer's K and V cache pools. */
+typedef struct {
+    int32_t num_blocks;    /* physical blocks in the pool (NB) */
+    int32_t block_size;    /* tokens per block (S): 4, 8, 16 or 32 */
+    int32_t num_kv_heads;  /* Hkv */
+    int32_t head_dim;      /* D: 64 or 128 */
+    int32_t dtype;         /* pkv_dtype of the cache elements */
+    float k_scale;         /* FP8 only: stored code * k_scale is the key value; 1 otherwise */
+    float v_scale;         /* FP8 only: same for values */
+} pkv_cache_desc;
+
+/*
+ * Cache write ("reshape_and_cache").
+ * Each step computes the new token's k_t, v_t and appends them to the cache
+ * ("大模型推理的KV Cache优化全解", §1.1; "3.3 批处理与内存管理", section
+ * "代码", append_token).  For token i with slot_mapping[i] >= 0:
+ *   k_cache[slot / S][slot % S][h][:] = convert(k_new[i][h][:])   (same for v)
+ * convert: same dtype -> bit copy; bf16 -> f32 exact; f32 -> bf16 round to
+ * nearest even; -> FP8 E4M3: sat(RNE(x / scale)) with an fp32 division.
+ *   k_new, v_new: [num_tokens][num_kv_heads][head_dim] of src_dtype (f32 or bf16).
+ * Tokens whose slot is beyond the pool set PKV_DEVERR_BAD_SLOT and are skipped.
+ * Two tokens with the same slot race (one of them wins).
+ * Alignment: k_new, v_new, k_cache, v_cache 16-byte aligned.
+ */
+pkv_status pkv_reshape_and_cache(const void* k_new, const void* v_new, int32_t src_dtype,
+                                 const int64_t* slot_mapping, int32_t num_tokens,
+                                 void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                 int32_t* device_error, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_attention_decode needs for these
+ * sizes on the CURRENT device (0 when num_splits == 1).  The workspace holds
+ * the split-KV partial results (m, l, O) and one completion counter per
+ * (sequence, KV head); the decode call clears the counters itself.
+ */
+pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32_t num_seqs,
+                                              int32_t num_q_heads, int32_t num_splits,
+                                              size_t* bytes);
+
+/*
+ * Paged decode attention over a ragged batch (one query token per sequence).
+ * For every sequence s and query head hq (KV head h = hq / G):
+ *   out[s][hq] = softmax(scale * q[s][hq] . K_s^T) V_s
+ * where K_s / V_s are positions [0, context_lens[s]) gathered through the
+ * block table ("3.3 批处理与内存管理", "PagedAttention：块表"), evaluated
+ * block by block with the online-softmax recurrence of "从 PagedAttention 到
+ * Chunked Prefill" §2.2 (running max m, running sum l, unnormalised O,
+ * rescaled by exp(m_old - m_new) when the max grows; out = O / l).
+ * A sequence with context length 0 gets an all-zero row.
+ *
+ * Split-KV: the work of all (sequence, KV head) pairs is laid end to end
+ * block by block and cut into equal shares, one per worker warp, so that
+ * long and short sequences load the GPU evenly; a pair cut across workers
+ * produces partial (m, l, O) triples that the last finishing worker merges
+ * (M = max m_p, l = sum e^(m_p - M) l_p, O = sum e^(m_p - M) O_p / l).
+ *   num_splits == 0 : cut anywhere on block boundaries (balanced; default)
+ *   num_splits == 1 : never cut a pair (single pass; workspace unused)
+ *   num_splits == P : cut only on boundaries of partitions of
+ *                     ceil(ceil(max_context_len / S) / P) blocks
+ * Any choice gives the same result up to fp32 rounding order.
+ *
+ *   q:   [num_seqs][num_q_heads][head_dim], q_dtype f32 (with an f32 cache)
+ *        or bf16 (with a bf16 or FP8 cache); out has q's dtype and shape.
+ *   max_context_len: an upper bound of context_lens (0 = use
+ *        max_blocks_per_seq * block_size); only shapes the partitions.
+ *   workspace: >= pkv_paged_attention_workspace_size bytes, 16-byte
+ *        aligned (may be NULL when num_splits == 1).  Concurrent calls must
+ *        not share a workspace.
+ * Supported: head_dim 64/128, block_size 4/8/16/32, G in {1, 2, 4, 8},
+ *   num_seqs <= 8192.  Pointers q, out and the caches 16-byte aligned.
+ */
+pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
+                                      const void* k_cache, const void* v_cache,
+                                      const pkv_cache_desc* cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, float scale, int32_t num_splits,
+                                      int32_t max_context_len, void* workspace,
+                                      size_t workspace_bytes, int32_t* device_error,
+                                      void* stream);
+
+/*
+ * Copy whole physical blocks, for copy-on-write of shared blocks
+ * ("3.3 批处理与内存管理", section "共享与写时复制": before a sequence writes
+ * into a block whose reference count is above one, the engine copies the
+ * block and points the sequence's table at the copy).  For each pair i:
+ *   k_cache[dst_i] = k_cache[src_i];  v_cache[dst_i] = v_cache[src_i]
+ * (all block_size slots, bit-exact).
+ *   block_mapping: int64 [num_pairs][2] = (src, dst), device memory.
+ * A dst may not appear as a src in the same call (the copies run
+ * concurrently); ids outside [0, num_blocks) set PKV_DEVERR_BAD_BLOCK and
+ * that pair is skipped.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                           const int64_t* block_mapping, int32_t num_pairs,
+                           int32_t* device_error, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* pkv_status_string(pkv_status status);
+
+/* Details of the last failed call on the calling host thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* PKV_ABI_VERSION of the loaded library. */
+int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,157 @@
+"""ctypes binding of libpkv.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does
+nothing but turn tensors into pointers and sizes, pick the current CUDA
+stream, call the library and raise on a non-OK status.  All computation
+happens in the library's CUDA kernels.  There is no fallback: without a
+built libpkv.so these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpkv.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "pkv.h")
+
+PKV_F32, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_OUT_OF_RANGE",
+                4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
+DEVERR_BAD_SLOT, DEVERR_BAD_BLOCK, DEVERR_BAD_LENGTH, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+_DTYPE_CODE = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3,
+               torch.float8_e4m3fn: PKV_FP8_E4M3}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, func: str, detail: str):
+        self.status = status
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)}: {detail}")
+
+
+class CacheDesc(ctypes.Structure):
+    """Mirror of pkv_cache_desc."""
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+    @classmethod
+    def for_cache(cls, k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> "CacheDesc":
+        NB, S, Hkv, D = k_cache.shape
+        return cls(NB, S, Hkv, D, _DTYPE_CODE[k_cache.dtype], float(k_scale), float(v_scale))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libpkv.so is not built ({LIB_PATH}); run __graft_entry__.build() or "
+                           "python -m paged_kv_cache_71_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(CacheDesc)
+    L.pkv_reshape_and_cache.argtypes = [P, P, i32, P, i32, P, P, D, P, P]
+    L.pkv_paged_attention_workspace_size.argtypes = [D, i32, i32, i32, ctypes.POINTER(sz)]
+    L.pkv_paged_attention_decode.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32, P, sz, P, P]
+    L.pkv_copy_blocks.argtypes = [P, P, D, P, i32, P, P]
+    for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
+                 "pkv_copy_blocks"):
+        getattr(L, name).restype = ctypes.c_int
+    L.pkv_status_string.argtypes = [ctypes.c_int]
+    L.pkv_status_string.restype = ctypes.c_char_p
+    L.pkv_last_error.argtypes = []
+    L.pkv_last_error.restype = ctypes.c_char_p
+    L.pkv_abi_version.argtypes = []
+    L.pkv_abi_version.restype = ctypes.c_int32
+    _lib = L
+    return L
+
+
+def declared_entry_points() -> list[str]:
+    """Names of the functions declared in include/pkv.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:pkv_status|const char\*|int32_t)\s+(pkv_\w+)\s*\(", text, re.M)))
+
+
+def _check(status: int, func: str) -> None:
+    if status != PKV_OK:
+        raise PkvError(status, func, (lib().pkv_last_error() or b"").decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(t: torch.Tensor) -> int:
+    return _DTYPE_CODE[t.dtype]
+
+
+# ---------------------------------------------------------------- entry points
+
+def pkv_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, cache: CacheDesc, device_error=None,
+                          stream=None) -> None:
+    _check(lib().pkv_reshape_and_cache(_ptr(k_new), _ptr(v_new), _dtype(k_new), _ptr(slot_mapping),
+                                       int(slot_mapping.shape[0]), _ptr(k_cache), _ptr(v_cache),
+                                       ctypes.byref(cache), _ptr(device_error), _stream(stream)),
+           "pkv_reshape_and_cache")
+
+
+def pkv_paged_attention_workspace_size(cache: CacheDesc, num_seqs: int, num_q_heads: int, num_splits: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pkv_paged_attention_workspace_size(ctypes.byref(cache), int(num_seqs), int(num_q_heads),
+                                                    int(num_splits), ctypes.byref(out)),
+           "pkv_paged_attention_workspace_size")
+    return int(out.value)
+
+
+def pkv_paged_attention_decode(out, q, k_cache, v_cache, cache: CacheDesc, block_tables, context_lens,
+                               scale: float, num_splits: int = 0, max_context_len: int = 0, workspace=None,
+                               device_error=None, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_attention_decode(_ptr(out), _ptr(q), _dtype(q), _ptr(k_cache), _ptr(v_cache),
+                                            ctypes.byref(cache), _ptr(block_tables), int(block_tables.shape[1]),
+                                            _ptr(context_lens), int(q.shape[0]), int(q.shape[1]), float(scale),
+                                            int(num_splits), int(max_context_len), _ptr(workspace), ws_bytes,
+                                            _ptr(device_error), _stream(stream)),
+           "pkv_paged_attention_decode")
+
+
+def pkv_copy_blocks(k_cache, v_cache, cache: CacheDesc, block_mapping, device_error=None, stream=None) -> None:
+    _check(lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(cache), _ptr(block_mapping),
+                                 int(block_mapping.shape[0]), _ptr(device_error), _stream(stream)),
+           "pkv_copy_blocks")
+
+
+def pkv_status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def pkv_last_error() -> str:
+    return (lib().pkv_last_error() or b"").decode()
+
+
+def pkv_abi_version() -> int:
+    return int(lib().pkv_abi_version())

@@ -1,0 +1,389 @@
+// api.cu -- the extern "C" entry points of libpkv.so: argument validation,
+// launch planning (grid, pipeline depth, workspace), TMA descriptor encoding
+// and dispatch to the kernel instantiations.  No entry point allocates,
+// frees or synchronises device memory.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "cache_ops.cuh"
+#include "decode.cuh"
+
+namespace pkv {
+
+// The kernel instantiations live in decode_{f32,bf16,fp8}.cu.
+#define PKV_EXTERN(G_, D_, KV_, QT_)                                                                        \
+    extern template cudaError_t launch_paged_decode<G_, D_, KV_, QT_>(                                       \
+        const CUtensorMap&, const CUtensorMap&, const DecodeArgs&, int, int, size_t, cudaStream_t);
+#define PKV_EXTERN_ALL(KV_, QT_)                                                                            \
+    PKV_EXTERN(1, 64, KV_, QT_) PKV_EXTERN(2, 64, KV_, QT_) PKV_EXTERN(4, 64, KV_, QT_)                      \
+    PKV_EXTERN(8, 64, KV_, QT_) PKV_EXTERN(1, 128, KV_, QT_) PKV_EXTERN(2, 128, KV_, QT_)                    \
+    PKV_EXTERN(4, 128, KV_, QT_) PKV_EXTERN(8, 128, KV_, QT_)
+PKV_EXTERN_ALL(KvF32, KvF32)
+PKV_EXTERN_ALL(KvBF16, KvBF16)
+PKV_EXTERN_ALL(KvE4M3, KvBF16)
+#undef PKV_EXTERN_ALL
+#undef PKV_EXTERN
+
+// ------------------------------------------------------------------ error detail
+
+static thread_local char g_detail[512] = "";
+
+static pkv_status fail(pkv_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static pkv_status fail(pkv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_detail, sizeof g_detail, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static pkv_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ device properties
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+static DeviceInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static pkv_status device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (g_dev[dev].sms == 0) {
+        int sms = 0, smem = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(shared memory)");
+        g_dev[dev].sms = sms;
+        g_dev[dev].smem_optin = smem;
+    }
+    *out = g_dev[dev];
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A [NB*S][Hkv][D] view of one cache tensor, box = one (block, head) tile [S][1][D].
+static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int es = c.dtype == PKV_F32 ? 4 : c.dtype == PKV_BF16 ? 2 : 1;
+    const CUtensorMapDataType dt = c.dtype == PKV_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : c.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(c.head_dim), static_cast<cuuint64_t>(c.num_kv_heads),
+                          static_cast<cuuint64_t>(c.num_blocks) * c.block_size};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(c.head_dim) * es,
+                             static_cast<cuuint64_t>(c.num_kv_heads) * c.head_dim * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(c.head_dim), 1u, static_cast<cuuint32_t>(c.block_size)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------ validation helpers
+
+static int elem_bytes(int dt) { return dt == PKV_F32 ? 4 : dt == PKV_BF16 ? 2 : dt == PKV_FP8_E4M3 ? 1 : 0; }
+
+static pkv_status check_cache(const pkv_cache_desc* c) {
+    if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+    if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->block_size <= 0 || c->head_dim <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "cache sizes must be positive (NB=%d S=%d Hkv=%d D=%d)", c->num_blocks,
+                    c->block_size, c->num_kv_heads, c->head_dim);
+    if (elem_bytes(c->dtype) == 0) return fail(PKV_ERR_INVALID_ARG, "unknown cache dtype %d", c->dtype);
+    if (c->block_size != 4 && c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
+        return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 4, 8, 16, 32)", c->block_size);
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+    if (static_cast<int64_t>(c->num_blocks) * c->block_size > INT32_MAX)
+        return fail(PKV_ERR_OUT_OF_RANGE, "num_blocks * block_size exceeds 2^31-1");
+    if (c->dtype == PKV_FP8_E4M3 &&
+        !(c->k_scale > 0.f && c->v_scale > 0.f && c->k_scale < 3.0e38f && c->v_scale < 3.0e38f))
+        return fail(PKV_ERR_INVALID_ARG, "FP8 cache needs finite positive k_scale / v_scale");
+    return PKV_OK;
+}
+
+constexpr int kWarpsMax = 8;
+
+static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D) {
+    const size_t tickets = ((static_cast<size_t>(B) * Hkv * 4 + 255) / 256) * 256;
+    const size_t W = static_cast<size_t>(sms) * kWarpsMax;
+    return tickets + W * 2 * static_cast<size_t>(G) * (D + 2) * 4;
+}
+
+template <int D, class KV, class QT>
+static cudaError_t dispatch_g(int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a, int grid,
+                              int block, size_t smem, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_paged_decode<1, D, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 2: return launch_paged_decode<2, D, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 4: return launch_paged_decode<4, D, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 8: return launch_paged_decode<8, D, KV, QT>(km, vm, a, grid, block, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class KV, class QT>
+static cudaError_t dispatch_d(int D, int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
+                              int grid, int block, size_t smem, cudaStream_t s) {
+    if (D == 64) return dispatch_g<64, KV, QT>(G, km, vm, a, grid, block, smem, s);
+    return dispatch_g<128, KV, QT>(G, km, vm, a, grid, block, smem, s);
+}
+
+}  // namespace pkv
+
+#define PKV_API extern "C" __attribute__((visibility("default")))
+
+using namespace pkv;
+
+// ------------------------------------------------------------------ entry points
+
+PKV_API const char* pkv_status_string(pkv_status st) {
+    switch (st) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_OUT_OF_RANGE: return "PKV_ERR_OUT_OF_RANGE";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    }
+    return "PKV_ERR_UNKNOWN";
+}
+
+PKV_API const char* pkv_last_error(void) { return g_detail; }
+
+PKV_API int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+PKV_API pkv_status pkv_reshape_and_cache(const void* k_new, const void* v_new, int32_t src_dtype,
+                                         const int64_t* slot_mapping, int32_t num_tokens, void* k_cache,
+                                         void* v_cache, const pkv_cache_desc* cache, int32_t* device_error,
+                                         void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d < 0", num_tokens);
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache)
+        return fail(PKV_ERR_INVALID_ARG, "null tensor pointer");
+    if (src_dtype != PKV_F32 && src_dtype != PKV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "source dtype %d (supported: f32, bf16)", src_dtype);
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "k_new, v_new and the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+        return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    const int64_t pool_slots = static_cast<int64_t>(cache->num_blocks) * cache->block_size;
+    const int row = cache->num_kv_heads * cache->head_dim;
+    cudaError_t e = launch_reshape_and_cache(k_new, v_new, src_dtype, slot_mapping, num_tokens, k_cache, v_cache,
+                                             cache->dtype, pool_slots, row, cache->k_scale, cache->v_scale,
+                                             device_error, di.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
+                                   const int64_t* block_mapping, int32_t num_pairs, int32_t* device_error,
+                                   void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d < 0", num_pairs);
+    if (num_pairs == 0) return PKV_OK;
+    if (num_pairs > (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d too large", num_pairs);
+    if (!k_cache || !v_cache || !block_mapping) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
+        return fail(PKV_ERR_INVALID_ARG, "block_mapping must be 8-byte aligned");
+    const int64_t block_bytes = static_cast<int64_t>(cache->block_size) * cache->num_kv_heads * cache->head_dim *
+                                elem_bytes(cache->dtype);
+    cudaError_t e = launch_copy_blocks(k_cache, v_cache, block_mapping, num_pairs, cache->num_blocks, block_bytes,
+                                       device_error, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32_t num_seqs,
+                                                      int32_t num_q_heads, int32_t num_splits, size_t* bytes) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (!bytes) return fail(PKV_ERR_INVALID_ARG, "bytes is NULL");
+    if (num_seqs < 0 || num_q_heads <= 0 || num_splits < 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_seqs=%d num_q_heads=%d num_splits=%d)", num_seqs,
+                    num_q_heads, num_splits);
+    if (num_q_heads % cache->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads,
+                    cache->num_kv_heads);
+    if (num_splits == 1) {
+        *bytes = 0;
+        return PKV_OK;
+    }
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    *bytes = workspace_bytes_for(di.sms, num_seqs, cache->num_kv_heads, num_q_heads / cache->num_kv_heads,
+                                 cache->head_dim);
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype, const void* k_cache,
+                                              const void* v_cache, const pkv_cache_desc* cache,
+                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                              float scale, int32_t num_splits, int32_t max_context_len,
+                                              void* workspace, size_t workspace_bytes, int32_t* device_error,
+                                              void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    const int Hkv = cache->num_kv_heads, D = cache->head_dim, S = cache->block_size;
+    if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_splits < 0 || max_context_len < 0)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "bad sizes (num_seqs=%d num_q_heads=%d max_blocks_per_seq=%d num_splits=%d max_context_len=%d)",
+                    num_seqs, num_q_heads, max_blocks_per_seq, num_splits, max_context_len);
+    if (num_q_heads % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
+    const int G = num_q_heads / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_ERR_UNSUPPORTED, "GQA group size %d (supported: 1, 2, 4, 8)", G);
+    if (num_seqs > 8192) return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > 8192", num_seqs);
+    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX)
+        return fail(PKV_ERR_OUT_OF_RANGE, "block table larger than 2^31-1 entries");
+    if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
+    const bool combo_ok = (q_dtype == PKV_F32 && cache->dtype == PKV_F32) ||
+                          (q_dtype == PKV_BF16 && (cache->dtype == PKV_BF16 || cache->dtype == PKV_FP8_E4M3));
+    if (!combo_ok)
+        return fail(PKV_ERR_UNSUPPORTED, "q dtype %d with cache dtype %d (supported: f32/f32, bf16/bf16, bf16/fp8)",
+                    q_dtype, cache->dtype);
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PKV_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "block_tables / context_lens must be 4-byte aligned");
+
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+
+    // ---- work split
+    int part_blocks;
+    if (num_splits == 0) {
+        part_blocks = 1;
+    } else if (num_splits == 1) {
+        part_blocks = 1 << 30;
+    } else {
+        const int64_t maxlen = max_context_len > 0 ? max_context_len : static_cast<int64_t>(max_blocks_per_seq) * S;
+        const int64_t mb = (maxlen + S - 1) / S;
+        part_blocks = static_cast<int>(std::max<int64_t>(1, (mb + num_splits - 1) / num_splits));
+    }
+    int32_t* tickets = nullptr;
+    float* partials = nullptr;
+    if (num_splits != 1) {
+        const size_t need = workspace_bytes_for(di.sms, num_seqs, Hkv, G, D);
+        if (!workspace || workspace_bytes < need)
+            return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                        workspace ? workspace_bytes : static_cast<size_t>(0));
+        if (!aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+        tickets = static_cast<int32_t*>(workspace);
+        const size_t tb = ((static_cast<size_t>(num_seqs) * Hkv * 4 + 255) / 256) * 256;
+        partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + tb);
+    }
+
+    // ---- shared-memory plan
+    const int kv_es = elem_bytes(cache->dtype), q_es = elem_bytes(q_dtype);
+    DecodeArgs a;
+    a.out = out;
+    a.q = q;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.tickets = tickets;
+    a.partials = partials;
+    a.err = device_error;
+    a.B = num_seqs;
+    a.Hq = num_q_heads;
+    a.Hkv = Hkv;
+    a.S = S;
+    a.MB = max_blocks_per_seq;
+    a.NB = cache->num_blocks;
+    a.part_blocks = part_blocks;
+    const float kLog2e = 1.4426950408889634f;
+    a.q_mul = scale * kLog2e * (cache->dtype == PKV_FP8_E4M3 ? cache->k_scale : 1.f);
+    a.o_mul = cache->dtype == PKV_FP8_E4M3 ? cache->v_scale : 1.f;
+    a.kv_bytes = static_cast<uint32_t>(S * D * kv_es);
+    a.q_bytes = static_cast<uint32_t>(G * D * q_es);
+    a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
+    a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
+    a.timeout_ns = 2000000000ull;
+    const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
+    int nw = kWarpsMax, depth = 0;
+    while (nw >= 1) {
+        const size_t fixed = 16 * G * 8 + G * 8 + 8 * 8;  // pbuf, abuf, up to 8 barriers
+        const size_t avail = budget > a.prefix_bytes ? budget - a.prefix_bytes : 0;
+        const size_t per_warp_avail = avail / nw;
+        depth = per_warp_avail > fixed ? static_cast<int>((per_warp_avail - fixed) / a.stage_bytes) : 0;
+        if (depth > 6) depth = 6;
+        if (depth >= 2) break;
+        nw >>= 1;
+    }
+    if (depth < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this block/head size");
+    a.depth = depth;
+    const size_t fixed = 16 * G * 8 + G * 8 + 8 * static_cast<size_t>(depth);
+    a.warp_bytes = static_cast<uint32_t>(((static_cast<size_t>(depth) * a.stage_bytes + fixed + 127) / 128) * 128);
+    const size_t smem = a.prefix_bytes + static_cast<size_t>(nw) * a.warp_bytes;
+
+    CUtensorMap km, vm;
+    if ((st = cache_tensor_map(&km, k_cache, *cache)) != PKV_OK) return st;
+    if ((st = cache_tensor_map(&vm, v_cache, *cache)) != PKV_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tickets) {
+        cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(num_seqs) * Hkv * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing split-KV counters");
+    }
+    cudaError_t e;
+    if (cache->dtype == PKV_F32)
+        e = dispatch_d<KvF32, KvF32>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+    else if (cache->dtype == PKV_BF16)
+        e = dispatch_d<KvBF16, KvBF16>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+    else
+        e = dispatch_d<KvE4M3, KvBF16>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
+    return PKV_OK;
+}

@@ -1,0 +1,726 @@
+// decode.cuh -- paged decode attention kernel (one query token per sequence).
+//
+// Method: for every (sequence s, KV head h) the kernel streams the K/V
+// blocks named by the sequence's block table ("3.3 批处理与内存管理",
+// "PagedAttention：块表": block = table[p / S], offset = p % S) and keeps the
+// online-softmax state of "从 PagedAttention 到 Chunked Prefill" §2.2:
+//   m_i = max(m_{i-1}, rowmax(S_i))
+//   l_i = e^{m_{i-1}-m_i} l_{i-1} + rowsum(e^{S_i - m_i})
+//   O_i = e^{m_{i-1}-m_i} O_{i-1} + e^{S_i - m_i} V_i          (out = O_N / l_N)
+// (the page prints a stray inverse on the O rescale factor; the recurrence
+// above is the one consistent with its l update and with exact softmax).
+// The G query heads that share KV head h are processed together, so each
+// K/V block is read from HBM once per KV head (GQA grouping).
+//
+// GB300 design:
+//  * Persistent grid, one CTA of 8 warps per SM.  Each warp is an
+//    independent worker with its own TMA pipeline of `depth` stages; a
+//    stage holds one K tile and one V tile ([S][D] each, fetched by 3-D
+//    bulk-tensor copies straight out of the [NB][S][Hkv][D] pool) plus, at
+//    the start of a segment, the G query rows (1-D bulk copy).
+//  * Work balance (split-KV): all (s, h) pairs are laid end to end, block
+//    by block; the warps get equal contiguous shares of that stream.  A
+//    pair cut by a share boundary yields partial (m, l, O) records, merged
+//    by whichever worker finishes that pair last (block-count ticket, no
+//    spinning).  `part_blocks` restricts where cuts may fall (1 = any
+//    block boundary; >= every length = never cut).
+//  * Math on CUDA cores in fp32: lanes split the head dimension (LPT lanes
+//    per token, TP tokens at a time); QK^T partial dots use packed FFMA2 and
+//    a reduce-scatter over the LPT lanes so each lane ends with one score;
+//    the row max is a warp butterfly; probabilities reach the P.V lanes
+//    through a small per-warp shared buffer.  The running max used for the
+//    exponentials is only raised when a block's max exceeds it by more than
+//    8 (log2 units), so the O rescale runs rarely; the result is the same
+//    softmax up to rounding.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// ------------------------------------------------------------------ element traits
+
+struct KvF32 {
+    static constexpr int es = 4;
+    static constexpr int code = PKV_F32;
+};
+struct KvBF16 {
+    static constexpr int es = 2;
+    static constexpr int code = PKV_BF16;
+};
+struct KvE4M3 {
+    static constexpr int es = 1;
+    static constexpr int code = PKV_FP8_E4M3;
+};
+
+// Load CH bytes of KV elements from shared memory and widen to fp32 pairs.
+template <class KV, int CH>
+__device__ __forceinline__ void load_kv_chunk(const uint8_t* p, float2 (&x)[CH / KV::es / 2]) {
+    if constexpr (KV::es == 4) {
+        static_assert(CH == 16 || CH == 8, "f32 chunk");
+        if constexpr (CH == 16) {
+            float4 v = *reinterpret_cast<const float4*>(p);
+            x[0] = make_float2(v.x, v.y);
+            x[1] = make_float2(v.z, v.w);
+        } else {
+            x[0] = *reinterpret_cast<const float2*>(p);
+        }
+    } else if constexpr (KV::es == 2) {
+        if constexpr (CH == 16) {
+            uint4 v = *reinterpret_cast<const uint4*>(p);
+            x[0] = bf16x2_to_float2(v.x);
+            x[1] = bf16x2_to_float2(v.y);
+            x[2] = bf16x2_to_float2(v.z);
+            x[3] = bf16x2_to_float2(v.w);
+        } else {
+            uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = bf16x2_to_float2(v.x);
+            x[1] = bf16x2_to_float2(v.y);
+        }
+    } else {
+        if constexpr (CH == 16) {
+            uint4 v = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xffffu));
+                x[2 * i + 1] = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
+            }
+        } else {
+            uint2 v = *reinterpret_cast<const uint2*>(p);
+            const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                x[2 * i] = e4m3x2_to_float2(static_cast<uint16_t>(w[i] & 0xffffu));
+                x[2 * i + 1] = e4m3x2_to_float2(static_cast<uint16_t>(w[i] >> 16));
+            }
+        }
+    }
+}
+
+template <class QT>
+__device__ __forceinline__ float load_q_elem(const uint8_t* base, int idx) {
+    if constexpr (QT::es == 4) {
+        return reinterpret_cast<const float*>(base)[idx];
+    } else {
+        const uint16_t b = reinterpret_cast<const uint16_t*>(base)[idx];
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+}
+
+// Store n consecutive fp32 values as QT (f32 or bf16) to global memory.
+template <class QT, int N>
+__device__ __forceinline__ void store_out(void* dst, const float (&v)[N]) {
+    if constexpr (QT::es == 4) {
+        static_assert(N % 4 == 0 || N == 2, "f32 store width");
+        if constexpr (N % 4 == 0) {
+#pragma unroll
+            for (int i = 0; i < N; i += 4)
+                reinterpret_cast<float4*>(dst)[i / 4] = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+            *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+        }
+    } else {
+        uint32_t w[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i)
+            w[i] = static_cast<uint32_t>(float_to_bf16_bits(v[2 * i])) |
+                   (static_cast<uint32_t>(float_to_bf16_bits(v[2 * i + 1])) << 16);
+        if constexpr (N / 2 == 4) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else if constexpr (N / 2 == 2) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+        } else if constexpr (N / 2 == 1) {
+            *reinterpret_cast<uint32_t*>(dst) = w[0];
+        } else {
+#pragma unroll
+            for (int i = 0; i < N / 2; i += 4)
+                reinterpret_cast<uint4*>(dst)[i / 4] = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ shape of the lane mapping
+
+template <int G, int D, class KV>
+struct DecodeShape {
+    static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token
+    static constexpr int TP = 32 / LPT;                              // tokens in flight per warp
+    static constexpr int DPL = D / LPT;                              // head dims per lane
+    static constexpr int RB = DPL * KV::es;                          // row bytes per lane
+    static constexpr int CH = RB >= 16 ? 16 : RB;                    // bytes per chunk
+    static constexpr int NCH = RB / CH;                              // chunks per lane and row
+    static constexpr int EPC = CH / KV::es;                          // elements per chunk
+    static constexpr int RMAX = 16 / TP;                             // rounds per 16-token tile
+    static constexpr int DUP = LPT / G;                              // lanes holding the same score
+    static_assert(LPT <= 32 && G <= LPT, "lane mapping");
+    static_assert(EPC % 2 == 0 && DPL % 2 == 0, "pairs");
+    static_assert(DPL == NCH * EPC, "chunking");
+};
+
+// ------------------------------------------------------------------ kernel arguments
+
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t* tickets;     // [B * Hkv], zero on entry
+    float* partials;      // [W][2][G*(D+2)]
+    int32_t* err;         // nullable
+    int B, Hq, Hkv, S, MB, NB;
+    int part_blocks;      // atoms of the work split (>= 1)
+    float q_mul;          // scale * log2(e) * k_scale
+    float o_mul;          // v_scale
+    int depth;            // pipeline stages per warp
+    uint32_t kv_bytes;    // one K (or V) tile: S * D * es
+    uint32_t q_bytes;     // G query rows: G * D * q_es
+    uint32_t stage_bytes; // 2 * kv_bytes + q_bytes, rounded to 128
+    uint32_t warp_bytes;  // per-warp shared region
+    uint32_t prefix_bytes;
+    uint64_t timeout_ns;
+};
+
+constexpr float kLazyRescale = 8.0f;   // log2 units: raise the running max only beyond this
+
+struct Meta {
+    int s, h, j, phys, vl;  // vl = valid tokens | (last block of the pair) << 8
+};
+
+__device__ __forceinline__ Meta shfl_meta(const Meta& m, int src) {
+    Meta r;
+    r.s = __shfl_sync(kFull, m.s, src);
+    r.h = __shfl_sync(kFull, m.h, src);
+    r.j = __shfl_sync(kFull, m.j, src);
+    r.phys = __shfl_sync(kFull, m.phys, src);
+    r.vl = __shfl_sync(kFull, m.vl, src);
+    return r;
+}
+
+// Largest s in [0, B) with P[s] <= key (P[0] = 0 <= key).
+__device__ __forceinline__ int find_seq(const int* P, int B, long long key) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P[mid] <= key) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// First allowed cut at or after stream position x.
+__device__ __forceinline__ long long snap_pos(const int* P, int B, int Hkv, long long T, int C, long long x) {
+    if (x >= T) return T;
+    const int s = find_seq(P, B, x / Hkv);
+    const long long base = static_cast<long long>(Hkv) * P[s];
+    const int nb = P[s + 1] - P[s];
+    const long long local = x - base;
+    const int j = static_cast<int>(local % nb);
+    if (j == 0) return x;
+    const int up = (C >= nb) ? nb : ((j + C - 1) / C) * C;
+    return x - j + (up < nb ? up : nb);
+}
+
+__device__ __forceinline__ long long worker_start(const int* P, int B, int Hkv, long long T, int C, int W,
+                                                  int w) {
+    if (w >= W) return T;
+    const long long raw = (static_cast<long long>(w) * T) / W;
+    return snap_pos(P, B, Hkv, T, C, raw);
+}
+
+// Last worker whose share starts at or before y.
+__device__ __forceinline__ int worker_of(const int* P, int B, int Hkv, long long T, int C, int W,
+                                         long long y) {
+    int lo = 0, hi = W - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (worker_start(P, B, Hkv, T, C, W, mid) <= y) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Reduce-scatter of V[0..N) over the lanes of an aligned LPT-lane group:
+// afterwards each lane holds the full sum for index lg / (LPT / G).
+template <int N, int OFF>
+__device__ __forceinline__ float reduce_scatter(float* v, int lane) {
+    if constexpr (OFF == 0) {
+        return v[0];
+    } else if constexpr (N > 1) {
+        const bool upper = (lane & OFF) != 0;
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float send = upper ? v[i] : v[i + N / 2];
+            const float keep = upper ? v[i + N / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(kFull, send, OFF);
+        }
+        return reduce_scatter<N / 2, OFF / 2>(v, lane);
+    } else {
+        v[0] += __shfl_xor_sync(kFull, v[0], OFF);
+        return reduce_scatter<1, OFF / 2>(v, lane);
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int G, int D, class KV, class QT>
+__global__ void __launch_bounds__(256, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const DecodeArgs a) {
+    using SH = DecodeShape<G, D, KV>;
+    constexpr int LPT = SH::LPT, TP = SH::TP, DPL = SH::DPL, CH = SH::CH, NCH = SH::NCH, EPC = SH::EPC;
+    constexpr int RMAX = SH::RMAX, DUP = SH::DUP;
+    constexpr int HP = DPL / 2;  // float2 pairs per lane and head
+
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NW = blockDim.x >> 5;
+    const int B = a.B, S = a.S, Hkv = a.Hkv;
+
+    // ---- 1. per-sequence block counts and their prefix sum (P[s] = blocks before s)
+    int* P = reinterpret_cast<int*>(smem);
+    {
+        const int per = (B + blockDim.x - 1) / blockDim.x;
+        const int s0 = tid * per;
+        const int s1 = min(B, s0 + per);
+        int local = 0;
+        for (int s = s0; s < s1; ++s) {
+            int L = a.context_lens[s];
+            if (L < 0 || L > a.MB * S) {
+                if (blockIdx.x == 0) raise_error(a.err, PKV_DEVERR_BAD_LENGTH);
+                L = 0;
+            }
+            local += (L + S - 1) / S;
+        }
+        // exclusive scan of `local` over the CTA
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __shared__ int warp_tot[32];
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int wbase = 0;
+        for (int i = 0; i < warp; ++i) wbase += warp_tot[i];
+        int run = wbase + incl - local;
+        for (int s = s0; s < s1; ++s) {
+            P[s] = run;
+            int L = a.context_lens[s];
+            if (L < 0 || L > a.MB * S) L = 0;
+            run += (L + S - 1) / S;
+        }
+        if (tid == blockDim.x - 1) {
+            int tot = 0;
+            for (int i = 0; i < NW; ++i) tot += warp_tot[i];
+            P[B] = tot;
+        }
+        __syncthreads();
+    }
+
+    // ---- 2. empty sequences get zero rows (spread over the CTAs)
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        if (P[s + 1] != P[s]) continue;
+        const int n = a.Hq * D;
+        for (int i = tid; i < n; i += blockDim.x) {
+            if constexpr (QT::es == 4)
+                reinterpret_cast<float*>(a.out)[static_cast<size_t>(s) * n + i] = 0.f;
+            else
+                reinterpret_cast<uint16_t*>(a.out)[static_cast<size_t>(s) * n + i] = 0;
+        }
+    }
+
+    // ---- 3. this warp's shared region and barriers
+    uint8_t* wreg = smem + a.prefix_bytes + static_cast<size_t>(warp) * a.warp_bytes;
+    float2* pbuf = reinterpret_cast<float2*>(wreg + static_cast<size_t>(a.depth) * a.stage_bytes);
+    float2* abuf = pbuf + 16 * G;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(abuf + G);
+    if (lane == 0) {
+        for (int i = 0; i < a.depth; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const long long T = static_cast<long long>(Hkv) * P[B];
+    const int W = gridDim.x * NW;
+    const int w = blockIdx.x * NW + warp;
+    const int C = a.part_blocks;
+    const long long A0 = worker_start(P, B, Hkv, T, C, W, w);
+    const long long A1 = worker_start(P, B, Hkv, T, C, W, w + 1);
+    if (A0 >= A1) return;
+    if (lane == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    const uint64_t pol = policy_evict_first();
+
+    const int tp = lane / LPT, lg = lane % LPT;
+    const int gl = lg / DUP;  // the query head whose score this lane holds
+
+    // Stream position -> (s, h, j, physical block, valid tokens) for this lane.
+    auto make_meta = [&](long long x) -> Meta {
+        Meta m;
+        if (x >= A1) {
+            m.s = 0; m.h = 0; m.j = 0; m.phys = -1; m.vl = 0;
+            return m;
+        }
+        const int s = find_seq(P, B, x / Hkv);
+        const long long local = x - static_cast<long long>(Hkv) * P[s];
+        const int nb = P[s + 1] - P[s];
+        const int h = static_cast<int>(local / nb);
+        const int j = static_cast<int>(local - static_cast<long long>(h) * nb);
+        const int L = a.context_lens[s];
+        m.s = s; m.h = h; m.j = j;
+        m.phys = a.block_tables[static_cast<size_t>(s) * a.MB + j];
+        const int valid = min(S, L - j * S);
+        m.vl = valid | ((j == nb - 1) ? 256 : 0);
+        return m;
+    };
+
+    auto stage_ptr = [&](int st) -> uint8_t* { return wreg + static_cast<size_t>(st) * a.stage_bytes; };
+
+    // Issue the copies of stream index k (position A0 + k) into stage k % depth.
+    auto issue = [&](long long k, const Meta& m) {
+        const int st = static_cast<int>(k % a.depth);
+        if (lane == 0) {
+            const bool seg_start = (m.j == 0) || (k == 0);
+            const bool ok = (m.phys >= 0 && m.phys < a.NB);
+            if (!ok) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
+            const uint32_t tx = (ok ? 2u * a.kv_bytes : 0u) + (seg_start ? a.q_bytes : 0u);
+            const uint32_t bar = smem_u32(&bars[st]);
+            uint8_t* dst = stage_ptr(st);
+            if (tx) mbar_arrive_expect_tx(bar, tx); else mbar_arrive(bar);
+            if (ok) {
+                tma_load_3d(smem_u32(dst), &kmap, 0, m.h, m.phys * S, bar, pol);
+                tma_load_3d(smem_u32(dst + a.kv_bytes), &vmap, 0, m.h, m.phys * S, bar, pol);
+            }
+            if (seg_start) {
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) +
+                                     (static_cast<size_t>(m.s) * a.Hq + static_cast<size_t>(m.h) * G) * D * QT::es;
+                bulk_load(smem_u32(dst + 2 * a.kv_bytes), src, a.q_bytes, bar);
+            }
+        }
+    };
+
+    const long long n_blocks = A1 - A0;
+    long long wbase = A0;
+    Meta cur = make_meta(wbase + lane);
+    Meta nxt = make_meta(wbase + 32 + lane);
+
+    // prologue: fill the pipeline
+    {
+        const long long pre = n_blocks < a.depth ? n_blocks : a.depth;
+        for (long long k = 0; k < pre; ++k) issue(k, shfl_meta(cur, static_cast<int>(k)));
+    }
+
+    // Meta of stream index k (never below the window base); slides the window.
+    auto meta_at = [&](long long k) -> Meta {
+        const long long x = A0 + k;
+        if (x - wbase >= 32) {
+            wbase += 32;
+            cur = nxt;
+            nxt = make_meta(wbase + 32 + lane);
+        }
+        return shfl_meta(cur, static_cast<int>(x - wbase));
+    };
+
+    // Bounded wait for stage k; on timeout record the error and drain the
+    // copies still in flight (also bounded) so the warp can leave safely.
+    auto wait_stage = [&](long long k) -> bool {
+        const int st = static_cast<int>(k % a.depth);
+        if (mbar_wait_bounded(smem_u32(&bars[st]), static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
+            return true;
+        raise_error(a.err, PKV_DEVERR_TIMEOUT);
+        for (long long kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
+            mbar_wait_bounded(smem_u32(&bars[kk % a.depth]), static_cast<uint32_t>((kk / a.depth) & 1),
+                              a.timeout_ns);
+        return false;
+    };
+
+    const int TS = S < 16 ? S : 16;  // tokens per softmax tile
+    const int R = TS / TP;           // rounds per tile
+
+    long long k = 0;
+    while (k < n_blocks) {
+        // ------------------------------------------------ one segment: blocks of one (s, h) pair
+        Meta m = meta_at(k);
+        const long long seg_x0 = A0 + k;
+        const int seg_j0 = m.j;
+        float2 q2[G][HP];
+        float2 o2[G][HP];
+        float m_ref = -INFINITY;  // running max of head gl (log2 units), warp-uniform per head
+        float l_run = 0.f;        // this lane's share of the running sum of head gl
+        bool first = true;
+        long long x_last;
+        while (true) {
+            const long long x = A0 + k;
+            if (!first) m = meta_at(k);
+            if (!wait_stage(k)) return;
+            const uint8_t* sp = stage_ptr(static_cast<int>(k % a.depth));
+            if (first) {
+                const uint8_t* qs = sp + 2 * a.kv_bytes;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                        for (int e = 0; e < EPC; e += 2) {
+                            const int d = (c * LPT + lg) * EPC + e;
+                            q2[g][(c * EPC + e) / 2] = make_float2(load_q_elem<QT>(qs, g * D + d) * a.q_mul,
+                                                                   load_q_elem<QT>(qs, g * D + d + 1) * a.q_mul);
+                            o2[g][(c * EPC + e) / 2] = make_float2(0.f, 0.f);
+                        }
+                first = false;
+            }
+            if (m.phys >= 0 && m.phys < a.NB) {
+                const int valid = m.vl & 0xff;
+                for (int t0 = 0; t0 < S && t0 < valid; t0 += TS) {
+                    const int tv = valid - t0;  // valid tokens from t0 on
+                    const uint8_t* Ks = sp + static_cast<size_t>(t0) * D * KV::es;
+                    const uint8_t* Vs = sp + a.kv_bytes + static_cast<size_t>(t0) * D * KV::es;
+                    // ---- scores of this tile
+                    float sr[RMAX];
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) {
+                        sr[r] = -INFINITY;
+                        if (r < R) {
+                            const int t = r * TP + tp;
+                            float2 acc[G];
+#pragma unroll
+                            for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                float2 kx[EPC / 2];
+                                load_kv_chunk<KV, CH>(Ks + static_cast<size_t>(t) * D * KV::es + (c * LPT + lg) * CH,
+                                                      kx);
+#pragma unroll
+                                for (int e = 0; e < EPC / 2; ++e)
+#pragma unroll
+                                    for (int g = 0; g < G; ++g)
+                                        acc[g] = __ffma2_rn(q2[g][c * (EPC / 2) + e], kx[e], acc[g]);
+                            }
+                            float v[G];
+#pragma unroll
+                            for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
+                            const float sc = reduce_scatter<G, LPT / 2>(v, lane);
+                            sr[r] = (t < tv) ? sc : -INFINITY;
+                        }
+                    }
+                    // ---- tile max over all tokens (butterfly over the token groups)
+                    float mb = sr[0];
+#pragma unroll
+                    for (int r = 1; r < RMAX; ++r) mb = fmaxf(mb, sr[r]);
+#pragma unroll
+                    for (int o = LPT; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+                    const bool need = mb > m_ref + kLazyRescale;
+                    if (__any_sync(kFull, need)) {
+                        const float m_new = need ? mb : m_ref;
+                        const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
+                        l_run *= alpha;
+                        m_ref = m_new;
+                        if (tp == 0 && (lg % DUP) == 0) abuf[gl] = make_float2(alpha, alpha);
+                        __syncwarp();
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float2 al = abuf[g];
+#pragma unroll
+                            for (int i = 0; i < HP; ++i) o2[g][i] = __fmul2_rn(o2[g][i], al);
+                        }
+                    }
+                    // ---- probabilities (relative to the running max)
+                    float lsum = 0.f;
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) {
+                        if (r < R) {
+                            const float p = (sr[r] == -INFINITY) ? 0.f : exp2f(sr[r] - m_ref);
+                            lsum += p;
+                            if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
+                        }
+                    }
+                    l_run += lsum;
+                    __syncwarp();
+                    // ---- P.V
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) {
+                        const int t = r * TP + tp;
+                        if (r < R && t < tv) {
+                            float2 pp[G];
+#pragma unroll
+                            for (int g = 0; g < G; ++g) pp[g] = pbuf[t * G + g];
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                float2 vx[EPC / 2];
+                                load_kv_chunk<KV, CH>(Vs + static_cast<size_t>(t) * D * KV::es + (c * LPT + lg) * CH,
+                                                      vx);
+#pragma unroll
+                                for (int e = 0; e < EPC / 2; ++e)
+#pragma unroll
+                                    for (int g = 0; g < G; ++g)
+                                        o2[g][c * (EPC / 2) + e] = __ffma2_rn(pp[g], vx[e], o2[g][c * (EPC / 2) + e]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                }
+            }
+            __syncwarp();
+
+            // ---- refill this stage with stream index k + depth
+            const long long kn = k + a.depth;
+            if (kn < n_blocks) {
+                const int src = static_cast<int>(A0 + kn - wbase);
+                const Meta m0 = shfl_meta(cur, src & 31);
+                const Meta m1 = shfl_meta(nxt, src & 31);
+                fence_proxy_async_smem();
+                issue(kn, (src < 32) ? m0 : m1);
+            }
+            const bool last = (m.vl & 256) != 0 || x == A1 - 1;
+            ++k;
+            if (last) {
+                x_last = x;
+                break;
+            }
+        }
+
+        // ------------------------------------------------ end of segment
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int i = 0; i < HP; ++i) {
+                    o2[g][i].x += __shfl_xor_sync(kFull, o2[g][i].x, o);
+                    o2[g][i].y += __shfl_xor_sync(kFull, o2[g][i].y, o);
+                }
+            l_run += __shfl_xor_sync(kFull, l_run, o);
+        }
+        const int s = m.s, h = m.h;
+        const int nb = P[s + 1] - P[s];
+        const bool whole = (seg_j0 == 0) && (x_last - seg_x0 + 1 == nb);
+        if (whole) {
+            float l_all[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) l_all[g] = __shfl_sync(kFull, l_run, g * DUP);
+            if (tp == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float inv = (l_all[g] > 0.f) ? a.o_mul / l_all[g] : 0.f;
+                    uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                                    (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        float v[EPC];
+#pragma unroll
+                        for (int e = 0; e < EPC / 2; ++e) {
+                            v[2 * e] = o2[g][c * (EPC / 2) + e].x * inv;
+                            v[2 * e + 1] = o2[g][c * (EPC / 2) + e].y * inv;
+                        }
+                        store_out<QT, EPC>(orow + static_cast<size_t>((c * LPT + lg) * EPC) * QT::es, v);
+                    }
+                }
+            }
+            continue;
+        }
+        // partial record of this segment: O[G][D], m[G], l[G]
+        const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
+        {
+            const int slot = (seg_x0 == A0) ? 0 : 1;
+            float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
+            if (tp == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                        for (int e = 0; e < EPC / 2; ++e)
+                            *reinterpret_cast<float2*>(rec + g * D + (c * LPT + lg) * EPC + 2 * e) =
+                                o2[g][c * (EPC / 2) + e];
+            }
+            if (tp == 0 && (lg % DUP) == 0) {
+                rec[G * D + gl] = m_ref;
+                rec[G * D + G + gl] = l_run;
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        const int seg_blocks = static_cast<int>(x_last - seg_x0 + 1);
+        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], seg_blocks);
+        old = __shfl_sync(kFull, old, 0);
+        if (old + seg_blocks != nb) continue;
+
+        // last finisher of pair (s, h): merge its segments in stream order
+        __threadfence();
+        const long long U0 = static_cast<long long>(Hkv) * P[s] + static_cast<long long>(h) * nb;
+        const long long U1 = U0 + nb;
+        float Mx[G], Ls[G];
+        float2 acc[G][HP];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            Mx[g] = -INFINITY;
+            Ls[g] = 0.f;
+#pragma unroll
+            for (int i = 0; i < HP; ++i) acc[g][i] = make_float2(0.f, 0.f);
+        }
+        long long y = U0;
+        int guard = 0;
+        while (y < U1 && guard++ <= W) {
+            const int wq = worker_of(P, B, Hkv, T, C, W, y);
+            const long long aq = worker_start(P, B, Hkv, T, C, W, wq);
+            const int sl = (aq == y) ? 0 : 1;
+            const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float mr = __ldcg(r + G * D + g);
+                const float lr = __ldcg(r + G * D + G + g);
+                const float mn = fmaxf(Mx[g], mr);
+                const float fo = (Mx[g] == -INFINITY) ? 0.f : exp2f(Mx[g] - mn);
+                const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mn);
+                Ls[g] = Ls[g] * fo + lr * fr;
+                Mx[g] = mn;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+#pragma unroll
+                    for (int e = 0; e < EPC / 2; ++e) {
+                        const float2 ov =
+                            __ldcg(reinterpret_cast<const float2*>(r + g * D + (c * LPT + lg) * EPC + 2 * e));
+                        float2& ac = acc[g][c * (EPC / 2) + e];
+                        ac.x = ac.x * fo + ov.x * fr;
+                        ac.y = ac.y * fo + ov.y * fr;
+                    }
+            }
+            y = worker_start(P, B, Hkv, T, C, W, wq + 1);
+        }
+        if (tp == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float inv = (Ls[g] > 0.f) ? a.o_mul / Ls[g] : 0.f;
+                uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                                (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    float v[EPC];
+#pragma unroll
+                    for (int e = 0; e < EPC / 2; ++e) {
+                        v[2 * e] = acc[g][c * (EPC / 2) + e].x * inv;
+                        v[2 * e + 1] = acc[g][c * (EPC / 2) + e].y * inv;
+                    }
+                    store_out<QT, EPC>(orow + static_cast<size_t>((c * LPT + lg) * EPC) * QT::es, v);
+                }
+            }
+        }
+    }
+}
+
+// Host-side launch for one instantiation (defined in the per-dtype .cu files).
+template <int G, int D, class KV, class QT>
+cudaError_t launch_paged_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,
+                                int block, size_t smem, cudaStream_t stream) {
+    auto kern = paged_decode_kernel<G, D, KV, QT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, block, smem, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

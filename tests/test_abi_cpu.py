@@ -1,0 +1,79 @@
+"""The C ABI without a GPU: the library loads, exports what include/pkv.h declares,
+and its host-side argument checks reject bad calls before touching a device."""
+import ctypes
+
+import pytest
+
+import paged_kv_cache_71_gb300 as pkv
+from paged_kv_cache_71_gb300 import _binding as B
+
+
+def test_library_exports_every_declared_entry_point():
+    names = pkv.declared_entry_points()
+    assert {"pkv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_copy_blocks",
+            "pkv_paged_attention_workspace_size", "pkv_status_string"} <= set(names)
+    L = pkv.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version():
+    assert pkv.pkv_abi_version() == 1
+    for code, name in B.STATUS_NAMES.items():
+        assert pkv.pkv_status_string(code) == name
+    assert pkv.pkv_status_string(99) == "PKV_ERR_UNKNOWN"
+
+
+def _desc(**kw):
+    d = dict(num_blocks=16, block_size=16, num_kv_heads=8, head_dim=128, dtype=B.PKV_BF16, k_scale=1.0, v_scale=1.0)
+    d.update(kw)
+    return B.CacheDesc(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), 2), (dict(block_size=12), 2), (dict(block_size=64), 2), (dict(num_blocks=0), 1),
+    (dict(dtype=7), 1), (dict(dtype=B.PKV_FP8_E4M3, k_scale=0.0), 1), (dict(num_kv_heads=-1), 1),
+])
+def test_cache_descriptor_checks(kw, status):
+    L = pkv.lib()
+    out = ctypes.c_size_t(0)
+    st = L.pkv_paged_attention_workspace_size(ctypes.byref(_desc(**kw)), 4, 32, 0, ctypes.byref(out))
+    assert st == status, pkv.pkv_last_error()
+    assert pkv.pkv_last_error()
+
+
+def test_decode_host_checks_before_any_device_work():
+    L = pkv.lib()
+    d = _desc()
+    args = lambda **o: dict(dict(out=16, q=16, q_dtype=B.PKV_BF16, k=16, v=16, bt=16, mb=4, cl=16, B=2, Hq=32,
+                                 scale=0.1, splits=1, maxlen=0, ws=None, wsb=0), **o)
+
+    def call(a):
+        return L.pkv_paged_attention_decode(a["out"], a["q"], a["q_dtype"], a["k"], a["v"], ctypes.byref(d), a["bt"],
+                                            a["mb"], a["cl"], a["B"], a["Hq"], a["scale"], a["splits"], a["maxlen"],
+                                            a["ws"], a["wsb"], None, None)
+    assert call(args(Hq=30)) == 1            # not a multiple of Hkv
+    assert call(args(Hq=8 * 3)) == 2         # G = 3
+    assert call(args(Hq=8 * 16)) == 2        # G = 16
+    assert call(args(q_dtype=B.PKV_F32)) == 2  # f32 q with bf16 cache
+    assert call(args(B=-1)) == 1
+    assert call(args(mb=0)) == 1
+    assert call(args(out=None)) == 1
+    assert call(args(q=24)) == 1             # misaligned
+    assert call(args(scale=float("nan"))) == 1
+    assert call(args(B=9000)) == 2
+    assert call(args(B=0)) == 0              # empty batch is a no-op
+
+
+def test_reshape_and_copy_host_checks():
+    L = pkv.lib()
+    d = _desc()
+    assert L.pkv_reshape_and_cache(16, 16, B.PKV_BF16, 16, -1, 16, 16, ctypes.byref(d), None, None) == 1
+    assert L.pkv_reshape_and_cache(16, 16, B.PKV_BF16, 16, 0, 16, 16, ctypes.byref(d), None, None) == 0
+    assert L.pkv_reshape_and_cache(16, 16, B.PKV_FP8_E4M3, 16, 4, 16, 16, ctypes.byref(d), None, None) == 2
+    assert L.pkv_reshape_and_cache(16, 17, B.PKV_BF16, 16, 4, 16, 16, ctypes.byref(d), None, None) == 1
+    assert L.pkv_reshape_and_cache(16, 16, B.PKV_BF16, 12, 4, 16, 16, ctypes.byref(d), None, None) == 1
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 16, -2, None, None) == 1
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 16, 0, None, None) == 0
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 12, 3, None, None) == 1
+    assert L.pkv_copy_blocks(None, 16, ctypes.byref(d), 16, 3, None, None) == 1

@@ -1,0 +1,193 @@
+"""GPU parity of paged decode attention against the fp64 oracle.
+
+Small cases are compared in full; the full-size batches in the launch
+configuration the benchmark times are compared on sampled sequences that
+include the longest and the shortest.  Tolerances are in parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_71_gb300 as pkv
+from paged_kv_cache_71_gb300 import _binding as B
+from paged_kv_cache_71_gb300 import workload as wl
+from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
+
+from parity import assert_close, host_bits, oracle_step, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, num_splits=0):
+    st = DeviceStep(w, num_splits=num_splits)
+    st.step()
+    torch.cuda.synchronize()
+    return st
+
+
+def _random_workload(lens, Hq, Hkv, D, S, kv, q, seed, extra_blocks=7):
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, np.int64)
+    need = int(sum(-(-int(L) // S) for L in lens))
+    NB = need + extra_blocks
+    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    slots = []
+    for s, L in enumerate(lens):
+        alloc.add_seq(s, int(L) - 1)
+        slots.append(alloc.append_token(s))
+    k_cache = wl.random_values(rng, (NB, S, Hkv, D), kv)
+    v_cache = wl.random_values(rng, (NB, S, Hkv, D), kv)
+    qa = wl.random_values(rng, (len(lens), Hq, D), q)
+    kn = wl.random_values(rng, (len(lens), Hkv, D), q)
+    vn = wl.random_values(rng, (len(lens), Hkv, D), q)
+    sc = wl.FP8_SCALE if kv == "e4m3" else 1.0
+    return wl.Workload("random", seed, Hq, Hkv, D, S, kv, q, sc, sc, qa, k_cache, v_cache,
+                       alloc.padded_tables(list(range(len(lens)))), lens.astype(np.int32), kn, vn,
+                       np.array(slots, np.int64), np.zeros((0, 2), np.int64))
+
+
+def test_tiny_config_all_split_modes():
+    w = wl.tiny()
+    kc, vc, ref = oracle_step(w)
+    for ns in (0, 1, 2, 3, 9):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        np.testing.assert_array_equal(host_bits(st.k_cache), kc)
+        assert_close("f32", to_host(st.out), ref, f"tiny splits={ns}")
+
+
+LENS = [1, 3, 4, 5, 15, 16, 17, 31, 33, 64, 100, 257]
+
+
+@pytest.mark.parametrize("kv,q", [("f32", "f32"), ("bf16", "bf16"), ("e4m3", "bf16")])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("D", [64, 128])
+def test_decode_shapes(kv, q, G, D):
+    S = 16 if D == 128 else 8
+    Hkv = 2
+    w = _random_workload(LENS, G * Hkv, Hkv, D, S, kv, q, seed=G * 1000 + D)
+    _, _, ref = oracle_step(w)
+    for ns in (0, 1, 3):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        assert_close(kv, to_host(st.out), ref, f"G={G} D={D} {kv} splits={ns}")
+
+
+@pytest.mark.parametrize("S", [4, 8, 16, 32])
+def test_decode_block_sizes(S):
+    w = _random_workload([1, S - 1, S, S + 1, 3 * S + 2, 10 * S, 200], 8, 2, 128, S, "bf16", "bf16", seed=S)
+    _, _, ref = oracle_step(w)
+    for ns in (0, 1, 4):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        assert_close("bf16", to_host(st.out), ref, f"S={S} splits={ns}")
+
+
+def test_split_modes_agree_closely():
+    """Any split gives the same attention up to fp32 rounding order."""
+    w = _random_workload([700, 1, 2048, 333, 5000], 16, 4, 64, 16, "f32", "f32", seed=77)
+    outs = [to_host(_run(w, ns).out) for ns in (0, 1, 2, 7, 64)]
+    for o in outs[1:]:
+        np.testing.assert_allclose(o, outs[0], rtol=0, atol=2e-6)
+
+
+def test_empty_sequence_gives_zero_row():
+    w = _random_workload([5, 9, 33], 8, 2, 128, 16, "bf16", "bf16", seed=3)
+    w.context_lens = w.context_lens.copy()
+    w.context_lens[1] = 0
+    w.slot_mapping = w.slot_mapping.copy()
+    w.slot_mapping[1] = -1
+    _, _, ref = oracle_step(w)
+    for ns in (0, 1):
+        st = _run(w, ns)
+        out = to_host(st.out)
+        assert (out[1] == 0).all()
+        assert_close("bf16", out, ref, "empty row")
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_poisoned_unused_slots_do_not_leak(kv):
+    """NaN in every slot that no sequence owns (tails of last blocks, free blocks) changes nothing."""
+    q = "f32" if kv == "f32" else "bf16"
+    w = _random_workload([13, 2, 40, 77], 8, 2, 64, 8, kv, q, seed=21, extra_blocks=12)
+    _, _, ref = oracle_step(w)
+    clean = to_host(_run(w, 0).out)
+    S = w.block_size
+    owned = np.zeros((w.num_blocks, S), bool)
+    for s in range(w.num_seqs):
+        for p in range(int(w.context_lens[s])):
+            owned[w.block_tables[s, p // S], p % S] = True
+    nan = np.float32(np.nan) if kv == "f32" else np.uint16(0x7FC0)
+    for cache in (w.k_cache, w.v_cache):
+        cache[~owned] = nan
+    for ns in (0, 1, 2):
+        out = to_host(_run(w, ns).out)
+        assert np.isfinite(out).all()
+        assert_close(kv, out, ref, f"poisoned splits={ns}")
+        if ns == 0:
+            np.testing.assert_array_equal(out, clean)
+
+
+def test_bad_block_id_and_bad_length_are_flagged():
+    w = _random_workload([20, 20, 20, 20], 8, 2, 64, 4, "f32", "f32", seed=31)
+    w.block_tables = w.block_tables.copy()
+    w.block_tables[1, 2] = w.num_blocks + 5        # bad id inside sequence 1's context
+    w.context_lens = w.context_lens.copy()
+    w.context_lens[2] = w.block_tables.shape[1] * w.block_size + 1  # longer than its table
+    st = _run(w, 1)
+    e = st.device_error()
+    assert e & B.DEVERR_BAD_BLOCK and e & B.DEVERR_BAD_LENGTH
+    out = to_host(st.out)
+    good = [0, 3]
+    _, _, ref = oracle_step(w, seqs=good)
+    assert_close("f32", out[good], ref, "sequences next to bad ones")
+    assert (out[2] == 0).all()
+
+
+def test_workspace_and_alignment_errors():
+    w = _random_workload([10, 20], 8, 2, 64, 8, "bf16", "bf16", seed=4)
+    st = DeviceStep(w, num_splits=0)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_attention_decode(st.out, st.q, st.k_cache, st.v_cache, st.cache, st.block_tables,
+                                       st.context_lens, w.scale, 0, 0, st.workspace[:16], st.err)
+    assert ei.value.status == 4
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_attention_decode(st.out, st.q, st.k_cache, st.v_cache, st.cache, st.block_tables,
+                                       st.context_lens, w.scale, 0, 0, None, st.err)
+    assert ei.value.status == 4
+    assert pkv.pkv_paged_attention_workspace_size(st.cache, 2, 8, 1) == 0
+
+
+# ---------------------------------------------------------------- the benchmark's batches
+
+def _sample(w, k=24, seed=0):
+    rng = np.random.default_rng(seed)
+    L = w.context_lens
+    pick = {int(np.argmax(L)), int(np.argmin(L))}
+    pick |= set(rng.choice(w.num_seqs, size=min(k, w.num_seqs), replace=False).tolist())
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("name", ["llama2_7b", "llama3_8b_gqa", "prefix_shared", "llama70b_mixed_bf16",
+                                  "llama70b_mixed_fp8"])
+def test_full_size_batches_sampled(name):
+    w = wl.make(name)
+    seqs = _sample(w)
+    kc, vc, ref = oracle_step(w, seqs=seqs)
+    st = _run(w, 0)
+    assert st.device_error() == 0
+    out = to_host(st.out)
+    assert_close(w.kv_dtype, out[seqs], ref, name)
+    # the cache write is bit-exact for every new token
+    gk = host_bits(st.k_cache)
+    S = w.block_size
+    for i, sl in enumerate(w.slot_mapping):
+        np.testing.assert_array_equal(gk[sl // S, sl % S], kc[sl // S, sl % S])
+    # the output is finite everywhere, and a split-free run agrees on every sequence
+    assert np.isfinite(out).all()
+    st1 = _run(w, 1)
+    o1 = to_host(st1.out)
+    assert np.abs(o1 - out).max() < (6e-2 if w.kv_dtype == "e4m3" else 2e-2)
