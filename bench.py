@@ -171,6 +171,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama3_8b_gqa")
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="smaller batch of the Llama-3-8B workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -193,8 +194,10 @@ def main():
     from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
 
     # every rank serves its own batch (sequences shard across GPUs; no exchange)
-    w = wl.make(args.config, seed=wl.CONFIG_SEEDS[args.config] + 1000 * rank) if args.config != "llama70b_mixed_fp8" \
-        else wl.make(args.config)
+    kw = {"seed": wl.CONFIG_SEEDS[args.config] + 1000 * rank} if args.config != "llama70b_mixed_fp8" else {}
+    if args.batch and args.config == "llama3_8b_gqa":
+        kw["batch"] = args.batch
+    w = wl.make(args.config, **kw)
     st = DeviceStep(w, num_splits=args.num_splits)
     stream = torch.cuda.current_stream()
     launches_per_step = 2 + (1 if st.copy_pairs is not None else 0)
