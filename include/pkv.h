@@ -163,6 +163,40 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
                            const int64_t* block_mapping, int32_t num_pairs,
                            int32_t* device_error, void* stream);
 
+/*
+ * Paged decode attention for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is an interface convenience.
+ *
+ * pkv_paged_attention_decode needs a caller-provided workspace whenever it
+ * splits the work (num_splits != 1).  Some callers cannot provide one: code
+ * that may not call cudaMalloc once its memory plan is fixed, hosts that
+ * own every device allocation and expose no allocator to plugins, or
+ * language runtimes that reach this library only through plain C.  This
+ * entry point computes the same result as pkv_paged_attention_decode
+ * (same arguments minus the workspace) but keeps the split-KV scratch in a
+ * static device array of PKV_STATIC_SCRATCH_BYTES that the library owns.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine.  The array occupies PKV_STATIC_SCRATCH_BYTES on every
+ *     GPU that loads the library, until the process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first
+ *     call before any stream capture.
+ *   - A batch whose scratch need (pkv_paged_attention_workspace_size) is
+ *     above PKV_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE
+ *     before anything is launched; num_splits == 1 needs no scratch.
+ *   - Every call shares the one array.  Each call clears the completion
+ *     counters it needs; the partial records keep the last call's contents.
+ *     Calls whose work overlaps on the GPU (different streams or host
+ *     threads without ordering between them) race on the array and give
+ *     wrong results: serialise them.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (12u * 1024u * 1024u)
+pkv_status pkv_paged_attention_decode_static_scratch(
+    void* out, const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+    const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+    int32_t num_splits, int32_t max_context_len, int32_t* device_error, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* pkv_status_string(pkv_status status);
 

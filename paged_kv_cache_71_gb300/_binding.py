@@ -64,8 +64,10 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_attention_workspace_size.argtypes = [D, i32, i32, i32, ctypes.POINTER(sz)]
     L.pkv_paged_attention_decode.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32, P, sz, P, P]
     L.pkv_copy_blocks.argtypes = [P, P, D, P, i32, P, P]
+    L.pkv_paged_attention_decode_static_scratch.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32,
+                                                            P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
-                 "pkv_copy_blocks"):
+                 "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch"):
         getattr(L, name).restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -137,6 +139,20 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, cache: CacheDesc, block
                                             int(num_splits), int(max_context_len), _ptr(workspace), ws_bytes,
                                             _ptr(device_error), _stream(stream)),
            "pkv_paged_attention_decode")
+
+
+def pkv_paged_attention_decode_static_scratch(out, q, k_cache, v_cache, cache: CacheDesc, block_tables,
+                                              context_lens, scale: float, num_splits: int = 0,
+                                              max_context_len: int = 0, device_error=None, stream=None) -> None:
+    """pkv_paged_attention_decode without a workspace argument: the library's static scratch is used."""
+    _check(lib().pkv_paged_attention_decode_static_scratch(
+        _ptr(out), _ptr(q), _dtype(q), _ptr(k_cache), _ptr(v_cache), ctypes.byref(cache), _ptr(block_tables),
+        int(block_tables.shape[1]), _ptr(context_lens), int(q.shape[0]), int(q.shape[1]), float(scale),
+        int(num_splits), int(max_context_len), _ptr(device_error), _stream(stream)),
+        "pkv_paged_attention_decode_static_scratch")
+
+
+STATIC_SCRATCH_BYTES = 12 * 1024 * 1024  # PKV_STATIC_SCRATCH_BYTES in include/pkv.h
 
 
 def pkv_copy_blocks(k_cache, v_cache, cache: CacheDesc, block_mapping, device_error=None, stream=None) -> None:

@@ -40,6 +40,8 @@ static pkv_status fail(pkv_status st, const char* fmt, ...) {
     return st;
 }
 
+void set_last_error(const char* msg) { snprintf(g_detail, sizeof g_detail, "%s", msg); }
+
 static pkv_status cuda_fail(cudaError_t e, const char* what) {
     return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
