@@ -13,18 +13,21 @@
 
 namespace pkv {
 
-// The kernel instantiations live in decode_{f32,bf16,fp8}.cu.
-#define PKV_EXTERN(G_, D_, KV_, QT_)                                                                        \
-    extern template cudaError_t launch_paged_decode<G_, D_, KV_, QT_>(                                       \
+// The kernel instantiations live in decode_{f32,bf16,fp8}_s{4,8,16,32}.cu.
+#define PKV_EXTERN(G_, D_, S_, KV_, QT_)                                                                    \
+    extern template cudaError_t launch_paged_decode<G_, D_, S_, KV_, QT_>(                                   \
         const CUtensorMap&, const CUtensorMap&, const DecodeArgs&, int, int, size_t, cudaStream_t);
+#define PKV_EXTERN_GD(S_, KV_, QT_)                                                                         \
+    PKV_EXTERN(1, 64, S_, KV_, QT_) PKV_EXTERN(2, 64, S_, KV_, QT_) PKV_EXTERN(4, 64, S_, KV_, QT_)          \
+    PKV_EXTERN(8, 64, S_, KV_, QT_) PKV_EXTERN(1, 128, S_, KV_, QT_) PKV_EXTERN(2, 128, S_, KV_, QT_)        \
+    PKV_EXTERN(4, 128, S_, KV_, QT_) PKV_EXTERN(8, 128, S_, KV_, QT_)
 #define PKV_EXTERN_ALL(KV_, QT_)                                                                            \
-    PKV_EXTERN(1, 64, KV_, QT_) PKV_EXTERN(2, 64, KV_, QT_) PKV_EXTERN(4, 64, KV_, QT_)                      \
-    PKV_EXTERN(8, 64, KV_, QT_) PKV_EXTERN(1, 128, KV_, QT_) PKV_EXTERN(2, 128, KV_, QT_)                    \
-    PKV_EXTERN(4, 128, KV_, QT_) PKV_EXTERN(8, 128, KV_, QT_)
+    PKV_EXTERN_GD(4, KV_, QT_) PKV_EXTERN_GD(8, KV_, QT_) PKV_EXTERN_GD(16, KV_, QT_) PKV_EXTERN_GD(32, KV_, QT_)
 PKV_EXTERN_ALL(KvF32, KvF32)
 PKV_EXTERN_ALL(KvBF16, KvBF16)
 PKV_EXTERN_ALL(KvE4M3, KvBF16)
 #undef PKV_EXTERN_ALL
+#undef PKV_EXTERN_GD
 #undef PKV_EXTERN
 
 // ------------------------------------------------------------------ error detail
@@ -148,23 +151,35 @@ static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D) {
     return tickets + W * 2 * static_cast<size_t>(G) * (D + 2) * 4;
 }
 
-template <int D, class KV, class QT>
+template <int D, int S, class KV, class QT>
 static cudaError_t dispatch_g(int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a, int grid,
                               int block, size_t smem, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_paged_decode<1, D, KV, QT>(km, vm, a, grid, block, smem, s);
-        case 2: return launch_paged_decode<2, D, KV, QT>(km, vm, a, grid, block, smem, s);
-        case 4: return launch_paged_decode<4, D, KV, QT>(km, vm, a, grid, block, smem, s);
-        case 8: return launch_paged_decode<8, D, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 1: return launch_paged_decode<1, D, S, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 2: return launch_paged_decode<2, D, S, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 4: return launch_paged_decode<4, D, S, KV, QT>(km, vm, a, grid, block, smem, s);
+        case 8: return launch_paged_decode<8, D, S, KV, QT>(km, vm, a, grid, block, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <class KV, class QT>
+template <int S, class KV, class QT>
 static cudaError_t dispatch_d(int D, int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
                               int grid, int block, size_t smem, cudaStream_t s) {
-    if (D == 64) return dispatch_g<64, KV, QT>(G, km, vm, a, grid, block, smem, s);
-    return dispatch_g<128, KV, QT>(G, km, vm, a, grid, block, smem, s);
+    if (D == 64) return dispatch_g<64, S, KV, QT>(G, km, vm, a, grid, block, smem, s);
+    return dispatch_g<128, S, KV, QT>(G, km, vm, a, grid, block, smem, s);
+}
+
+template <class KV, class QT>
+static cudaError_t dispatch_s(int S, int D, int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
+                              int grid, int block, size_t smem, cudaStream_t s) {
+    switch (S) {
+        case 4: return dispatch_d<4, KV, QT>(D, G, km, vm, a, grid, block, smem, s);
+        case 8: return dispatch_d<8, KV, QT>(D, G, km, vm, a, grid, block, smem, s);
+        case 16: return dispatch_d<16, KV, QT>(D, G, km, vm, a, grid, block, smem, s);
+        case 32: return dispatch_d<32, KV, QT>(D, G, km, vm, a, grid, block, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pkv
@@ -285,6 +300,7 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return fail(PKV_ERR_UNSUPPORTED, "GQA group size %d (supported: 1, 2, 4, 8)", G);
     if (num_seqs > 8192) return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > 8192", num_seqs);
+    if (Hkv > 1024) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d > 1024", Hkv);
     if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX)
         return fail(PKV_ERR_OUT_OF_RANGE, "block table larger than 2^31-1 entries");
     if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
@@ -381,11 +397,11 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     }
     cudaError_t e;
     if (cache->dtype == PKV_F32)
-        e = dispatch_d<KvF32, KvF32>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+        e = dispatch_s<KvF32, KvF32>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     else if (cache->dtype == PKV_BF16)
-        e = dispatch_d<KvBF16, KvBF16>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+        e = dispatch_s<KvBF16, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     else
-        e = dispatch_d<KvE4M3, KvBF16>(D, G, km, vm, a, di.sms, nw * 32, smem, s);
+        e = dispatch_s<KvE4M3, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
     return PKV_OK;
 }

@@ -151,7 +151,6 @@ struct DecodeShape {
     static constexpr int CH = RB >= 16 ? 16 : RB;                    // bytes per chunk
     static constexpr int NCH = RB / CH;                              // chunks per lane and row
     static constexpr int EPC = CH / KV::es;                          // elements per chunk
-    static constexpr int RMAX = 16 / TP;                             // rounds per 16-token tile
     static constexpr int DUP = LPT / G;                              // lanes holding the same score
     static_assert(LPT <= 32 && G <= LPT, "lane mapping");
     static_assert(EPC % 2 == 0 && DPL % 2 == 0, "pairs");
@@ -182,20 +181,6 @@ struct DecodeArgs {
 };
 
 constexpr float kLazyRescale = 8.0f;   // log2 units: raise the running max only beyond this
-
-struct Meta {
-    int s, h, j, phys, vl;  // vl = valid tokens | (last block of the pair) << 8
-};
-
-__device__ __forceinline__ Meta shfl_meta(const Meta& m, int src) {
-    Meta r;
-    r.s = __shfl_sync(kFull, m.s, src);
-    r.h = __shfl_sync(kFull, m.h, src);
-    r.j = __shfl_sync(kFull, m.j, src);
-    r.phys = __shfl_sync(kFull, m.phys, src);
-    r.vl = __shfl_sync(kFull, m.vl, src);
-    return r;
-}
 
 // Largest s in [0, B) with P[s] <= key (P[0] = 0 <= key).
 __device__ __forceinline__ int find_seq(const int* P, int B, long long key) {
@@ -261,20 +246,35 @@ __device__ __forceinline__ float reduce_scatter(float* v, int lane) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int G, int D, class KV, class QT>
+// Packed per-block metadata, one block of the worker's stream per lane.
+//   a = s * 1024 + h            (sequence, KV head)
+//   b = physical block id
+//   c = valid tokens | first << 6 (block 0 of its pair) | last << 7 (last block of its pair)
+//       | ok << 8 (block id in range)
+struct Meta {
+    int a, b, c;
+};
+constexpr int kMetaFirst = 1 << 6, kMetaLast = 1 << 7, kMetaOk = 1 << 8;
+
+template <int G, int D, int S, class KV, class QT>
 __global__ void __launch_bounds__(256, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeArgs a) {
     using SH = DecodeShape<G, D, KV>;
     constexpr int LPT = SH::LPT, TP = SH::TP, DPL = SH::DPL, CH = SH::CH, NCH = SH::NCH, EPC = SH::EPC;
-    constexpr int RMAX = SH::RMAX, DUP = SH::DUP;
-    constexpr int HP = DPL / 2;  // float2 pairs per lane and head
+    constexpr int DUP = SH::DUP;
+    constexpr int HP = DPL / 2;              // float2 pairs per lane and head
+    constexpr int TS = S < 16 ? S : 16;      // tokens per softmax tile
+    constexpr int NT = S / TS;               // tiles per block
+    constexpr int R = TS / TP;               // rounds per tile
+    constexpr int ROW = D * KV::es;          // bytes of one token row of one head
+    static_assert(TS % TP == 0 && S % TS == 0, "tiling");
 
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int NW = blockDim.x >> 5;
-    const int B = a.B, S = a.S, Hkv = a.Hkv;
+    const int B = a.B, Hkv = a.Hkv;
 
     // ---- 1. per-sequence block counts and their prefix sum (P[s] = blocks before s)
     int* P = reinterpret_cast<int*>(smem);
@@ -291,7 +291,6 @@ __global__ void __launch_bounds__(256, 1)
             }
             local += (L + S - 1) / S;
         }
-        // exclusive scan of `local` over the CTA
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -330,13 +329,15 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
 
-    // ---- 3. this warp's shared region and barriers
+    // ---- 3. this warp's shared region, barriers and share of the work stream
     uint8_t* wreg = smem + a.prefix_bytes + static_cast<size_t>(warp) * a.warp_bytes;
     float2* pbuf = reinterpret_cast<float2*>(wreg + static_cast<size_t>(a.depth) * a.stage_bytes);
     float2* abuf = pbuf + 16 * G;
     uint64_t* bars = reinterpret_cast<uint64_t*>(abuf + G);
+    const uint32_t wreg_u32 = smem_u32(wreg);
+    const uint32_t bars_u32 = smem_u32(bars);
     if (lane == 0) {
-        for (int i = 0; i < a.depth; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 0; i < a.depth; ++i) mbar_init(bars_u32 + 8 * i, 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -357,48 +358,44 @@ __global__ void __launch_bounds__(256, 1)
     const int tp = lane / LPT, lg = lane % LPT;
     const int gl = lg / DUP;  // the query head whose score this lane holds
 
-    // Stream position -> (s, h, j, physical block, valid tokens) for this lane.
+    // Stream position x -> packed metadata (computed by the lane that owns x).
     auto make_meta = [&](long long x) -> Meta {
-        Meta m;
-        if (x >= A1) {
-            m.s = 0; m.h = 0; m.j = 0; m.phys = -1; m.vl = 0;
-            return m;
-        }
+        Meta m{0, -1, 0};
+        if (x >= A1) return m;
         const int s = find_seq(P, B, x / Hkv);
         const long long local = x - static_cast<long long>(Hkv) * P[s];
         const int nb = P[s + 1] - P[s];
         const int h = static_cast<int>(local / nb);
         const int j = static_cast<int>(local - static_cast<long long>(h) * nb);
         const int L = a.context_lens[s];
-        m.s = s; m.h = h; m.j = j;
-        m.phys = a.block_tables[static_cast<size_t>(s) * a.MB + j];
+        m.a = s * 1024 + h;
+        m.b = a.block_tables[static_cast<size_t>(s) * a.MB + j];
         const int valid = min(S, L - j * S);
-        m.vl = valid | ((j == nb - 1) ? 256 : 0);
+        m.c = valid | (j == 0 ? kMetaFirst : 0) | (j == nb - 1 ? kMetaLast : 0) |
+              ((m.b >= 0 && m.b < a.NB) ? kMetaOk : 0);
         return m;
     };
 
-    auto stage_ptr = [&](int st) -> uint8_t* { return wreg + static_cast<size_t>(st) * a.stage_bytes; };
-
     // Issue the copies of stream index k (position A0 + k) into stage k % depth.
+    // Called by the one lane that holds the block's metadata.
     auto issue = [&](long long k, const Meta& m) {
         const int st = static_cast<int>(k % a.depth);
-        if (lane == 0) {
-            const bool seg_start = (m.j == 0) || (k == 0);
-            const bool ok = (m.phys >= 0 && m.phys < a.NB);
-            if (!ok) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
-            const uint32_t tx = (ok ? 2u * a.kv_bytes : 0u) + (seg_start ? a.q_bytes : 0u);
-            const uint32_t bar = smem_u32(&bars[st]);
-            uint8_t* dst = stage_ptr(st);
-            if (tx) mbar_arrive_expect_tx(bar, tx); else mbar_arrive(bar);
-            if (ok) {
-                tma_load_3d(smem_u32(dst), &kmap, 0, m.h, m.phys * S, bar, pol);
-                tma_load_3d(smem_u32(dst + a.kv_bytes), &vmap, 0, m.h, m.phys * S, bar, pol);
-            }
-            if (seg_start) {
-                const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) +
-                                     (static_cast<size_t>(m.s) * a.Hq + static_cast<size_t>(m.h) * G) * D * QT::es;
-                bulk_load(smem_u32(dst + 2 * a.kv_bytes), src, a.q_bytes, bar);
-            }
+        const bool seg_start = (m.c & kMetaFirst) || (k == 0);
+        const bool ok = (m.c & kMetaOk) != 0;
+        if (!ok) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
+        const uint32_t tx = (ok ? 2u * a.kv_bytes : 0u) + (seg_start ? a.q_bytes : 0u);
+        const uint32_t bar = bars_u32 + 8 * st;
+        const uint32_t dst = wreg_u32 + st * a.stage_bytes;
+        if (tx) mbar_arrive_expect_tx(bar, tx); else mbar_arrive(bar);
+        const int s = m.a >> 10, h = m.a & 1023;
+        if (ok) {
+            tma_load_3d(dst, &kmap, 0, h, m.b * S, bar, pol);
+            tma_load_3d(dst + a.kv_bytes, &vmap, 0, h, m.b * S, bar, pol);
+        }
+        if (seg_start) {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) +
+                                 (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G) * D * QT::es;
+            bulk_load(dst + 2 * a.kv_bytes, src, a.q_bytes, bar);
         }
     };
 
@@ -407,57 +404,50 @@ __global__ void __launch_bounds__(256, 1)
     Meta cur = make_meta(wbase + lane);
     Meta nxt = make_meta(wbase + 32 + lane);
 
-    // prologue: fill the pipeline
-    {
-        const long long pre = n_blocks < a.depth ? n_blocks : a.depth;
-        for (long long k = 0; k < pre; ++k) issue(k, shfl_meta(cur, static_cast<int>(k)));
+    // prologue: fill the pipeline (lane k issues stream index k)
+    if (lane < a.depth && lane < n_blocks) {
+        fence_proxy_async_smem();
+        issue(lane, cur);
     }
-
-    // Meta of stream index k (never below the window base); slides the window.
-    auto meta_at = [&](long long k) -> Meta {
-        const long long x = A0 + k;
-        if (x - wbase >= 32) {
-            wbase += 32;
-            cur = nxt;
-            nxt = make_meta(wbase + 32 + lane);
-        }
-        return shfl_meta(cur, static_cast<int>(x - wbase));
-    };
 
     // Bounded wait for stage k; on timeout record the error and drain the
     // copies still in flight (also bounded) so the warp can leave safely.
     auto wait_stage = [&](long long k) -> bool {
         const int st = static_cast<int>(k % a.depth);
-        if (mbar_wait_bounded(smem_u32(&bars[st]), static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
+        if (mbar_wait_bounded(bars_u32 + 8 * st, static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
             return true;
         raise_error(a.err, PKV_DEVERR_TIMEOUT);
         for (long long kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
-            mbar_wait_bounded(smem_u32(&bars[kk % a.depth]), static_cast<uint32_t>((kk / a.depth) & 1),
-                              a.timeout_ns);
+            mbar_wait_bounded(bars_u32 + 8 * static_cast<int>(kk % a.depth),
+                              static_cast<uint32_t>((kk / a.depth) & 1), a.timeout_ns);
         return false;
     };
 
-    const int TS = S < 16 ? S : 16;  // tokens per softmax tile
-    const int R = TS / TP;           // rounds per tile
-
     long long k = 0;
     while (k < n_blocks) {
-        // ------------------------------------------------ one segment: blocks of one (s, h) pair
-        Meta m = meta_at(k);
+        // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
         const long long seg_x0 = A0 + k;
-        const int seg_j0 = m.j;
         float2 q2[G][HP];
         float2 o2[G][HP];
-        float m_ref = -INFINITY;  // running max of head gl (log2 units), warp-uniform per head
+        float m_ref = -INFINITY;  // running max of head gl (log2 units), uniform over lanes holding gl
         float l_run = 0.f;        // this lane's share of the running sum of head gl
+        int ma = 0, mc = 0, seg_first = 0;
         bool first = true;
         long long x_last;
         while (true) {
             const long long x = A0 + k;
-            if (!first) m = meta_at(k);
+            if (x - wbase >= 32) {
+                wbase += 32;
+                cur = nxt;
+                nxt = make_meta(wbase + 32 + lane);
+            }
+            const int src = static_cast<int>(x - wbase);
+            ma = __shfl_sync(kFull, cur.a, src);
+            mc = __shfl_sync(kFull, cur.c, src);
             if (!wait_stage(k)) return;
-            const uint8_t* sp = stage_ptr(static_cast<int>(k % a.depth));
+            const uint8_t* sp = wreg + static_cast<size_t>(k % a.depth) * a.stage_bytes;
             if (first) {
+                seg_first = mc & kMetaFirst;
                 const uint8_t* qs = sp + 2 * a.kv_bytes;
 #pragma unroll
                 for (int g = 0; g < G; ++g)
@@ -472,44 +462,43 @@ __global__ void __launch_bounds__(256, 1)
                         }
                 first = false;
             }
-            if (m.phys >= 0 && m.phys < a.NB) {
-                const int valid = m.vl & 0xff;
-                for (int t0 = 0; t0 < S && t0 < valid; t0 += TS) {
-                    const int tv = valid - t0;  // valid tokens from t0 on
-                    const uint8_t* Ks = sp + static_cast<size_t>(t0) * D * KV::es;
-                    const uint8_t* Vs = sp + a.kv_bytes + static_cast<size_t>(t0) * D * KV::es;
+            if (mc & kMetaOk) {
+                const int valid = mc & 63;
+#pragma unroll
+                for (int ti = 0; ti < NT; ++ti) {
+                    const int tv = valid - ti * TS;  // valid tokens from this tile on
+                    if (tv <= 0) break;
+                    const uint8_t* Ks = sp + ti * TS * ROW + (lg * CH);
+                    const uint8_t* Vs = sp + a.kv_bytes + ti * TS * ROW + (lg * CH);
+                    const bool full = tv >= TS;
                     // ---- scores of this tile
-                    float sr[RMAX];
+                    float sr[R];
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
-                        sr[r] = -INFINITY;
-                        if (r < R) {
-                            const int t = r * TP + tp;
-                            float2 acc[G];
+                    for (int r = 0; r < R; ++r) {
+                        const int t = r * TP + tp;
+                        float2 acc[G];
 #pragma unroll
-                            for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+                        for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
 #pragma unroll
-                            for (int c = 0; c < NCH; ++c) {
-                                float2 kx[EPC / 2];
-                                load_kv_chunk<KV, CH>(Ks + static_cast<size_t>(t) * D * KV::es + (c * LPT + lg) * CH,
-                                                      kx);
+                        for (int c = 0; c < NCH; ++c) {
+                            float2 kx[EPC / 2];
+                            load_kv_chunk<KV, CH>(Ks + t * ROW + c * LPT * CH, kx);
 #pragma unroll
-                                for (int e = 0; e < EPC / 2; ++e)
+                            for (int e = 0; e < EPC / 2; ++e)
 #pragma unroll
-                                    for (int g = 0; g < G; ++g)
-                                        acc[g] = __ffma2_rn(q2[g][c * (EPC / 2) + e], kx[e], acc[g]);
-                            }
-                            float v[G];
-#pragma unroll
-                            for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
-                            const float sc = reduce_scatter<G, LPT / 2>(v, lane);
-                            sr[r] = (t < tv) ? sc : -INFINITY;
+                                for (int g = 0; g < G; ++g)
+                                    acc[g] = __ffma2_rn(q2[g][c * (EPC / 2) + e], kx[e], acc[g]);
                         }
+                        float v[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
+                        const float sc = reduce_scatter<G, LPT / 2>(v, lane);
+                        sr[r] = (full || t < tv) ? sc : -INFINITY;
                     }
                     // ---- tile max over all tokens (butterfly over the token groups)
                     float mb = sr[0];
 #pragma unroll
-                    for (int r = 1; r < RMAX; ++r) mb = fmaxf(mb, sr[r]);
+                    for (int r = 1; r < R; ++r) mb = fmaxf(mb, sr[r]);
 #pragma unroll
                     for (int o = LPT; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
                     const bool need = mb > m_ref + kLazyRescale;
@@ -527,31 +516,28 @@ __global__ void __launch_bounds__(256, 1)
                             for (int i = 0; i < HP; ++i) o2[g][i] = __fmul2_rn(o2[g][i], al);
                         }
                     }
-                    // ---- probabilities (relative to the running max)
+                    // ---- probabilities relative to the running max
                     float lsum = 0.f;
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
-                        if (r < R) {
-                            const float p = (sr[r] == -INFINITY) ? 0.f : exp2f(sr[r] - m_ref);
-                            lsum += p;
-                            if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
-                        }
+                    for (int r = 0; r < R; ++r) {
+                        const float p = (full || sr[r] != -INFINITY) ? exp2f(sr[r] - m_ref) : 0.f;
+                        lsum += p;
+                        if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
                     }
                     l_run += lsum;
                     __syncwarp();
                     // ---- P.V
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
+                    for (int r = 0; r < R; ++r) {
                         const int t = r * TP + tp;
-                        if (r < R && t < tv) {
+                        if (full || t < tv) {
                             float2 pp[G];
 #pragma unroll
                             for (int g = 0; g < G; ++g) pp[g] = pbuf[t * G + g];
 #pragma unroll
                             for (int c = 0; c < NCH; ++c) {
                                 float2 vx[EPC / 2];
-                                load_kv_chunk<KV, CH>(Vs + static_cast<size_t>(t) * D * KV::es + (c * LPT + lg) * CH,
-                                                      vx);
+                                load_kv_chunk<KV, CH>(Vs + t * ROW + c * LPT * CH, vx);
 #pragma unroll
                                 for (int e = 0; e < EPC / 2; ++e)
 #pragma unroll
@@ -565,16 +551,16 @@ __global__ void __launch_bounds__(256, 1)
             }
             __syncwarp();
 
-            // ---- refill this stage with stream index k + depth
+            // ---- refill this stage with stream index k + depth (issued by the lane holding its metadata)
             const long long kn = k + a.depth;
             if (kn < n_blocks) {
-                const int src = static_cast<int>(A0 + kn - wbase);
-                const Meta m0 = shfl_meta(cur, src & 31);
-                const Meta m1 = shfl_meta(nxt, src & 31);
-                fence_proxy_async_smem();
-                issue(kn, (src < 32) ? m0 : m1);
+                const int sn = static_cast<int>(A0 + kn - wbase);
+                if (lane == (sn & 31)) {
+                    fence_proxy_async_smem();
+                    issue(kn, sn < 32 ? cur : nxt);
+                }
             }
-            const bool last = (m.vl & 256) != 0 || x == A1 - 1;
+            const bool last = (mc & kMetaLast) != 0 || x == A1 - 1;
             ++k;
             if (last) {
                 x_last = x;
@@ -594,9 +580,9 @@ __global__ void __launch_bounds__(256, 1)
                 }
             l_run += __shfl_xor_sync(kFull, l_run, o);
         }
-        const int s = m.s, h = m.h;
+        const int s = ma >> 10, h = ma & 1023;
         const int nb = P[s + 1] - P[s];
-        const bool whole = (seg_j0 == 0) && (x_last - seg_x0 + 1 == nb);
+        const bool whole = seg_first && (mc & kMetaLast) && (x_last - seg_x0 + 1 == nb);
         if (whole) {
             float l_all[G];
 #pragma unroll
@@ -713,10 +699,10 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // Host-side launch for one instantiation (defined in the per-dtype .cu files).
-template <int G, int D, class KV, class QT>
+template <int G, int D, int S, class KV, class QT>
 cudaError_t launch_paged_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,
                                 int block, size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_kernel<G, D, KV, QT>;
+    auto kern = paged_decode_kernel<G, D, S, KV, QT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, block, smem, stream>>>(kmap, vmap, a);

@@ -1,0 +1,21 @@
+// decode_f32_s32.cu -- paged decode kernel instantiations for an fp32 K/V cache with fp32 queries,
+// block size 32.  (One file per cache dtype and block size, so that the
+// instantiations compile in parallel.)
+#include "decode.cuh"
+
+namespace pkv {
+
+#define PKV_INST(G_, D_)                                                                                     \
+    template cudaError_t launch_paged_decode<G_, D_, 32, KvF32, KvF32>(                                       \
+        const CUtensorMap&, const CUtensorMap&, const DecodeArgs&, int, int, size_t, cudaStream_t);
+PKV_INST(1, 64)
+PKV_INST(2, 64)
+PKV_INST(4, 64)
+PKV_INST(8, 64)
+PKV_INST(1, 128)
+PKV_INST(2, 128)
+PKV_INST(4, 128)
+PKV_INST(8, 128)
+#undef PKV_INST
+
+}  // namespace pkv
