@@ -143,11 +143,24 @@ static pkv_status check_cache(const pkv_cache_desc* c) {
     return PKV_OK;
 }
 
-constexpr int kWarpsMax = 8;
+static int policy_warps(int G, int D) {
+    switch (G * 1000 + D) {
+        case 1064: return DecodePolicy<1, 64>::warps;
+        case 2064: return DecodePolicy<2, 64>::warps;
+        case 4064: return DecodePolicy<4, 64>::warps;
+        case 8064: return DecodePolicy<8, 64>::warps;
+        case 1128: return DecodePolicy<1, 128>::warps;
+        case 2128: return DecodePolicy<2, 128>::warps;
+        case 4128: return DecodePolicy<4, 128>::warps;
+        default: return DecodePolicy<8, 128>::warps;
+    }
+}
 
+// Split-KV scratch: one completion counter per (sequence, KV head), then two
+// partial (O[G][D], m[G], l[G]) records per worker warp.
 static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D) {
     const size_t tickets = ((static_cast<size_t>(B) * Hkv * 4 + 255) / 256) * 256;
-    const size_t W = static_cast<size_t>(sms) * kWarpsMax;
+    const size_t W = static_cast<size_t>(sms) * policy_warps(G, D);
     return tickets + W * 2 * static_cast<size_t>(G) * (D + 2) * 4;
 }
 
@@ -370,7 +383,7 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
     a.timeout_ns = 2000000000ull;
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
-    int nw = kWarpsMax, depth = 0;
+    int nw = policy_warps(G, D), depth = 0;
     while (nw >= 1) {
         const size_t fixed = 16 * G * 8 + G * 8 + 8 * 8;  // pbuf, abuf, up to 8 barriers
         const size_t avail = budget > a.prefix_bytes ? budget - a.prefix_bytes : 0;

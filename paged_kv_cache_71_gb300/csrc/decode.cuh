@@ -34,6 +34,8 @@
 //    softmax up to rounding.
 #pragma once
 
+#include <type_traits>
+
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -142,9 +144,29 @@ __device__ __forceinline__ void store_out(void* dst, const float (&v)[N]) {
 
 // ------------------------------------------------------------------ shape of the lane mapping
 
+// Launch policy per instantiation, chosen from measurements on GB300: the
+// kernel is bound by instruction issue, so it trades query/accumulator
+// registers (more lanes per token) for more resident warps when the GQA
+// group is small, and keeps 8 warps with 64 query registers per lane for
+// G * D >= 1024, where the extra reductions would cost more than the warps
+// gain.  PKV_DECODE_QREGS / PKV_DECODE_WARPS override both (experiments).
+template <int G, int D>
+struct DecodePolicy {
+#ifdef PKV_DECODE_QREGS
+    static constexpr int qregs = PKV_DECODE_QREGS;
+#else
+    static constexpr int qregs = (G * D <= 512) ? 32 : 64;
+#endif
+#ifdef PKV_DECODE_WARPS
+    static constexpr int warps = PKV_DECODE_WARPS;
+#else
+    static constexpr int warps = (qregs <= 32) ? 12 : 8;
+#endif
+};
+
 template <int G, int D, class KV>
 struct DecodeShape {
-    static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token
+    static constexpr int LPT = (G * D / DecodePolicy<G, D>::qregs > 8) ? G * D / DecodePolicy<G, D>::qregs : 8;  // lanes per token
     static constexpr int TP = 32 / LPT;                              // tokens in flight per warp
     static constexpr int DPL = D / LPT;                              // head dims per lane
     static constexpr int RB = DPL * KV::es;                          // row bytes per lane
@@ -257,7 +279,7 @@ struct Meta {
 constexpr int kMetaFirst = 1 << 6, kMetaLast = 1 << 7, kMetaOk = 1 << 8;
 
 template <int G, int D, int S, class KV, class QT>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const DecodeArgs a) {
     using SH = DecodeShape<G, D, KV>;
@@ -434,6 +456,88 @@ __global__ void __launch_bounds__(256, 1)
         int ma = 0, mc = 0, seg_first = 0;
         bool first = true;
         long long x_last;
+            // One softmax tile (TS tokens) of the block in this stage; M = some tokens are past the end.
+            auto tile = [&](auto masked, const uint8_t* sp, int ti, int tv) {
+                constexpr bool M = decltype(masked)::value;
+                    const uint8_t* Ks = sp + ti * TS * ROW + (lg * CH);
+                    const uint8_t* Vs = sp + a.kv_bytes + ti * TS * ROW + (lg * CH);
+                    // ---- scores of this tile
+                    float sr[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const int t = r * TP + tp;
+                        float2 acc[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            float2 kx[EPC / 2];
+                            load_kv_chunk<KV, CH>(Ks + t * ROW + c * LPT * CH, kx);
+#pragma unroll
+                            for (int e = 0; e < EPC / 2; ++e)
+#pragma unroll
+                                for (int g = 0; g < G; ++g)
+                                    acc[g] = __ffma2_rn(q2[g][c * (EPC / 2) + e], kx[e], acc[g]);
+                        }
+                        float v[G];
+#pragma unroll
+                        for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
+                        const float sc = reduce_scatter<G, LPT / 2>(v, lane);
+                        sr[r] = (!M || t < tv) ? sc : -INFINITY;
+                    }
+                    // ---- tile max over all tokens (butterfly over the token groups)
+                    float mb = sr[0];
+#pragma unroll
+                    for (int r = 1; r < R; ++r) mb = fmaxf(mb, sr[r]);
+#pragma unroll
+                    for (int o = LPT; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+                    const bool need = mb > m_ref + kLazyRescale;
+                    if (__any_sync(kFull, need)) {
+                        const float m_new = need ? mb : m_ref;
+                        const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
+                        l_run *= alpha;
+                        m_ref = m_new;
+                        if (tp == 0 && (lg % DUP) == 0) abuf[gl] = make_float2(alpha, alpha);
+                        __syncwarp();
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float2 al = abuf[g];
+#pragma unroll
+                            for (int i = 0; i < HP; ++i) o2[g][i] = __fmul2_rn(o2[g][i], al);
+                        }
+                    }
+                    // ---- probabilities relative to the running max
+                    float lsum = 0.f;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float p = (!M || sr[r] != -INFINITY) ? exp2f(sr[r] - m_ref) : 0.f;
+                        lsum += p;
+                        if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
+                    }
+                    l_run += lsum;
+                    __syncwarp();
+                    // ---- P.V
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const int t = r * TP + tp;
+                        if (!M || t < tv) {
+                            float2 pp[G];
+#pragma unroll
+                            for (int g = 0; g < G; ++g) pp[g] = pbuf[t * G + g];
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                float2 vx[EPC / 2];
+                                load_kv_chunk<KV, CH>(Vs + t * ROW + c * LPT * CH, vx);
+#pragma unroll
+                                for (int e = 0; e < EPC / 2; ++e)
+#pragma unroll
+                                    for (int g = 0; g < G; ++g)
+                                        o2[g][c * (EPC / 2) + e] = __ffma2_rn(pp[g], vx[e], o2[g][c * (EPC / 2) + e]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+            };
         while (true) {
             const long long x = A0 + k;
             if (x - wbase >= 32) {
@@ -464,89 +568,17 @@ __global__ void __launch_bounds__(256, 1)
             }
             if (mc & kMetaOk) {
                 const int valid = mc & 63;
+                if (valid == S) {
 #pragma unroll
-                for (int ti = 0; ti < NT; ++ti) {
-                    const int tv = valid - ti * TS;  // valid tokens from this tile on
-                    if (tv <= 0) break;
-                    const uint8_t* Ks = sp + ti * TS * ROW + (lg * CH);
-                    const uint8_t* Vs = sp + a.kv_bytes + ti * TS * ROW + (lg * CH);
-                    const bool full = tv >= TS;
-                    // ---- scores of this tile
-                    float sr[R];
+                    for (int ti = 0; ti < NT; ++ti) tile(std::false_type{}, sp, ti, TS);
+                } else {
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int t = r * TP + tp;
-                        float2 acc[G];
-#pragma unroll
-                        for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int c = 0; c < NCH; ++c) {
-                            float2 kx[EPC / 2];
-                            load_kv_chunk<KV, CH>(Ks + t * ROW + c * LPT * CH, kx);
-#pragma unroll
-                            for (int e = 0; e < EPC / 2; ++e)
-#pragma unroll
-                                for (int g = 0; g < G; ++g)
-                                    acc[g] = __ffma2_rn(q2[g][c * (EPC / 2) + e], kx[e], acc[g]);
-                        }
-                        float v[G];
-#pragma unroll
-                        for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
-                        const float sc = reduce_scatter<G, LPT / 2>(v, lane);
-                        sr[r] = (full || t < tv) ? sc : -INFINITY;
+                    for (int ti = 0; ti < NT; ++ti) {
+                        const int tv = valid - ti * TS;
+                        if (tv <= 0) break;
+                        if (tv >= TS) tile(std::false_type{}, sp, ti, TS);
+                        else tile(std::true_type{}, sp, ti, tv);
                     }
-                    // ---- tile max over all tokens (butterfly over the token groups)
-                    float mb = sr[0];
-#pragma unroll
-                    for (int r = 1; r < R; ++r) mb = fmaxf(mb, sr[r]);
-#pragma unroll
-                    for (int o = LPT; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
-                    const bool need = mb > m_ref + kLazyRescale;
-                    if (__any_sync(kFull, need)) {
-                        const float m_new = need ? mb : m_ref;
-                        const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
-                        l_run *= alpha;
-                        m_ref = m_new;
-                        if (tp == 0 && (lg % DUP) == 0) abuf[gl] = make_float2(alpha, alpha);
-                        __syncwarp();
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float2 al = abuf[g];
-#pragma unroll
-                            for (int i = 0; i < HP; ++i) o2[g][i] = __fmul2_rn(o2[g][i], al);
-                        }
-                    }
-                    // ---- probabilities relative to the running max
-                    float lsum = 0.f;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float p = (full || sr[r] != -INFINITY) ? exp2f(sr[r] - m_ref) : 0.f;
-                        lsum += p;
-                        if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
-                    }
-                    l_run += lsum;
-                    __syncwarp();
-                    // ---- P.V
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const int t = r * TP + tp;
-                        if (full || t < tv) {
-                            float2 pp[G];
-#pragma unroll
-                            for (int g = 0; g < G; ++g) pp[g] = pbuf[t * G + g];
-#pragma unroll
-                            for (int c = 0; c < NCH; ++c) {
-                                float2 vx[EPC / 2];
-                                load_kv_chunk<KV, CH>(Vs + t * ROW + c * LPT * CH, vx);
-#pragma unroll
-                                for (int e = 0; e < EPC / 2; ++e)
-#pragma unroll
-                                    for (int g = 0; g < G; ++g)
-                                        o2[g][c * (EPC / 2) + e] = __ffma2_rn(pp[g], vx[e], o2[g][c * (EPC / 2) + e]);
-                            }
-                        }
-                    }
-                    __syncwarp();
                 }
             }
             __syncwarp();
