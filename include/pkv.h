@@ -148,6 +148,25 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
                                       void* stream);
 
 /*
+ * One chunk of a chunked prefill ("3.3 批处理与内存管理", section "分块预填充":
+ * the chunk's queries attend to a KV cache that already holds the earlier
+ * chunks).  The chunk's own K/V must already be written (pkv_reshape_and_cache),
+ * so kv_len >= q_start_pos + num_q_tokens.  Query token i (position
+ * q_start_pos + i) and query head hq (KV head hq / G) attend causally:
+ *   out[i][hq] = softmax(scale * q[i][hq] . K[0 .. q_start_pos + i]^T) V[0 .. q_start_pos + i]
+ * with K/V gathered through block_table (one sequence, ceil(kv_len / S)
+ * entries).  Runs on the tensor cores: bf16 inputs, fp32 accumulation, the
+ * softmax weights rounded to bf16 for the P.V product.
+ *   q, out: [num_q_tokens][num_q_heads][128] bf16.
+ * Supported: bf16 queries and cache, head_dim 128, block_size 8/16/32,
+ *   G = num_q_heads / num_kv_heads dividing 128.  No workspace.
+ */
+pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,
+                                   int32_t q_start_pos, const void* k_cache, const void* v_cache,
+                                   const pkv_cache_desc* cache, const int32_t* block_table, int32_t kv_len,
+                                   int32_t num_q_heads, float scale, int32_t* device_error, void* stream);
+
+/*
  * Copy whole physical blocks, for copy-on-write of shared blocks
  * ("3.3 批处理与内存管理", section "共享与写时复制": before a sequence writes
  * into a block whose reference count is above one, the engine copies the

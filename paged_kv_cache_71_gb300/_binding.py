@@ -66,8 +66,9 @@ def lib() -> ctypes.CDLL:
     L.pkv_copy_blocks.argtypes = [P, P, D, P, i32, P, P]
     L.pkv_paged_attention_decode_static_scratch.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32,
                                                             P, P]
+    L.pkv_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, D, P, i32, i32, f32, P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
-                 "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch"):
+                 "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch", "pkv_paged_prefill_chunk"):
         getattr(L, name).restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -150,6 +151,15 @@ def pkv_paged_attention_decode_static_scratch(out, q, k_cache, v_cache, cache: C
         int(block_tables.shape[1]), _ptr(context_lens), int(q.shape[0]), int(q.shape[1]), float(scale),
         int(num_splits), int(max_context_len), _ptr(device_error), _stream(stream)),
         "pkv_paged_attention_decode_static_scratch")
+
+
+def pkv_paged_prefill_chunk(out, q, q_start: int, k_cache, v_cache, cache: CacheDesc, block_table, kv_len: int,
+                            scale: float, device_error=None, stream=None) -> None:
+    _check(lib().pkv_paged_prefill_chunk(_ptr(out), _ptr(q), _dtype(q), int(q.shape[0]), int(q_start),
+                                         _ptr(k_cache), _ptr(v_cache), ctypes.byref(cache), _ptr(block_table),
+                                         int(kv_len), int(q.shape[1]), float(scale), _ptr(device_error),
+                                         _stream(stream)),
+           "pkv_paged_prefill_chunk")
 
 
 STATIC_SCRATCH_BYTES = 12 * 1024 * 1024  # PKV_STATIC_SCRATCH_BYTES in include/pkv.h

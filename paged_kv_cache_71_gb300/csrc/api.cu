@@ -10,6 +10,7 @@
 
 #include "cache_ops.cuh"
 #include "decode.cuh"
+#include "prefill.cuh"
 
 namespace pkv {
 
@@ -118,6 +119,22 @@ static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return PKV_OK;
+}
+
+// A 3-D tiled map with 128-byte swizzle (inner box of 64 bf16 = 128 bytes).
+static pkv_status tensor_map_sw128_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                                        uint32_t b1, uint32_t b2) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64u, b1, b2};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)", static_cast<int>(r));
     return PKV_OK;
 }
 
@@ -416,5 +433,62 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     else
         e = dispatch_s<KvE4M3, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,
+                                           int32_t q_start_pos, const void* k_cache, const void* v_cache,
+                                           const pkv_cache_desc* cache, const int32_t* block_table, int32_t kv_len,
+                                           int32_t num_q_heads, float scale, int32_t* device_error, void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    const int Hkv = cache->num_kv_heads, D = cache->head_dim, S = cache->block_size;
+    if (num_q_tokens < 0 || q_start_pos < 0 || num_q_heads <= 0 || kv_len < 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_q_tokens=%d q_start_pos=%d num_q_heads=%d kv_len=%d)",
+                    num_q_tokens, q_start_pos, num_q_heads, kv_len);
+    if (static_cast<int64_t>(q_start_pos) + num_q_tokens > kv_len)
+        return fail(PKV_ERR_INVALID_ARG, "kv_len %d < q_start_pos + num_q_tokens (the chunk's own keys must be cached)",
+                    kv_len);
+    if (num_q_heads % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
+    const int G = num_q_heads / Hkv;
+    if (q_dtype != PKV_BF16 || cache->dtype != PKV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports bf16 queries with a bf16 cache");
+    if (D != 128) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports head_dim 128");
+    if (S < 8) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports block_size 8, 16, 32");
+    if (G > 128 || 128 % G != 0) return fail(PKV_ERR_UNSUPPORTED, "GQA group %d must divide 128", G);
+    if (num_q_tokens == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(block_table) & 3u) return fail(PKV_ERR_INVALID_ARG, "block_table alignment");
+    if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    if (static_cast<size_t>(di.smem_optin) < prefill_smem_bytes())
+        return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
+    CUtensorMap qm, km, vm;
+    if ((st = tensor_map_sw128_bf16(&qm, q, 128, num_q_heads, num_q_tokens, G, 128 / G)) != PKV_OK) return st;
+    const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
+    if ((st = tensor_map_sw128_bf16(&km, k_cache, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128_bf16(&vm, v_cache, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    PrefillArgs a;
+    a.out = out;
+    a.block_table = block_table;
+    a.err = device_error;
+    a.NQ = num_q_tokens;
+    a.q_start = q_start_pos;
+    a.kv_len = kv_len;
+    a.Hq = num_q_heads;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.S = S;
+    a.NB = cache->num_blocks;
+    a.n_table = (kv_len + S - 1) / S;
+    a.sm_log2 = scale * 1.4426950408889634f;
+    a.timeout_ns = 2000000000ull;
+    cudaError_t e = launch_paged_prefill(qm, km, vm, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
     return PKV_OK;
 }
