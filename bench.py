@@ -54,6 +54,15 @@ def decode_algorithmic_bytes(w) -> int:
     return kv + qo + table + 4 * w.num_seqs
 
 
+def prefill_flops(w) -> int:
+    """Multiply-add work of the causal chunk: query i sees q_start + i + 1 keys; QK^T and P.V each
+    cost 2 * head_dim flops per (query head, key)."""
+    pf = w.prefill
+    nq = pf.q.shape[0]
+    keys = sum(pf.q_start + i + 1 for i in range(nq))
+    return 4 * w.head_dim * w.num_q_heads * keys
+
+
 def write_bytes(w) -> int:
     from paged_kv_cache_71_gb300.workload import elem_size
     T = len(w.slot_mapping)
@@ -202,9 +211,13 @@ def main():
     stream = torch.cuda.current_stream()
     launches_per_step = 2 + (1 if st.copy_pairs is not None else 0)
 
+    has_prefill = st.pf_q is not None
+    launches_per_step += 1 if has_prefill else 0
+
     def step():
         st.write(stream)
         st.attend(stream)
+        st.prefill(stream)
 
     for _ in range(args.warmup):
         step()
@@ -213,7 +226,7 @@ def main():
         raise RuntimeError(f"device error {st.device_error():#x}")
 
     # ---- device-resident timing: events around each step and around each decode launch
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -229,6 +242,8 @@ def main():
         ev[i][1].record(stream)
         st.attend(stream)
         ev[i][2].record(stream)
+        st.prefill(stream)
+        ev[i][3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -237,6 +252,7 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    prefill_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)] if has_prefill else None
     if dist:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -309,6 +325,12 @@ def main():
                         "reshape_and_cache_us": round(float(np.mean(write_ms)) * 1e3, 2),
                         "write_bytes": write_bytes(w)},
         }
+        if has_prefill:
+            pf_us = float(np.mean(prefill_ms)) * 1e3
+            fl = prefill_flops(w)
+            line["kernels"]["paged_prefill_us"] = round(pf_us, 2)
+            line["kernels"]["prefill_tflops"] = round(fl / (pf_us * 1e-6) / 1e12, 1)
+            line["kernels"]["prefill_flops"] = fl
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -156,9 +156,12 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
  *   out[i][hq] = softmax(scale * q[i][hq] . K[0 .. q_start_pos + i]^T) V[0 .. q_start_pos + i]
  * with K/V gathered through block_table (one sequence, ceil(kv_len / S)
  * entries).  Runs on the tensor cores: bf16 inputs, fp32 accumulation, the
- * softmax weights rounded to bf16 for the P.V product.
+ * softmax weights rounded to bf16 for the P.V product.  An FP8 cache is
+ * widened to bf16 on chip (exactly) and its per-tensor scales are applied to
+ * the scores and the output.
  *   q, out: [num_q_tokens][num_q_heads][128] bf16.
- * Supported: bf16 queries and cache, head_dim 128, block_size 8/16/32,
+ * scale must be positive.
+ * Supported: bf16 queries, bf16 or FP8 cache, head_dim 128, block_size 8/16/32,
  *   G = num_q_heads / num_kv_heads dividing 128.  No workspace.
  */
 pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,

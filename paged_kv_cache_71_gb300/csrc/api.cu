@@ -122,16 +122,17 @@ static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv
     return PKV_OK;
 }
 
-// A 3-D tiled map with 128-byte swizzle (inner box of 64 bf16 = 128 bytes).
-static pkv_status tensor_map_sw128_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                                        uint32_t b1, uint32_t b2) {
+// A 3-D tiled map with 128-byte swizzle; the inner box is 128 bytes (64 bf16 or 128 FP8 codes).
+static pkv_status tensor_map_sw128(CUtensorMap* map, const void* base, bool fp8, uint64_t d0, uint64_t d1, uint64_t d2,
+                                   uint32_t b1, uint32_t b2) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    cuuint32_t box[3] = {64u, b1, b2};
+    const uint64_t es = fp8 ? 1 : 2;
+    cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+    cuuint32_t box[3] = {fp8 ? 128u : 64u, b1, b2};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)", static_cast<int>(r));
@@ -453,8 +454,9 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     if (num_q_heads % Hkv != 0)
         return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
     const int G = num_q_heads / Hkv;
-    if (q_dtype != PKV_BF16 || cache->dtype != PKV_BF16)
-        return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports bf16 queries with a bf16 cache");
+    if (q_dtype != PKV_BF16 || (cache->dtype != PKV_BF16 && cache->dtype != PKV_FP8_E4M3))
+        return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports bf16 queries with a bf16 or FP8 cache");
+    const bool fp8 = cache->dtype == PKV_FP8_E4M3;
     if (D != 128) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports head_dim 128");
     if (S < 8) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports block_size 8, 16, 32");
     if (G > 128 || 128 % G != 0) return fail(PKV_ERR_UNSUPPORTED, "GQA group %d must divide 128", G);
@@ -463,16 +465,16 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(block_table) & 3u) return fail(PKV_ERR_INVALID_ARG, "block_table alignment");
-    if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
+    if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
     DeviceInfo di;
     if ((st = device_info(&di)) != PKV_OK) return st;
-    if (static_cast<size_t>(di.smem_optin) < prefill_smem_bytes())
+    if (static_cast<size_t>(di.smem_optin) < prefill_smem_bytes(fp8))
         return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
     CUtensorMap qm, km, vm;
-    if ((st = tensor_map_sw128_bf16(&qm, q, 128, num_q_heads, num_q_tokens, G, 128 / G)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&qm, q, false, 128, num_q_heads, num_q_tokens, G, 128 / G)) != PKV_OK) return st;
     const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
-    if ((st = tensor_map_sw128_bf16(&km, k_cache, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
-    if ((st = tensor_map_sw128_bf16(&vm, v_cache, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&km, k_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
     PrefillArgs a;
     a.out = out;
     a.block_table = block_table;
@@ -486,9 +488,10 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     a.S = S;
     a.NB = cache->num_blocks;
     a.n_table = (kv_len + S - 1) / S;
-    a.sm_log2 = scale * 1.4426950408889634f;
+    a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
+    a.out_mul = fp8 ? cache->v_scale : 1.f;
     a.timeout_ns = 2000000000ull;
-    cudaError_t e = launch_paged_prefill(qm, km, vm, a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_paged_prefill(qm, km, vm, a, fp8, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
     return PKV_OK;
 }

@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                     const bool need = mb > m_ref + kLazyRescale;
                     if (__any_sync(kFull, need)) {
                         const float m_new = need ? mb : m_ref;
-                        const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
+                        const float alpha = (m_new == m_ref) ? 1.f : ex2_approx(m_ref - m_new);
                         l_run *= alpha;
                         m_ref = m_new;
                         if (tp == 0 && (lg % DUP) == 0) abuf[gl] = make_float2(alpha, alpha);
@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                     float lsum = 0.f;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
-                        const float p = (!M || sr[r] != -INFINITY) ? exp2f(sr[r] - m_ref) : 0.f;
+                        const float p = (!M || sr[r] != -INFINITY) ? ex2_approx(sr[r] - m_ref) : 0.f;
                         lsum += p;
                         if ((lg % DUP) == 0) pbuf[(r * TP + tp) * G + gl] = make_float2(p, p);
                     }
@@ -692,8 +692,8 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                 const float mr = __ldcg(r + G * D + g);
                 const float lr = __ldcg(r + G * D + G + g);
                 const float mn = fmaxf(Mx[g], mr);
-                const float fo = (Mx[g] == -INFINITY) ? 0.f : exp2f(Mx[g] - mn);
-                const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mn);
+                const float fo = (Mx[g] == -INFINITY) ? 0.f : ex2_approx(Mx[g] - mn);
+                const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
                 Ls[g] = Ls[g] * fo + lr * fr;
                 Mx[g] = mn;
 #pragma unroll

@@ -134,6 +134,13 @@ __device__ __forceinline__ uint8_t float_to_e4m3_sat(float x) {
     return static_cast<uint8_t>(r & 0xff);
 }
 
+// 2^x with the hardware approximation (flushes results below 2^-126 to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
     __nv_bfloat16 b = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t*>(&b);

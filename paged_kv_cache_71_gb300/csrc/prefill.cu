@@ -33,7 +33,9 @@ constexpr int kOffQ = 0;                       // 2 halves
 constexpr int kOffK = kOffQ + 2 * kHalf;       // 2 stages x 2 halves
 constexpr int kOffV = kOffK + 4 * kHalf;       // 2 stages x 2 halves
 constexpr int kOffP = kOffV + 4 * kHalf;       // 2 halves
-constexpr int kOffBar = kOffP + 2 * kHalf;     // mbarriers, TMEM address, abort flag
+constexpr int kOffStage = kOffP + 2 * kHalf;   // FP8 caches only: K and V codes of one key tile (32 KB)
+template <bool FP8>
+constexpr int off_bar() { return kOffStage + (FP8 ? 2 * kHalf : 0); }  // mbarriers, TMEM address, abort flag
 constexpr int kTmemCols = 256;                 // S: columns 0..127, O: 128..255
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);   // S = Q K^T, both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);   // O = P V, V is N (d) major
@@ -50,16 +52,16 @@ __device__ __forceinline__ void tma_load_3d_plain(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(float_to_bf16_bits(lo)) | (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
-}
-
-__device__ __forceinline__ float bf16_round(float x) {
-    return __uint_as_float(static_cast<uint32_t>(float_to_bf16_bits(x)) << 16);
+// Two floats -> packed bf16x2 (round to nearest even), low half first.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 }  // namespace
 
+template <bool FP8>
 __global__ void __launch_bounds__(128, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(128, 1)
     const int h = blockIdx.y;
     const int rows_q = kRows / a.G;                                   // query tokens per CTA
     const int i0 = (gridDim.x - 1 - blockIdx.x) * rows_q;             // heaviest (latest) tiles first
+    constexpr int kOffBar = off_bar<FP8>();
     const uint32_t bar = sb + kOffBar;                                // 8 bytes per mbarrier
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 72);
@@ -98,11 +101,11 @@ __global__ void __launch_bounds__(128, 1)
     const int n_tiles = max_key / kKeys + 1;
     const int blocks_per_tile = kKeys / a.S;
 
-    // thread 0: copy the K and V tiles of key tile j into stage j & 1
+    // thread 0: copy the K and V tiles of key tile j (bf16: into stage j & 1; FP8: into the code staging area)
     auto load_kv = [&](int j) {
-        const int st = j & 1;
+        const int st = FP8 ? 0 : (j & 1);
         const uint32_t b = bar + 8 * (kBarKV0 + st);
-        mbar_arrive_expect_tx(b, 4 * kHalf);
+        mbar_arrive_expect_tx(b, FP8 ? 2 * kHalf : 4 * kHalf);
         for (int bi = 0; bi < blocks_per_tile; ++bi) {
             const int idx = j * blocks_per_tile + bi;
             int c2 = a.NB * a.S;  // beyond the pool: the copy fills zeros
@@ -111,11 +114,52 @@ __global__ void __launch_bounds__(128, 1)
                 if (phys >= 0 && phys < a.NB) c2 = phys * a.S;
                 else raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
             }
+            if constexpr (FP8) {
+                const uint32_t off = bi * a.S * 128;  // 128 one-byte codes per key row
+                tma_load_3d_plain(sb + kOffStage + off, &kmap, 0, h, c2, b);
+                tma_load_3d_plain(sb + kOffStage + kHalf + off, &vmap, 0, h, c2, b);
+            } else {
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t off = st * 2 * kHalf + hf * kHalf + bi * a.S * 128;
-                tma_load_3d_plain(sb + kOffK + off, &kmap, hf * 64, h, c2, b);
-                tma_load_3d_plain(sb + kOffV + off, &vmap, hf * 64, h, c2, b);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t off = st * 2 * kHalf + hf * kHalf + bi * a.S * 128;
+                    tma_load_3d_plain(sb + kOffK + off, &kmap, hf * 64, h, c2, b);
+                    tma_load_3d_plain(sb + kOffV + off, &vmap, hf * 64, h, c2, b);
+                }
+            }
+        }
+    };
+
+    // FP8: widen the staged codes of one key tile into the bf16 stage st (exact; the
+    // per-tensor scales are applied to the scores and to the output instead).
+    // Thread t converts key row t of K and of V; V rows of keys past the end become 0.
+    auto widen_fp8 = [&](int st, int nvalid) {
+        const int t = tid;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint8_t* src = smem + kOffStage + kv * kHalf + t * 128;
+            uint8_t* dst0 = smem + (kv ? kOffV : kOffK) + st * 2 * kHalf + t * 128;
+            const bool zero = kv == 1 && t >= nvalid;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // logical 16-code chunk: head dims 16c .. 16c + 15
+                uint32_t o[8];
+                if (zero) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[i] = 0u;
+                } else {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ (t & 7)) * 16));
+                    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                        const float2 f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                        o[2 * i] = pack_bf16x2_rn(f0.x, f0.y);
+                        o[2 * i + 1] = pack_bf16x2_rn(f1.x, f1.y);
+                    }
+                }
+                uint8_t* dst = dst0 + (c >> 2) * kHalf;
+                const int lc = 2 * (c & 3);
+                *reinterpret_cast<uint4*>(dst + ((lc ^ (t & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<uint4*>(dst + (((lc + 1) ^ (t & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
         }
     };
@@ -128,7 +172,7 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_3d_plain(sb + kOffQ, &qmap, 0, h * a.G, i0, bar + 8 * kBarQ);
         tma_load_3d_plain(sb + kOffQ + kHalf, &qmap, 64, h * a.G, i0, bar + 8 * kBarQ);
         load_kv(0);
-        if (n_tiles > 1) load_kv(1);
+        if (!FP8 && n_tiles > 1) load_kv(1);
     }
     if (!mbar_wait_bounded(bar + 8 * kBarQ, 0, a.timeout_ns)) *abort_flag = 1;
 
@@ -137,22 +181,32 @@ __global__ void __launch_bounds__(128, 1)
     int issued_s = 0;         // S = Q K^T groups committed so far
     int issued_o = 0;         // P.V groups committed so far
     int kv_waited = 0;        // key tiles whose copies were waited for
-    int kv_loaded = n_tiles < 2 ? n_tiles : 2;  // key tiles whose copies were issued
+    int kv_loaded = FP8 ? 1 : (n_tiles < 2 ? n_tiles : 2);  // key tiles whose copies were issued
 
     for (int j = 0; j < n_tiles; ++j) {
         const int st = j & 1;
         const int tile0 = j * kKeys;
         // ---- K/V of this tile landed; zero V rows of keys past the end (their slots are not data)
-        if (!mbar_wait_bounded(bar + 8 * (kBarKV0 + st), (j >> 1) & 1, a.timeout_ns)) *abort_flag = 1;
-        kv_waited = j + 1;
         const int nvalid = min(kKeys, a.kv_len - tile0);
-        if (nvalid < kKeys) {
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            for (int idx = tid; idx < (kKeys - nvalid) * 16; idx += blockDim.x) {
-                const int row = nvalid + idx / 16, hf = (idx / 8) & 1, ch = idx & 7;
-                *reinterpret_cast<uint4*>(smem + kOffV + st * 2 * kHalf + hf * kHalf + row * 128 + ch * 16) = z;
-            }
+        if constexpr (FP8) {
+            if (!mbar_wait_bounded(bar + 8 * kBarKV0, j & 1, a.timeout_ns)) *abort_flag = 1;
+            kv_waited = j + 1;
+            widen_fp8(st, nvalid);
             fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0 && j + 1 < n_tiles && !*abort_flag) load_kv(j + 1);  // the staging area is free again
+            if (j + 1 < n_tiles) kv_loaded = j + 2;
+        } else {
+            if (!mbar_wait_bounded(bar + 8 * (kBarKV0 + st), (j >> 1) & 1, a.timeout_ns)) *abort_flag = 1;
+            kv_waited = j + 1;
+            if (nvalid < kKeys) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int idx = tid; idx < (kKeys - nvalid) * 16; idx += blockDim.x) {
+                    const int row = nvalid + idx / 16, hf = (idx / 8) & 1, ch = idx & 7;
+                    *reinterpret_cast<uint4*>(smem + kOffV + st * 2 * kHalf + hf * kHalf + row * 128 + ch * 16) = z;
+                }
+                fence_proxy_async_smem();
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -174,24 +228,30 @@ __global__ void __launch_bounds__(128, 1)
         if (!mbar_wait_bounded(bar + 8 * kBarS, j & 1, a.timeout_ns)) *abort_flag = 1;
         tc_fence_after();
 
-        // ---- pass 1: this row's maximum over the tile (masked keys excluded)
-        float mt = -INFINITY;
+        // ---- pass 1: this row's maximum over the tile.  Keys <= q_start + i0 are visible to every
+        // row of the CTA, so only tiles past that point (or past kv_len) need per-key masks.
+        const bool masked = (tile0 + kKeys - 1 > a.q_start + i0) || (tile0 + kKeys > a.kv_len);
+        const int lim = min(a.kv_len, qpos + 1) - tile0;  // this row sees keys [tile0, tile0 + lim)
+        float mraw = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kKeys; c += 32) {
             float v[32];
             tmem_ld32(tS + trow + c, v);
+            if (!masked) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int key = tile0 + c + i;
-                if (key < a.kv_len && key <= qpos) mt = fmaxf(mt, v[i] * a.sm_log2);
+                for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, v[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, (c + i < lim) ? v[i] : -INFINITY);
             }
         }
+        const float mt = mraw * a.sm_log2;  // the scale is positive, so it keeps the order
 
         // ---- the previous P.V has finished: O may be rescaled and P overwritten
         if (j > 0) {
             if (!mbar_wait_bounded(bar + 8 * kBarO, (j - 1) & 1, a.timeout_ns)) *abort_flag = 1;
             tc_fence_after();
-            if (j + 1 < n_tiles) {
+            if (!FP8 && j + 1 < n_tiles) {
                 if (tid == 0) load_kv(j + 1);  // its stage was read by tile j - 1
                 kv_loaded = j + 2;
             }
@@ -199,7 +259,7 @@ __global__ void __launch_bounds__(128, 1)
         const bool need = mt > m_ref + 8.f;
         if (j > 0 && __any_sync(kFull, need)) {
             const float m_new = need ? mt : m_ref;
-            const float alpha = exp2f(m_ref - m_new);
+            const float alpha = ex2_approx(m_ref - m_new);
 #pragma unroll
             for (int c = 0; c < 128; c += 32) {
                 float o[32];
@@ -216,6 +276,7 @@ __global__ void __launch_bounds__(128, 1)
 
         // ---- pass 2: probabilities as bf16 into the swizzled K-major P tile, and the row sum
         float ls = 0.f;
+        const float neg_m = -m_ref;
 #pragma unroll
         for (int c = 0; c < kKeys; c += 32) {
             float v[32];
@@ -223,12 +284,14 @@ __global__ void __launch_bounds__(128, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                float p0 = 0.f, p1 = 0.f;
-                const int k0 = tile0 + c + i;
-                if (k0 < a.kv_len && k0 <= qpos) p0 = bf16_round(exp2f(v[i] * a.sm_log2 - m_ref));
-                if (k0 + 1 < a.kv_len && k0 + 1 <= qpos) p1 = bf16_round(exp2f(v[i + 1] * a.sm_log2 - m_ref));
+                float p0 = ex2_approx(fmaf(v[i], a.sm_log2, neg_m));
+                float p1 = ex2_approx(fmaf(v[i + 1], a.sm_log2, neg_m));
+                if (masked) {
+                    p0 = (c + i < lim) ? p0 : 0.f;
+                    p1 = (c + i + 1 < lim) ? p1 : 0.f;
+                }
                 ls += p0 + p1;
-                pk[i / 2] = pack_bf16x2(p0, p1);
+                pk[i / 2] = pack_bf16x2_rn(p0, p1);
             }
             const int hf = c >> 6;
 #pragma unroll
@@ -276,7 +339,7 @@ __global__ void __launch_bounds__(128, 1)
         if (tid == 0) raise_error(a.err, PKV_DEVERR_TIMEOUT);
     } else {
         // ---- out = O / l for this row
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = l_run > 0.f ? a.out_mul / l_run : 0.f;
         const int g = r % a.G;
         uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
                         ((static_cast<size_t>(qi) * a.Hq + static_cast<size_t>(h) * a.G + g) * 128) * 2;
@@ -288,10 +351,10 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     uint4 w;
-                    w.x = pack_bf16x2(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
-                    w.y = pack_bf16x2(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-                    w.z = pack_bf16x2(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-                    w.w = pack_bf16x2(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+                    w.x = pack_bf16x2_rn(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                    w.y = pack_bf16x2_rn(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                    w.z = pack_bf16x2_rn(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                    w.w = pack_bf16x2_rn(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
                     *reinterpret_cast<uint4*>(orow + (c + 8 * q4) * 2) = w;
                 }
             }
@@ -302,17 +365,19 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-size_t prefill_smem_bytes() { return static_cast<size_t>(kOffBar) + 128 + 1024; }
+size_t prefill_smem_bytes(bool fp8) {
+    return static_cast<size_t>(fp8 ? off_bar<true>() : off_bar<false>()) + 128 + 1024;
+}
 
 cudaError_t launch_paged_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const PrefillArgs& a, cudaStream_t stream) {
-    const size_t smem = prefill_smem_bytes();
-    cudaError_t e =
-        cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+                                 const PrefillArgs& a, bool fp8, cudaStream_t stream) {
+    const size_t smem = prefill_smem_bytes(fp8);
+    auto kern = fp8 ? paged_prefill_kernel<true> : paged_prefill_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int rows_q = kRows / a.G;
     dim3 grid((a.NQ + rows_q - 1) / rows_q, a.Hkv);
-    paged_prefill_kernel<<<grid, 128, smem, stream>>>(qmap, kmap, vmap, a);
+    kern<<<grid, 128, smem, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
 }
 

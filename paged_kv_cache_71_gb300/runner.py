@@ -45,6 +45,11 @@ class DeviceStep:
         self.workspace = torch.zeros(max(ws, 16), dtype=torch.uint8, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.max_context_len = int(w.context_lens.max()) if w.num_seqs else 0
+        self.pf_q = self.pf_out = self.pf_table = None
+        if w.prefill is not None:
+            self.pf_q = to_device(w.prefill.q, device=device)
+            self.pf_out = torch.empty_like(self.pf_q)
+            self.pf_table = to_device(w.prefill.block_table, device=device)
 
     def write(self, stream=None) -> None:
         if self.copy_pairs is not None:
@@ -57,9 +62,17 @@ class DeviceStep:
                                      self.context_lens, self.w.scale, self.num_splits, self.max_context_len,
                                      self.workspace, self.err, stream)
 
+    def prefill(self, stream=None) -> None:
+        if self.pf_q is None:
+            return
+        pf = self.w.prefill
+        B.pkv_paged_prefill_chunk(self.pf_out, self.pf_q, pf.q_start, self.k_cache, self.v_cache, self.cache,
+                                  self.pf_table, pf.kv_len, self.w.scale, self.err, stream)
+
     def step(self, stream=None) -> None:
         self.write(stream)
         self.attend(stream)
+        self.prefill(stream)
 
     def device_error(self) -> int:
         return int(self.err.item())

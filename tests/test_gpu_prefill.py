@@ -18,7 +18,7 @@ from parity import assert_close, to_host
 pytestmark = pytest.mark.gpu
 
 
-def _chunk_case(NQ, q_start, Hq, Hkv, S, seed, extra_blocks=5, poison=False):
+def _chunk_case(NQ, q_start, Hq, Hkv, S, seed, extra_blocks=5, poison=False, kv="bf16"):
     """One sequence of kv_len = q_start + NQ tokens in a shuffled pool, plus a query chunk."""
     rng = np.random.default_rng(seed)
     D = 128
@@ -28,8 +28,8 @@ def _chunk_case(NQ, q_start, Hq, Hkv, S, seed, extra_blocks=5, poison=False):
     alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
     alloc.add_seq("s", kv_len)
     table = np.array(alloc.tables["s"], np.int32)
-    kc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
-    vc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
+    kc = wl.random_values(rng, (NB, S, Hkv, D), kv)
+    vc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     if poison:  # NaN in every slot that is not one of the sequence's tokens
         owned = np.zeros((NB, S), bool)
         for p in range(kv_len):
@@ -40,12 +40,12 @@ def _chunk_case(NQ, q_start, Hq, Hkv, S, seed, extra_blocks=5, poison=False):
     return q, kc, vc, table, kv_len
 
 
-def _run(q, kc, vc, table, q_start, kv_len, scale):
+def _run(q, kc, vc, table, q_start, kv_len, scale, k_scale=1.0, v_scale=1.0):
     dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
     out = torch.full_like(dq, float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pkv.pkv_paged_prefill_chunk(out, dq, q_start, dk, dv, B.CacheDesc.for_cache(dk), to_device(table), kv_len,
-                                scale, err)
+    pkv.pkv_paged_prefill_chunk(out, dq, q_start, dk, dv, B.CacheDesc.for_cache(dk, k_scale, v_scale),
+                                to_device(table), kv_len, scale, err)
     torch.cuda.synchronize()
     assert err.item() == 0, hex(err.item())
     return to_host(out)
@@ -64,6 +64,15 @@ def test_prefill_chunk_matches_oracle(NQ, q_start, Hq, Hkv, S):
     ref = oracle.paged_prefill_chunk(q, q_start, kc, vc, table, kv_len, scale)
     got = _run(q, kc, vc, table, q_start, kv_len, scale)
     assert_close("bf16", got, ref, f"prefill NQ={NQ} q_start={q_start} G={Hq // Hkv} S={S}")
+
+
+@pytest.mark.parametrize("NQ,q_start,Hq,Hkv,S", [(40, 100, 8, 1, 16), (130, 3, 4, 4, 32), (33, 500, 16, 2, 8)])
+def test_prefill_chunk_fp8_cache(NQ, q_start, Hq, Hkv, S):
+    q, kc, vc, table, kv_len = _chunk_case(NQ, q_start, Hq, Hkv, S, seed=7 + NQ, kv="e4m3")
+    scale = 1 / np.sqrt(128)
+    ref = oracle.paged_prefill_chunk(q, q_start, kc, vc, table, kv_len, scale, k_scale=0.25, v_scale=0.5)
+    got = _run(q, kc, vc, table, q_start, kv_len, scale, 0.25, 0.5)
+    assert_close("e4m3", got, ref, f"fp8 prefill NQ={NQ} q_start={q_start}")
 
 
 def test_prefill_poisoned_slots_do_not_leak():
@@ -89,16 +98,20 @@ def test_prefill_rejects_missing_chunk_keys_and_bad_shapes():
     assert ei.value.status == 2
 
 
-def test_llama70b_chunk_sampled_rows():
+@pytest.mark.parametrize("name", ["llama70b_mixed_bf16", "llama70b_mixed_fp8"])
+def test_llama70b_chunk_sampled_rows(name):
     """The 512-token chunk at positions 8192..8703 over the Llama-70B-shaped pool (64 q / 8 kv heads)."""
-    w = wl.make("llama70b_mixed_bf16")
+    w = wl.make(name)
     pf = w.prefill
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
-    oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    cdt = oracle.E4M3 if w.kv_dtype == "e4m3" else oracle.BF16
+    oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc, cache_dtype=cdt, k_scale=w.k_scale,
+                             v_scale=w.v_scale)
     rows = [0, 1, 15, 16, 127, 255, 256, 400, 510, 511]
-    ref = oracle.paged_prefill_chunk(pf.q, pf.q_start, kc, vc, pf.block_table, pf.kv_len, w.scale, rows=rows)
+    ref = oracle.paged_prefill_chunk(pf.q, pf.q_start, kc, vc, pf.block_table, pf.kv_len, w.scale, rows=rows,
+                                     cache_dtype=cdt, k_scale=w.k_scale, v_scale=w.v_scale)
     dk, dv = to_device(w.k_cache), to_device(w.v_cache)
-    desc = B.CacheDesc.for_cache(dk)
+    desc = B.CacheDesc.for_cache(dk, w.k_scale, w.v_scale)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.pkv_reshape_and_cache(to_device(w.k_new), to_device(w.v_new), to_device(w.slot_mapping), dk, dv, desc, err)
     dq = to_device(pf.q)
@@ -109,4 +122,4 @@ def test_llama70b_chunk_sampled_rows():
     assert err.item() == 0
     got = to_host(out)
     assert np.isfinite(got).all()
-    assert_close("bf16", got[rows], ref, "llama70b chunk")
+    assert_close(w.kv_dtype, got[rows], ref, name)
