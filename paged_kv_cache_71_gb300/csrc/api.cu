@@ -332,8 +332,8 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
         return fail(PKV_ERR_UNSUPPORTED, "GQA group size %d (supported: 1, 2, 4, 8)", G);
     if (num_seqs > 8192) return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > 8192", num_seqs);
     if (Hkv > 1024) return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d > 1024", Hkv);
-    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX)
-        return fail(PKV_ERR_OUT_OF_RANGE, "block table larger than 2^31-1 entries");
+    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * Hkv > INT32_MAX - 64)
+        return fail(PKV_ERR_OUT_OF_RANGE, "num_seqs * max_blocks_per_seq * num_kv_heads must stay below 2^31");
     if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
     const bool combo_ok = (q_dtype == PKV_F32 && cache->dtype == PKV_F32) ||
                           (q_dtype == PKV_BF16 && (cache->dtype == PKV_BF16 || cache->dtype == PKV_FP8_E4M3));

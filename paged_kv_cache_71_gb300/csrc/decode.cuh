@@ -205,7 +205,7 @@ struct DecodeArgs {
 constexpr float kLazyRescale = 8.0f;   // log2 units: raise the running max only beyond this
 
 // Largest s in [0, B) with P[s] <= key (P[0] = 0 <= key).
-__device__ __forceinline__ int find_seq(const int* P, int B, long long key) {
+__device__ __forceinline__ int find_seq(const int* P, int B, int key) {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -214,36 +214,30 @@ __device__ __forceinline__ int find_seq(const int* P, int B, long long key) {
     return lo;
 }
 
-// First allowed cut at or after stream position x.
-__device__ __forceinline__ long long snap_pos(const int* P, int B, int Hkv, long long T, int C, long long x) {
-    if (x >= T) return T;
-    const int s = find_seq(P, B, x / Hkv);
-    const long long base = static_cast<long long>(Hkv) * P[s];
-    const int nb = P[s + 1] - P[s];
-    const long long local = x - base;
-    const int j = static_cast<int>(local % nb);
-    if (j == 0) return x;
-    const int up = (C >= nb) ? nb : ((j + C - 1) / C) * C;
-    return x - j + (up < nb ? up : nb);
-}
+// The work split: the T = Hkv * sum(blocks) (sequence, KV head, block) items laid end to end,
+// worker w owning [start(w), start(w + 1)).  Raw shares are floor(w * T / W), moved forward to
+// the next allowed cut (a pair boundary, or a multiple of C blocks inside a pair).  All
+// arithmetic is 32-bit: T < 2^31 is checked on the host, and floor(w * T / W) is formed as
+// w * (T / W) + floor(w * (T % W) / W) with w * (T % W) < W^2.
+struct WorkSplit {
+    const int* P;
+    int B, Hkv, T, C, W, tq, tr;
 
-__device__ __forceinline__ long long worker_start(const int* P, int B, int Hkv, long long T, int C, int W,
-                                                  int w) {
-    if (w >= W) return T;
-    const long long raw = (static_cast<long long>(w) * T) / W;
-    return snap_pos(P, B, Hkv, T, C, raw);
-}
-
-// Last worker whose share starts at or before y.
-__device__ __forceinline__ int worker_of(const int* P, int B, int Hkv, long long T, int C, int W,
-                                         long long y) {
-    int lo = 0, hi = W - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (worker_start(P, B, Hkv, T, C, W, mid) <= y) lo = mid; else hi = mid - 1;
+    __device__ __forceinline__ int snap(int x) const {
+        if (x >= T) return T;
+        const int s = find_seq(P, B, x / Hkv);
+        const int nb = P[s + 1] - P[s];
+        const int local = x - Hkv * P[s];
+        const int j = local % nb;
+        if (j == 0) return x;
+        const int up = (C >= nb) ? nb : ((j + C - 1) / C) * C;
+        return x - j + (up < nb ? up : nb);
     }
-    return lo;
-}
+    __device__ __forceinline__ int start(int w) const {
+        if (w >= W) return T;
+        return snap(w * tq + (w * tr) / W);
+    }
+};
 
 // Reduce-scatter of V[0..N) over the lanes of an aligned LPT-lane group:
 // afterwards each lane holds the full sum for index lg / (LPT / G).
@@ -364,12 +358,12 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
     }
     __syncwarp();
 
-    const long long T = static_cast<long long>(Hkv) * P[B];
+    const int T = Hkv * P[B];
     const int W = gridDim.x * NW;
     const int w = blockIdx.x * NW + warp;
-    const int C = a.part_blocks;
-    const long long A0 = worker_start(P, B, Hkv, T, C, W, w);
-    const long long A1 = worker_start(P, B, Hkv, T, C, W, w + 1);
+    const WorkSplit split{P, B, Hkv, T, a.part_blocks, W, T / W, T % W};
+    const int A0 = split.start(w);
+    const int A1 = split.start(w + 1);
     if (A0 >= A1) return;
     if (lane == 0) {
         prefetch_tensormap(&kmap);
@@ -381,14 +375,14 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
     const int gl = lg / DUP;  // the query head whose score this lane holds
 
     // Stream position x -> packed metadata (computed by the lane that owns x).
-    auto make_meta = [&](long long x) -> Meta {
+    auto make_meta = [&](int x) -> Meta {
         Meta m{0, -1, 0};
         if (x >= A1) return m;
         const int s = find_seq(P, B, x / Hkv);
-        const long long local = x - static_cast<long long>(Hkv) * P[s];
+        const int local = x - Hkv * P[s];
         const int nb = P[s + 1] - P[s];
-        const int h = static_cast<int>(local / nb);
-        const int j = static_cast<int>(local - static_cast<long long>(h) * nb);
+        const int h = local / nb;
+        const int j = local - h * nb;
         const int L = a.context_lens[s];
         m.a = s * 1024 + h;
         m.b = a.block_tables[static_cast<size_t>(s) * a.MB + j];
@@ -400,7 +394,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
 
     // Issue the copies of stream index k (position A0 + k) into stage k % depth.
     // Called by the one lane that holds the block's metadata.
-    auto issue = [&](long long k, const Meta& m) {
+    auto issue = [&](int k, const Meta& m) {
         const int st = static_cast<int>(k % a.depth);
         const bool seg_start = (m.c & kMetaFirst) || (k == 0);
         const bool ok = (m.c & kMetaOk) != 0;
@@ -421,8 +415,8 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
         }
     };
 
-    const long long n_blocks = A1 - A0;
-    long long wbase = A0;
+    const int n_blocks = A1 - A0;
+    int wbase = A0;
     Meta cur = make_meta(wbase + lane);
     Meta nxt = make_meta(wbase + 32 + lane);
 
@@ -434,28 +428,28 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
 
     // Bounded wait for stage k; on timeout record the error and drain the
     // copies still in flight (also bounded) so the warp can leave safely.
-    auto wait_stage = [&](long long k) -> bool {
+    auto wait_stage = [&](int k) -> bool {
         const int st = static_cast<int>(k % a.depth);
         if (mbar_wait_bounded(bars_u32 + 8 * st, static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
             return true;
         raise_error(a.err, PKV_DEVERR_TIMEOUT);
-        for (long long kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
+        for (int kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
             mbar_wait_bounded(bars_u32 + 8 * static_cast<int>(kk % a.depth),
                               static_cast<uint32_t>((kk / a.depth) & 1), a.timeout_ns);
         return false;
     };
 
-    long long k = 0;
+    int k = 0;
     while (k < n_blocks) {
         // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
-        const long long seg_x0 = A0 + k;
+        const int seg_x0 = A0 + k;
         float2 q2[G][HP];
         float2 o2[G][HP];
         float m_ref = -INFINITY;  // running max of head gl (log2 units), uniform over lanes holding gl
         float l_run = 0.f;        // this lane's share of the running sum of head gl
         int ma = 0, mc = 0, seg_first = 0;
         bool first = true;
-        long long x_last;
+        int x_last;
             // One softmax tile (TS tokens) of the block in this stage; M = some tokens are past the end.
             auto tile = [&](auto masked, const uint8_t* sp, int ti, int tv) {
                 constexpr bool M = decltype(masked)::value;
@@ -539,13 +533,13 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                     __syncwarp();
             };
         while (true) {
-            const long long x = A0 + k;
+            const int x = A0 + k;
             if (x - wbase >= 32) {
                 wbase += 32;
                 cur = nxt;
                 nxt = make_meta(wbase + 32 + lane);
             }
-            const int src = static_cast<int>(x - wbase);
+            const int src = x - wbase;
             ma = __shfl_sync(kFull, cur.a, src);
             mc = __shfl_sync(kFull, cur.c, src);
             if (!wait_stage(k)) return;
@@ -584,9 +578,9 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
             __syncwarp();
 
             // ---- refill this stage with stream index k + depth (issued by the lane holding its metadata)
-            const long long kn = k + a.depth;
+            const int kn = k + a.depth;
             if (kn < n_blocks) {
-                const int sn = static_cast<int>(A0 + kn - wbase);
+                const int sn = A0 + kn - wbase;
                 if (lane == (sn & 31)) {
                     fence_proxy_async_smem();
                     issue(kn, sn < 32 ? cur : nxt);
@@ -662,15 +656,15 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
         __threadfence();
         __syncwarp();
         int old = 0;
-        const int seg_blocks = static_cast<int>(x_last - seg_x0 + 1);
+        const int seg_blocks = x_last - seg_x0 + 1;
         if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], seg_blocks);
         old = __shfl_sync(kFull, old, 0);
         if (old + seg_blocks != nb) continue;
 
         // last finisher of pair (s, h): merge its segments in stream order
         __threadfence();
-        const long long U0 = static_cast<long long>(Hkv) * P[s] + static_cast<long long>(h) * nb;
-        const long long U1 = U0 + nb;
+        const int U0 = Hkv * P[s] + h * nb;
+        const int U1 = U0 + nb;
         float Mx[G], Ls[G];
         float2 acc[G][HP];
 #pragma unroll
@@ -680,34 +674,37 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
 #pragma unroll
             for (int i = 0; i < HP; ++i) acc[g][i] = make_float2(0.f, 0.f);
         }
-        long long y = U0;
-        int guard = 0;
-        while (y < U1 && guard++ <= W) {
-            const int wq = worker_of(P, B, Hkv, T, C, W, y);
-            const long long aq = worker_start(P, B, Hkv, T, C, W, wq);
-            const int sl = (aq == y) ? 0 : 1;
-            const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
+        // the workers that cut this pair are consecutive: step down from this one to the first
+        int wq = w, ys = A0;
+        while (ys > U0 && wq > 0) ys = split.start(--wq);
+        while (ys < U1 && wq < W) {
+            const int ye = split.start(wq + 1);
+            if (ye > ys) {  // a non-empty share holds one segment of the pair
+                const int sl = (ys >= U0) ? 0 : 1;
+                const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float mr = __ldcg(r + G * D + g);
-                const float lr = __ldcg(r + G * D + G + g);
-                const float mn = fmaxf(Mx[g], mr);
-                const float fo = (Mx[g] == -INFINITY) ? 0.f : ex2_approx(Mx[g] - mn);
-                const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
-                Ls[g] = Ls[g] * fo + lr * fr;
-                Mx[g] = mn;
+                for (int g = 0; g < G; ++g) {
+                    const float mr = __ldcg(r + G * D + g);
+                    const float lr = __ldcg(r + G * D + G + g);
+                    const float mn = fmaxf(Mx[g], mr);
+                    const float fo = (Mx[g] == -INFINITY) ? 0.f : ex2_approx(Mx[g] - mn);
+                    const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
+                    Ls[g] = Ls[g] * fo + lr * fr;
+                    Mx[g] = mn;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c)
+                    for (int c = 0; c < NCH; ++c)
 #pragma unroll
-                    for (int e = 0; e < EPC / 2; ++e) {
-                        const float2 ov =
-                            __ldcg(reinterpret_cast<const float2*>(r + g * D + (c * LPT + lg) * EPC + 2 * e));
-                        float2& ac = acc[g][c * (EPC / 2) + e];
-                        ac.x = ac.x * fo + ov.x * fr;
-                        ac.y = ac.y * fo + ov.y * fr;
-                    }
+                        for (int e = 0; e < EPC / 2; ++e) {
+                            const float2 ov =
+                                __ldcg(reinterpret_cast<const float2*>(r + g * D + (c * LPT + lg) * EPC + 2 * e));
+                            float2& ac = acc[g][c * (EPC / 2) + e];
+                            ac.x = ac.x * fo + ov.x * fr;
+                            ac.y = ac.y * fo + ov.y * fr;
+                        }
+                }
             }
-            y = worker_start(P, B, Hkv, T, C, W, wq + 1);
+            ++wq;
+            ys = ye;
         }
         if (tp == 0) {
 #pragma unroll
