@@ -359,7 +359,9 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
     __syncwarp();
 
     const int T = Hkv * P[B];
-    const int W = gridDim.x * NW;
+    if (T == 0) return;
+    // never more shares than blocks, so that no share is empty when cuts may fall anywhere
+    const int W = min(static_cast<int>(gridDim.x) * NW, T);
     const int w = blockIdx.x * NW + warp;
     const WorkSplit split{P, B, Hkv, T, a.part_blocks, W, T / W, T % W};
     const int A0 = split.start(w);
