@@ -82,6 +82,34 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "of fallback"
 
 
+DECODE_SOURCES = ("decode.cuh", "pkv_device.cuh", "decode_bf16_s16.cu")
+
+
+def kernel_digest(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_71_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this workload, if that summary was
+    taken on the kernel sources as they are now (same digest); otherwise None."""
+    import re
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    dig = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    if not dig or not tr or dig.group(1) != kernel_digest(DECODE_SOURCES):
+        return None
+    return int(tr.group(1))
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
 
@@ -181,6 +209,8 @@ def main():
     ap.add_argument("--config", default="llama3_8b_gqa")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="smaller batch of the Llama-3-8B workload (profiling)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the chunked-prefill kernel on a pool holding just the chunk's sequence")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -192,6 +222,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, ws, rank)
+    if args.prefill_only:
+        return run_prefill_only(args, local)
 
     torch.cuda.set_device(local)
     dist = None
@@ -299,7 +331,7 @@ def main():
     dec_avg = float(np.mean(decode_ms))
     achieved = alg / (dec_avg / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name), "peak_source": peak_src,
             "kernel": "paged_decode_kernel", "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
 
     cpu = None
@@ -334,6 +366,57 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def run_prefill_only(args, local):
+    """The Llama-70B-shaped prefill chunk alone (512 queries at positions 8192..8703, 64 q / 8 kv
+    heads, head_dim 128, 16-token blocks) over a pool that holds only that sequence."""
+    import torch
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300 import workload as wl
+    from paged_kv_cache_71_gb300.runner import to_device
+    torch.cuda.set_device(local)
+    kv = "e4m3" if args.config.endswith("fp8") else "bf16"
+    NQ, q_start, Hq, Hkv, S, D = 512, 8192, 64, 8, 16, 128
+    rng = np.random.default_rng(wl.CONFIG_SEEDS["llama70b_mixed_bf16"])
+    kv_len = q_start + NQ
+    NB = -(-kv_len // S) + 16
+    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc.add_seq("chunk", kv_len)
+    table = to_device(np.array(alloc.tables["chunk"], np.int32))
+    dk = to_device(wl.random_values(rng, (NB, S, Hkv, D), kv))
+    dv = to_device(wl.random_values(rng, (NB, S, Hkv, D), kv))
+    dq = to_device(wl.random_values(rng, (NQ, Hq, D), "bf16"))
+    out = torch.empty_like(dq)
+    sc = wl.FP8_SCALE if kv == "e4m3" else 1.0
+    desc = B.CacheDesc.for_cache(dk, sc, sc)
+    scale = 1.0 / np.sqrt(D)
+
+    def run():
+        B.pkv_paged_prefill_chunk(out, dq, q_start, dk, dv, desc, table, kv_len, scale)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / args.steps * 1e3
+    flops = 4 * D * Hq * sum(q_start + i + 1 for i in range(NQ))
+    tflops = flops / (us * 1e-6) / 1e12
+    peak = 1941.1
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    print(json.dumps({"metric": "chunked-prefill tile TFLOP/s", "value": round(tflops, 1), "unit": "TFLOP/s",
+                      "us": round(us, 1), "flops": flops, "kv_dtype": kv, "steps": args.steps,
+                      "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                                   "unit": "TFLOP/s", "frac": round(tflops / peak, 4)}}), flush=True)
 
 
 def run_reference(args, ws, rank):

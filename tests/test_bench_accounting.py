@@ -1,0 +1,46 @@
+"""The benchmark's byte and flop accounting, pinned to the pages' capacity arithmetic."""
+import json
+import math
+import os
+
+import numpy as np
+
+import bench
+from paged_kv_cache_71_gb300 import workload as wl
+
+
+def test_kv_bytes_per_token_matches_capacity_example(golden_dir):
+    with open(os.path.join(golden_dir, "capacity_worked_example.json")) as f:
+        g = json.load(f)
+    per_tok = bench.kv_bytes_per_token(g["n_layers"], g["n_kv_heads"], g["head_dim"], g["dtype_bytes"])
+    assert per_tok == g["kv_bytes_per_token"] == 128 * 1024
+    assert per_tok * g["block_size"] == g["block_bytes"]
+    assert g["kv_pool_bytes"] // g["block_bytes"] == g["pool_blocks"]
+    assert g["pool_blocks"] * g["block_size"] == g["pool_tokens"]
+    req = g["request_blocks_at_end"]
+    assert math.ceil(req["tokens"] / g["block_size"]) == req["blocks"] and req["blocks"] * 16 == req["slots"]
+    assert round(g["pool_tokens"] / g["contiguous_reservation_tokens"]) == g["concurrency"]["contiguous"]
+    assert round(g["pool_tokens"] / req["slots"]) == g["concurrency"]["paged"]
+
+
+def test_decode_algorithmic_bytes_by_hand():
+    w = wl.tiny()
+    L = np.array([10, 6, 33, 1])
+    kv = int(L.sum()) * 2 * 2 * 64 * 4            # K and V, 2 kv heads, d = 64, fp32
+    qo = 2 * 4 * 4 * 64 * 4                       # q and out, 4 seqs x 4 heads x 64 x fp32
+    table = int(np.ceil(L / 4).sum()) * 4         # block-table entries read
+    assert bench.decode_algorithmic_bytes(w) == kv + qo + table + 4 * 4
+
+
+def test_prefill_flops_closed_form():
+    class PF:
+        q = np.zeros((512, 64, 128))
+        q_start = 8192
+
+    class W:
+        prefill = PF()
+        head_dim = 128
+        num_q_heads = 64
+    # sum_{i<512} (8193 + i) = 512 * 8193 + 511 * 512 / 2
+    keys = 512 * 8193 + 511 * 256
+    assert bench.prefill_flops(W()) == 4 * 128 * 64 * keys == 141742309376
