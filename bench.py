@@ -211,6 +211,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="smaller batch of the Llama-3-8B workload (profiling)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill kernel on a pool holding just the chunk's sequence")
+    ap.add_argument("--swap-only", action="store_true",
+                    help="time swap_blocks between the device pool and pinned host memory (Llama-3-8B block geometry)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -224,6 +226,8 @@ def main():
         return run_reference(args, ws, rank)
     if args.prefill_only:
         return run_prefill_only(args, local)
+    if args.swap_only:
+        return run_swap_only(args, local)
 
     torch.cuda.set_device(local)
     dist = None
@@ -417,6 +421,52 @@ def run_prefill_only(args, local):
                       "us": round(us, 1), "flops": flops, "kv_dtype": kv, "steps": args.steps,
                       "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                                    "unit": "TFLOP/s", "frac": round(tflops / peak, 4)}}), flush=True)
+
+
+def run_swap_only(args, local, nblocks: int = 2048):
+    """Swap 2048 scattered blocks (16 tokens x 8 kv heads x 128 x bf16, K and V: 64 KB each) out to pinned
+    host memory and back in; a contiguous pinned copy of the same bytes is timed beside it."""
+    import torch
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300 import workload as wl
+    from paged_kv_cache_71_gb300.runner import to_device
+    torch.cuda.set_device(local)
+    rng = np.random.default_rng(7110)
+    NB, S, Hkv, D = 8192, 16, 8, 128
+    dk = torch.empty((NB, S, Hkv, D), dtype=torch.bfloat16, device="cuda").normal_()
+    dv = torch.empty_like(dk).normal_()
+    hk = torch.empty((nblocks, S, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    out_pairs = to_device(np.stack([rng.choice(NB, nblocks, replace=False), rng.permutation(nblocks)], 1).astype(np.int64))
+    in_pairs = to_device(np.stack([rng.permutation(nblocks), rng.choice(NB, nblocks, replace=False)], 1).astype(np.int64))
+    desc = B.CacheDesc.for_cache(dk)
+    moved = 2 * nblocks * S * Hkv * D * 2
+    ref_dev = torch.empty(moved // 2, dtype=torch.bfloat16, device="cuda")
+    ref_host = torch.empty(moved // 2, dtype=torch.bfloat16).pin_memory()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps * 1e3
+
+    out_us = timed(lambda: B.pkv_swap_blocks(dk, dv, hk, hv, desc, out_pairs))
+    in_us = timed(lambda: B.pkv_swap_blocks(hk, hv, dk, dv, desc, in_pairs))
+    d2h_us = timed(lambda: ref_host.copy_(ref_dev, non_blocking=True))
+    h2d_us = timed(lambda: ref_dev.copy_(ref_host, non_blocking=True))
+    gbs = lambda us: round(moved / (us * 1e-6) / 1e9, 1)
+    print(json.dumps({"metric": "swap_blocks GB/s (device <-> pinned host)", "blocks": nblocks, "bytes": moved,
+                      "swap_out_us": round(out_us, 1), "swap_out_GBps": gbs(out_us),
+                      "swap_in_us": round(in_us, 1), "swap_in_GBps": gbs(in_us),
+                      "contiguous_d2h_GBps": gbs(d2h_us), "contiguous_h2d_GBps": gbs(h2d_us),
+                      "swap_out_frac_of_contiguous": round(d2h_us / out_us, 3),
+                      "swap_in_frac_of_contiguous": round(h2d_us / in_us, 3)}), flush=True)
 
 
 def run_reference(args, ws, rank):

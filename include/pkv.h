@@ -219,6 +219,27 @@ pkv_status pkv_paged_attention_decode_static_scratch(
     const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
     int32_t num_splits, int32_t max_context_len, int32_t* device_error, void* stream);
 
+/*
+ * Swap whole blocks between two pools, for preemption by swapping ("从
+ * PagedAttention 到 Chunked Prefill" §3.1 and "3.3 批处理与内存管理",
+ * scheduling section: a preempted sequence's KV blocks move to CPU memory
+ * and come back when it is resumed).  For each pair i:
+ *   dst_k[dst_i] = src_k[src_i];  dst_v[dst_i] = src_v[src_i]   (whole blocks, bit-exact)
+ * Either pool may be device memory or host memory the device can reach
+ * (cudaHostAlloc / cudaHostRegister memory; any host memory on devices with
+ * pageable-memory access, such as Grace-attached GPUs); the copies run in one
+ * kernel over NVLink-C2C / PCIe.  `cache` gives the block geometry and dtype
+ * (its num_blocks is not used); src_num_blocks / dst_num_blocks bound the ids.
+ *   block_mapping: int64 [num_pairs][2] = (src, dst), device-accessible memory.
+ * Destination blocks must be distinct; out-of-range ids set
+ * PKV_DEVERR_BAD_BLOCK and that pair is skipped.  Pointers that the device
+ * cannot dereference are rejected with PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks, void* dst_k,
+                           void* dst_v, int32_t dst_num_blocks, const pkv_cache_desc* cache,
+                           const int64_t* block_mapping, int32_t num_pairs, int32_t* device_error,
+                           void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* pkv_status_string(pkv_status status);
 

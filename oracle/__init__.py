@@ -69,6 +69,8 @@ def _load():
         lib.orc_reshape_and_cache.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, f32, f32]
         lib.orc_copy_blocks.restype = i32
         lib.orc_copy_blocks.argtypes = [P, P, ctypes.c_size_t, i32, P, i32]
+        lib.orc_swap_blocks.restype = i32
+        lib.orc_swap_blocks.argtypes = [P, P, i32, P, P, i32, ctypes.c_size_t, P, i32]
         lib.orc_paged_attention_decode.restype = i32
         lib.orc_paged_attention_decode.argtypes = [P, P, i32, P, P, i32, f64, f64, i32, i32, i32, i32,
                                                    P, i32, P, i32, i32, f64, P, i32, i32]
@@ -169,6 +171,16 @@ def copy_blocks(k_cache, v_cache, block_mapping):
     block_bytes = k_cache[0].nbytes
     st = lib.orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), block_bytes, NB, _ptr(bm), bm.shape[0])
     return _check(st, "copy_blocks", allow=(3,))
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping):
+    """Copy whole blocks from one pool to another (src -> dst pairs, in order), in place."""
+    lib = _load()
+    bm = np.ascontiguousarray(block_mapping, dtype=np.int64).reshape(-1, 2)
+    assert src_k[0].nbytes == dst_k[0].nbytes
+    st = lib.orc_swap_blocks(_ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
+                             src_k[0].nbytes, _ptr(bm), bm.shape[0])
+    return _check(st, "swap_blocks", allow=(3,))
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, *,

@@ -269,6 +269,30 @@ int orc_copy_blocks(void *k_cache, void *v_cache, size_t block_bytes, int NB,
     return status;
 }
 
+/* Swap blocks between two pools (preemption: a preempted sequence's KV is
+ * swapped out to CPU memory and back in later -- "从 PagedAttention 到 Chunked
+ * Prefill" §3.1; "3.3 批处理与内存管理", scheduling and preemption).  For each
+ * (src, dst) pair, block dst of the destination pool becomes a byte copy of
+ * block src of the source pool, for K and for V. */
+int orc_swap_blocks(const void *src_k, const void *src_v, int src_nb, void *dst_k,
+                    void *dst_v, int dst_nb, size_t block_bytes,
+                    const int64_t *pairs, int n)
+{
+    int status = ORC_OK;
+    for (int i = 0; i < n; ++i) {
+        int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+        if (s < 0 || s >= src_nb || d < 0 || d >= dst_nb) {
+            status = ORC_BAD_BLOCK;
+            continue;
+        }
+        memcpy((char *)dst_k + (size_t)d * block_bytes,
+               (const char *)src_k + (size_t)s * block_bytes, block_bytes);
+        memcpy((char *)dst_v + (size_t)d * block_bytes,
+               (const char *)src_v + (size_t)s * block_bytes, block_bytes);
+    }
+    return status;
+}
+
 /* ------------------------------------------------------------------ */
 /* Gather and textbook attention                                        */
 /* ------------------------------------------------------------------ */

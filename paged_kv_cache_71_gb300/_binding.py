@@ -67,8 +67,10 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_attention_decode_static_scratch.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32,
                                                             P, P]
     L.pkv_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, D, P, i32, i32, f32, P, P]
+    L.pkv_swap_blocks.argtypes = [P, P, i32, P, P, i32, D, P, i32, P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
-                 "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch", "pkv_paged_prefill_chunk"):
+                 "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch", "pkv_paged_prefill_chunk",
+                 "pkv_swap_blocks"):
         getattr(L, name).restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -169,6 +171,15 @@ def pkv_copy_blocks(k_cache, v_cache, cache: CacheDesc, block_mapping, device_er
     _check(lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), ctypes.byref(cache), _ptr(block_mapping),
                                  int(block_mapping.shape[0]), _ptr(device_error), _stream(stream)),
            "pkv_copy_blocks")
+
+
+def pkv_swap_blocks(src_k, src_v, dst_k, dst_v, cache: CacheDesc, block_mapping, device_error=None,
+                    stream=None) -> None:
+    """Whole-block copies between two pools (device or pinned host memory)."""
+    _check(lib().pkv_swap_blocks(_ptr(src_k), _ptr(src_v), int(src_k.shape[0]), _ptr(dst_k), _ptr(dst_v),
+                                 int(dst_k.shape[0]), ctypes.byref(cache), _ptr(block_mapping),
+                                 int(block_mapping.shape[0]), _ptr(device_error), _stream(stream)),
+           "pkv_swap_blocks")
 
 
 def pkv_status_string(status: int) -> str:

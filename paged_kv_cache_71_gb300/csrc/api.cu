@@ -287,6 +287,53 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache
     return PKV_OK;
 }
 
+// True when the device can dereference p (device, managed or mapped host memory, or any host
+// memory on a device with pageable-memory access such as a Grace-attached GPU).
+static bool device_accessible(const void* p, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return true;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer == p;
+    int pageable = 0;
+    cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+    return pageable != 0;
+}
+
+PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks, void* dst_k,
+                                   void* dst_v, int32_t dst_num_blocks, const pkv_cache_desc* cache,
+                                   const int64_t* block_mapping, int32_t num_pairs, int32_t* device_error,
+                                   void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_pairs=%d src_num_blocks=%d dst_num_blocks=%d)", num_pairs,
+                    src_num_blocks, dst_num_blocks);
+    if (num_pairs == 0) return PKV_OK;
+    if (num_pairs > (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d too large", num_pairs);
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_mapping) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+        return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(block_mapping) & 7u) != 0)
+        return fail(PKV_ERR_INVALID_ARG, "block_mapping must be 8-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const void* ptrs[5] = {src_k, src_v, dst_k, dst_v, block_mapping};
+    for (const void* p : ptrs)
+        if (!device_accessible(p, dev))
+            return fail(PKV_ERR_INVALID_ARG, "pointer %p is not accessible from the device (pin or register it)", p);
+    const int64_t block_bytes = static_cast<int64_t>(cache->block_size) * cache->num_kv_heads * cache->head_dim *
+                                elem_bytes(cache->dtype);
+    e = launch_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks, block_mapping, num_pairs,
+                           block_bytes, device_error, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "swap_blocks launch");
+    return PKV_OK;
+}
+
 PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32_t num_seqs,
                                                       int32_t num_q_heads, int32_t num_splits, size_t* bytes) {
     g_detail[0] = 0;

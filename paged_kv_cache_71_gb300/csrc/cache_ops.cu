@@ -159,3 +159,57 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* mapp
 }
 
 }  // namespace pkv
+
+namespace pkv {
+
+// ------------------------------------------------------------------ swap_blocks
+//
+// Preemption by swapping ("从 PagedAttention 到 Chunked Prefill" §3.1): a
+// preempted sequence's blocks move to CPU memory and back.  On GB300 the
+// Grace memory is reachable from the GPU over NVLink-C2C, so one kernel
+// gathers all pairs with 16-byte loads and stores, whichever side is host
+// memory.  One CTA per (pair, tensor).
+
+__global__ void __launch_bounds__(256) swap_blocks_kernel(const uint8_t* __restrict__ src_k,
+                                                          const uint8_t* __restrict__ src_v,
+                                                          uint8_t* __restrict__ dst_k, uint8_t* __restrict__ dst_v,
+                                                          const int64_t* __restrict__ mapping, int num_pairs,
+                                                          int src_nb, int dst_nb, int64_t block_bytes, int32_t* err) {
+    const int pair = blockIdx.x >> 1;
+    const int kv = blockIdx.x & 1;
+    if (pair >= num_pairs) return;
+    const int64_t src = mapping[2 * pair];
+    const int64_t dst = mapping[2 * pair + 1];
+    if (src < 0 || src >= src_nb || dst < 0 || dst >= dst_nb) {
+        if (kv == 0 && threadIdx.x == 0) raise_error(err, PKV_DEVERR_BAD_BLOCK);
+        return;
+    }
+    const uint4* s = reinterpret_cast<const uint4*>((kv ? src_v : src_k) + src * block_bytes);
+    uint4* d = reinterpret_cast<uint4*>((kv ? dst_v : dst_k) + dst * block_bytes);
+    const int64_t nvec = block_bytes / 16;
+    constexpr int U = 8;
+    for (int64_t i = threadIdx.x; i < nvec; i += static_cast<int64_t>(blockDim.x) * U) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = i + static_cast<int64_t>(u) * blockDim.x;
+            if (j < nvec) r[u] = __ldcs(s + j);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t j = i + static_cast<int64_t>(u) * blockDim.x;
+            if (j < nvec) __stcs(d + j, r[u]);
+        }
+    }
+}
+
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, int src_nb, void* dst_k, void* dst_v,
+                               int dst_nb, const int64_t* mapping, int num_pairs, int64_t block_bytes, int32_t* err,
+                               cudaStream_t stream) {
+    swap_blocks_kernel<<<2 * num_pairs, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src_k), static_cast<const uint8_t*>(src_v), static_cast<uint8_t*>(dst_k),
+        static_cast<uint8_t*>(dst_v), mapping, num_pairs, src_nb, dst_nb, block_bytes, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -13,4 +13,8 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, int s
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* mapping, int num_pairs, int num_blocks,
                                int64_t block_bytes, int32_t* err, cudaStream_t stream);
 
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, int src_nb, void* dst_k, void* dst_v,
+                               int dst_nb, const int64_t* mapping, int num_pairs, int64_t block_bytes, int32_t* err,
+                               cudaStream_t stream);
+
 }  // namespace pkv

@@ -381,3 +381,25 @@ def test_copy_blocks_page_example(golden_dir):
     untouched = [b for b in range(8) if b not in {d for _, d in g["cow_pairs"]}]
     assert (kc[untouched] == k0[untouched]).all() and (vc[untouched] == v0[untouched]).all()
     assert oracle.copy_blocks(kc, vc, np.array([[0, 8]], np.int64)) == 3
+
+
+def test_swap_blocks_round_trip_and_agrees_with_copy_blocks():
+    rng = np.random.default_rng(16)
+    dev_k = rng.standard_normal((10, 4, 2, 8)).astype(np.float32)
+    dev_v = rng.standard_normal((10, 4, 2, 8)).astype(np.float32)
+    host_k = np.zeros((6, 4, 2, 8), np.float32)
+    host_v = np.zeros_like(host_k)
+    out_pairs = np.array([[7, 0], [2, 5], [9, 3]], np.int64)
+    oracle.swap_blocks(dev_k, dev_v, host_k, host_v, out_pairs)
+    k2, v2 = np.zeros_like(dev_k), np.zeros_like(dev_v)
+    oracle.swap_blocks(host_k, host_v, k2, v2, out_pairs[:, ::-1].copy())
+    for src, _ in out_pairs:
+        assert (k2[src] == dev_k[src]).all() and (v2[src] == dev_v[src]).all()
+    # within one pool, a swap from a snapshot equals copy_blocks
+    pairs = np.array([[1, 4], [3, 8]], np.int64)
+    a_k, a_v = dev_k.copy(), dev_v.copy()
+    oracle.copy_blocks(a_k, a_v, pairs)
+    b_k, b_v = dev_k.copy(), dev_v.copy()
+    oracle.swap_blocks(dev_k.copy(), dev_v.copy(), b_k, b_v, pairs)
+    assert (a_k == b_k).all() and (a_v == b_v).all()
+    assert oracle.swap_blocks(dev_k, dev_v, host_k, host_v, np.array([[0, 6]], np.int64)) == 3
