@@ -213,6 +213,8 @@ def main():
                     help="time only the chunked-prefill kernel on a pool holding just the chunk's sequence")
     ap.add_argument("--swap-only", action="store_true",
                     help="time swap_blocks between the device pool and pinned host memory (Llama-3-8B block geometry)")
+    ap.add_argument("--hash-only", action="store_true",
+                    help="time the chained block content hashes of the Llama-3-8B batch's token ids")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -228,6 +230,8 @@ def main():
         return run_prefill_only(args, local)
     if args.swap_only:
         return run_swap_only(args, local)
+    if args.hash_only:
+        return run_hash_only(args, local)
 
     torch.cuda.set_device(local)
     dist = None
@@ -467,6 +471,38 @@ def run_swap_only(args, local, nblocks: int = 2048):
                       "contiguous_d2h_GBps": gbs(d2h_us), "contiguous_h2d_GBps": gbs(h2d_us),
                       "swap_out_frac_of_contiguous": round(d2h_us / out_us, 3),
                       "swap_in_frac_of_contiguous": round(h2d_us / in_us, 3)}), flush=True)
+
+
+def run_hash_only(args, local):
+    """Content hashes of every full 16-token block of 256 sequences with the Llama-3-8B lengths."""
+    import torch
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300 import workload as wl
+    from paged_kv_cache_71_gb300.runner import to_device
+    torch.cuda.set_device(local)
+    rng = np.random.default_rng(wl.CONFIG_SEEDS["llama3_8b_gqa"])
+    lens = wl.lognormal_lengths(rng, 256)
+    S = 16
+    toks = to_device(rng.integers(0, 128000, int(lens.sum())).astype(np.int32))
+    cu = to_device(np.concatenate([[0], np.cumsum(lens)]).astype(np.int64))
+    nfull = lens // S
+    offs = to_device(np.concatenate([[0], np.cumsum(nfull)[:-1]]).astype(np.int64))
+    out = torch.zeros(int(nfull.sum()), dtype=torch.int64, device="cuda")
+    run = lambda: B.pkv_block_hashes(toks, cu, S, offs, out)
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        run()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / args.steps * 1e3
+    print(json.dumps({"metric": "block content hashes per second", "blocks": int(nfull.sum()),
+                      "tokens": int(lens.sum()), "us": round(us, 1),
+                      "blocks_per_s": round(int(nfull.sum()) / (us * 1e-6)),
+                      "token_GBps": round(4 * int(lens.sum()) / (us * 1e-6) / 1e9, 2)}), flush=True)
 
 
 def run_reference(args, ws, rank):

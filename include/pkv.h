@@ -240,6 +240,26 @@ pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num
                            const int64_t* block_mapping, int32_t num_pairs, int32_t* device_error,
                            void* stream);
 
+/*
+ * Content hashes of full blocks, for hash-based prefix caching ("3.3
+ * 批处理与内存管理", section "前缀缓存与 RadixAttention": each full block is
+ * identified by its tokens together with the hash of all blocks before it; a
+ * new request reuses every leading block whose hash is cached).  The pages
+ * name no hash function; this one is FNV-1a, 64-bit, over little-endian bytes:
+ *   d_j = FNV-1a(token ids of block j, 4 bytes each)
+ *   h_j = FNV-1a(h_{j-1} as 8 bytes (0 before the first block) ++ d_j as 8 bytes)
+ * Sequence s has tokens token_ids[cu_tokens[s] .. cu_tokens[s+1]) and
+ * floor(L_s / block_size) full blocks; a partial last block has no hash.
+ * Hash j of sequence s goes to hashes[out_offsets[s] + j] (out_offsets is
+ * normally the exclusive prefix sum of the full-block counts).  Sequences
+ * whose hashes would fall outside [0, hashes_capacity) set
+ * PKV_DEVERR_BAD_SLOT and are skipped; a negative length sets
+ * PKV_DEVERR_BAD_LENGTH.  All pointers are device memory.
+ */
+pkv_status pkv_block_hashes(const int32_t* token_ids, const int64_t* cu_tokens, int32_t num_seqs,
+                            int32_t block_size, const int64_t* out_offsets, uint64_t* hashes,
+                            int64_t hashes_capacity, int32_t* device_error, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* pkv_status_string(pkv_status status);
 

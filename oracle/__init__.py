@@ -71,6 +71,10 @@ def _load():
         lib.orc_copy_blocks.argtypes = [P, P, ctypes.c_size_t, i32, P, i32]
         lib.orc_swap_blocks.restype = i32
         lib.orc_swap_blocks.argtypes = [P, P, i32, P, P, i32, ctypes.c_size_t, P, i32]
+        lib.orc_fnv1a64.restype = ctypes.c_uint64
+        lib.orc_fnv1a64.argtypes = [P, ctypes.c_size_t, ctypes.c_uint64]
+        lib.orc_block_hashes.restype = None
+        lib.orc_block_hashes.argtypes = [P, P, i32, i32, P, P]
         lib.orc_paged_attention_decode.restype = i32
         lib.orc_paged_attention_decode.argtypes = [P, P, i32, P, P, i32, f64, f64, i32, i32, i32, i32,
                                                    P, i32, P, i32, i32, f64, P, i32, i32]
@@ -181,6 +185,31 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, block_mapping):
     st = lib.orc_swap_blocks(_ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k), _ptr(dst_v), dst_k.shape[0],
                              src_k[0].nbytes, _ptr(bm), bm.shape[0])
     return _check(st, "swap_blocks", allow=(3,))
+
+
+FNV_OFFSET_BASIS = 14695981039346656037
+
+
+def fnv1a64(data: bytes, h: int = FNV_OFFSET_BASIS) -> int:
+    lib = _load()
+    buf = np.frombuffer(bytes(data), dtype=np.uint8).copy() if len(data) else np.zeros(1, np.uint8)
+    return int(lib.orc_fnv1a64(_ptr(buf), len(data), h))
+
+
+def block_hashes(tokens, cu_tokens, block_size):
+    """Chained content hashes of every full block of every sequence (uint64, concatenated)."""
+    lib = _load()
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_tokens, dtype=np.int64)
+    B = cu.shape[0] - 1
+    nfull = (cu[1:] - cu[:-1]) // block_size
+    offs = np.zeros(B, np.int64)
+    if B > 1:
+        offs[1:] = np.cumsum(nfull)[:-1]
+    out = np.zeros(max(1, int(nfull.sum())), np.uint64)
+    lib.orc_block_hashes(_ptr(tok if tok.size else np.zeros(1, np.int32)), _ptr(cu), B, int(block_size),
+                         _ptr(offs), _ptr(out))
+    return out[: int(nfull.sum())]
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, *,

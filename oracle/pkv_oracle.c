@@ -294,6 +294,63 @@ int orc_swap_blocks(const void *src_k, const void *src_v, int src_nb, void *dst_
 }
 
 /* ------------------------------------------------------------------ */
+/* Content hashes of full blocks (prefix caching)                       */
+/* ------------------------------------------------------------------ */
+
+/* FNV-1a, 64-bit (Fowler-Noll-Vo): start from the offset basis
+ * 14695981039346656037; for each byte, xor it in, then multiply by the
+ * prime 1099511628211 modulo 2^64. */
+uint64_t orc_fnv1a64(const uint8_t *bytes, size_t n, uint64_t h)
+{
+    for (size_t i = 0; i < n; ++i) {
+        h ^= (uint64_t)bytes[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+#define ORC_FNV_BASIS 14695981039346656037ull
+
+static void put_le64(uint8_t *b, uint64_t v)
+{
+    for (int i = 0; i < 8; ++i)
+        b[i] = (uint8_t)(v >> (8 * i));
+}
+
+/* Hash-based prefix caching ("3.3 批处理与内存管理", "前缀缓存与
+ * RadixAttention"): every FULL block is identified by its own tokens together
+ * with the hash of all blocks before it.  Definition used here:
+ *   d_j = FNV-1a-64 over the block's S token ids, each as 4 little-endian bytes
+ *   h_0 = FNV-1a-64 over (8 zero bytes) ++ (d_0 as 8 little-endian bytes)
+ *   h_j = FNV-1a-64 over (h_{j-1} as 8 LE bytes) ++ (d_j as 8 LE bytes)
+ * Sequence s has tokens [cu_tokens[s], cu_tokens[s+1]) and floor(L_s / S) full
+ * blocks, whose hashes go to out[out_offsets[s] + j]. */
+void orc_block_hashes(const int32_t *tokens, const int64_t *cu_tokens, int B, int S,
+                      const int64_t *out_offsets, uint64_t *out)
+{
+    for (int s = 0; s < B; ++s) {
+        int64_t L = cu_tokens[s + 1] - cu_tokens[s];
+        int64_t nfull = L / S;
+        uint64_t prev = 0;
+        for (int64_t j = 0; j < nfull; ++j) {
+            uint64_t d = ORC_FNV_BASIS;
+            for (int t = 0; t < S; ++t) {
+                uint8_t b[4];
+                uint32_t v = (uint32_t)tokens[cu_tokens[s] + j * S + t];
+                for (int i = 0; i < 4; ++i)
+                    b[i] = (uint8_t)(v >> (8 * i));
+                d = orc_fnv1a64(b, 4, d);
+            }
+            uint8_t buf[16];
+            put_le64(buf, prev);
+            put_le64(buf + 8, d);
+            prev = orc_fnv1a64(buf, 16, ORC_FNV_BASIS);
+            out[out_offsets[s] + j] = prev;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Gather and textbook attention                                        */
 /* ------------------------------------------------------------------ */
 

@@ -68,9 +68,10 @@ def lib() -> ctypes.CDLL:
                                                             P, P]
     L.pkv_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, D, P, i32, i32, f32, P, P]
     L.pkv_swap_blocks.argtypes = [P, P, i32, P, P, i32, D, P, i32, P, P]
+    L.pkv_block_hashes.argtypes = [P, P, i32, i32, P, P, ctypes.c_int64, P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
                  "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch", "pkv_paged_prefill_chunk",
-                 "pkv_swap_blocks"):
+                 "pkv_swap_blocks", "pkv_block_hashes"):
         getattr(L, name).restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -180,6 +181,15 @@ def pkv_swap_blocks(src_k, src_v, dst_k, dst_v, cache: CacheDesc, block_mapping,
                                  int(dst_k.shape[0]), ctypes.byref(cache), _ptr(block_mapping),
                                  int(block_mapping.shape[0]), _ptr(device_error), _stream(stream)),
            "pkv_swap_blocks")
+
+
+def pkv_block_hashes(token_ids, cu_tokens, block_size: int, out_offsets, hashes, device_error=None,
+                     stream=None) -> None:
+    """Chained FNV-1a-64 content hashes of every full block (hashes: int64/uint64 device tensor)."""
+    _check(lib().pkv_block_hashes(_ptr(token_ids), _ptr(cu_tokens), int(cu_tokens.shape[0]) - 1, int(block_size),
+                                  _ptr(out_offsets), _ptr(hashes), int(hashes.numel()), _ptr(device_error),
+                                  _stream(stream)),
+           "pkv_block_hashes")
 
 
 def pkv_status_string(status: int) -> str:

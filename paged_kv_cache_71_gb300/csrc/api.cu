@@ -334,6 +334,27 @@ PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t
     return PKV_OK;
 }
 
+PKV_API pkv_status pkv_block_hashes(const int32_t* token_ids, const int64_t* cu_tokens, int32_t num_seqs,
+                                    int32_t block_size, const int64_t* out_offsets, uint64_t* hashes,
+                                    int64_t hashes_capacity, int32_t* device_error, void* stream) {
+    g_detail[0] = 0;
+    if (num_seqs < 0 || block_size <= 0 || hashes_capacity < 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_seqs=%d block_size=%d capacity=%lld)", num_seqs, block_size,
+                    static_cast<long long>(hashes_capacity));
+    if (num_seqs == 0) return PKV_OK;
+    if (!token_ids || !cu_tokens || !out_offsets || !hashes) return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if ((reinterpret_cast<uintptr_t>(cu_tokens) & 7u) || (reinterpret_cast<uintptr_t>(out_offsets) & 7u) ||
+        (reinterpret_cast<uintptr_t>(hashes) & 7u) || (reinterpret_cast<uintptr_t>(token_ids) & 3u))
+        return fail(PKV_ERR_INVALID_ARG, "misaligned pointer");
+    DeviceInfo di;
+    pkv_status st = device_info(&di);
+    if (st != PKV_OK) return st;
+    cudaError_t e = launch_block_hashes(token_ids, cu_tokens, num_seqs, block_size, out_offsets, hashes,
+                                        hashes_capacity, device_error, di.sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block_hashes launch");
+    return PKV_OK;
+}
+
 PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32_t num_seqs,
                                                       int32_t num_q_heads, int32_t num_splits, size_t* bytes) {
     g_detail[0] = 0;

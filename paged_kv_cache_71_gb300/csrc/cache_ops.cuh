@@ -17,4 +17,8 @@ cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, int src_nb,
                                int dst_nb, const int64_t* mapping, int num_pairs, int64_t block_bytes, int32_t* err,
                                cudaStream_t stream);
 
+cudaError_t launch_block_hashes(const int32_t* tokens, const int64_t* cu_tokens, int num_seqs, int block_size,
+                                const int64_t* out_offsets, uint64_t* out, int64_t capacity, int32_t* err,
+                                int num_sms, cudaStream_t stream);
+
 }  // namespace pkv

@@ -403,3 +403,34 @@ def test_swap_blocks_round_trip_and_agrees_with_copy_blocks():
     oracle.swap_blocks(dev_k.copy(), dev_v.copy(), b_k, b_v, pairs)
     assert (a_k == b_k).all() and (a_v == b_v).all()
     assert oracle.swap_blocks(dev_k, dev_v, host_k, host_v, np.array([[0, 6]], np.int64)) == 3
+
+
+def test_fnv1a64_published_vectors():
+    """FNV-1a 64-bit test vectors from the algorithm's reference description."""
+    assert oracle.fnv1a64(b"") == 0xCBF29CE484222325
+    assert oracle.fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert oracle.fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def test_block_hashes_chain_and_prefix_property():
+    """Equal prefixes give equal block hashes; a change in block j changes hashes j.. only;
+    partial last blocks get no hash; the chain is the stated two-level FNV-1a."""
+    rng = np.random.default_rng(30)
+    S = 4
+    a = rng.integers(0, 32000, 23).astype(np.int32)
+    b = a.copy()
+    b[13] += 1                       # block 3 differs
+    c = a[:9].copy()                 # 2 full blocks + 1 partial
+    toks = np.concatenate([a, b, c])
+    cu = np.array([0, 23, 46, 55], np.int64)
+    h = oracle.block_hashes(toks, cu, S)
+    ha, hb, hc = h[:5], h[5:10], h[10:]
+    assert len(h) == 5 + 5 + 2
+    assert (ha[:3] == hb[:3]).all() and (ha[3:] != hb[3:]).all()
+    assert (hc == ha[:2]).all()
+    # by hand, from the definition
+    d0 = oracle.fnv1a64(a[:4].astype("<i4").tobytes())
+    h0 = oracle.fnv1a64((0).to_bytes(8, "little") + d0.to_bytes(8, "little"))
+    d1 = oracle.fnv1a64(a[4:8].astype("<i4").tobytes())
+    h1 = oracle.fnv1a64(h0.to_bytes(8, "little") + d1.to_bytes(8, "little"))
+    assert int(ha[0]) == h0 and int(ha[1]) == h1
