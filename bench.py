@@ -175,7 +175,7 @@ def time_oracle(w, steps: int = 1, max_seconds: float = 20.0) -> dict:
     oracle.build()
     threads = oracle.max_threads()
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
-    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3}[w.kv_dtype]
+    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}[w.kv_dtype]
     done, t0 = 0, time.perf_counter()
     while done < steps:
         oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc, cache_dtype=cache_dt,

@@ -57,7 +57,8 @@ typedef enum {
 typedef enum {
     PKV_F32 = 0,
     PKV_BF16 = 1,
-    PKV_FP8_E4M3 = 2   /* OCP E4M3 (bias 7, max 448, no inf), per-tensor scale */
+    PKV_FP8_E4M3 = 2,  /* OCP E4M3 (bias 7, max 448, no inf), per-tensor scale */
+    PKV_INT8 = 3       /* symmetric int8 in [-127, 127], per-tensor scale */
 } pkv_dtype;
 
 /* Bits OR-ed into *device_error by the kernels. */
@@ -73,8 +74,8 @@ typedef struct {
     int32_t num_kv_heads;  /* Hkv */
     int32_t head_dim;      /* D: 64 or 128 */
     int32_t dtype;         /* pkv_dtype of the cache elements */
-    float k_scale;         /* FP8 only: stored code * k_scale is the key value; 1 otherwise */
-    float v_scale;         /* FP8 only: same for values */
+    float k_scale;         /* FP8 / INT8: stored code * k_scale is the key value; 1 otherwise */
+    float v_scale;         /* FP8 / INT8: same for values */
 } pkv_cache_desc;
 
 /*
@@ -84,7 +85,10 @@ typedef struct {
  * "代码", append_token).  For token i with slot_mapping[i] >= 0:
  *   k_cache[slot / S][slot % S][h][:] = convert(k_new[i][h][:])   (same for v)
  * convert: same dtype -> bit copy; bf16 -> f32 exact; f32 -> bf16 round to
- * nearest even; -> FP8 E4M3: sat(RNE(x / scale)) with an fp32 division.
+ * nearest even; -> FP8 E4M3: sat(RNE(x / scale)) with an fp32 division;
+ * -> INT8: clamp(RNE(x / scale), -127, 127) with an fp32 division (the INT8
+ * KV quantisation of "从 PagedAttention 到 Chunked Prefill" §5.4 and the
+ * "INT8量化" row of "大模型推理的KV Cache优化全解", per-tensor scale).
  *   k_new, v_new: [num_tokens][num_kv_heads][head_dim] of src_dtype (f32 or bf16).
  * Tokens whose slot is beyond the pool set PKV_DEVERR_BAD_SLOT and are skipped.
  * Two tokens with the same slot race (one of them wins).
@@ -128,7 +132,7 @@ pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32
  * Any choice gives the same result up to fp32 rounding order.
  *
  *   q:   [num_seqs][num_q_heads][head_dim], q_dtype f32 (with an f32 cache)
- *        or bf16 (with a bf16 or FP8 cache); out has q's dtype and shape.
+ *        or bf16 (with a bf16, FP8 or INT8 cache); out has q's dtype and shape.
  *   max_context_len: an upper bound of context_lens (0 = use
  *        max_blocks_per_seq * block_size); only shapes the partitions.
  *   workspace: >= pkv_paged_attention_workspace_size bytes, 16-byte
@@ -156,12 +160,12 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
  *   out[i][hq] = softmax(scale * q[i][hq] . K[0 .. q_start_pos + i]^T) V[0 .. q_start_pos + i]
  * with K/V gathered through block_table (one sequence, ceil(kv_len / S)
  * entries).  Runs on the tensor cores: bf16 inputs, fp32 accumulation, the
- * softmax weights rounded to bf16 for the P.V product.  An FP8 cache is
- * widened to bf16 on chip (exactly) and its per-tensor scales are applied to
- * the scores and the output.
+ * softmax weights rounded to bf16 for the P.V product.  An FP8 or INT8 cache
+ * is widened to bf16 on chip (exactly) and its per-tensor scales are applied
+ * to the scores and the output.
  *   q, out: [num_q_tokens][num_q_heads][128] bf16.
  * scale must be positive.
- * Supported: bf16 queries, bf16 or FP8 cache, head_dim 128, block_size 8/16/32,
+ * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
  *   G = num_q_heads / num_kv_heads dividing 128.  No workspace.
  */
 pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,

@@ -22,7 +22,7 @@ _SRC = os.path.join(_HERE, "pkv_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, I8 = 0, 1, 2, 3
 _STATUS = {0: "ok", 1: "bad argument", 2: "slot out of range", 3: "block id out of range", 4: "out of memory"}
 
 _lock = threading.Lock()
@@ -63,6 +63,8 @@ def _load():
         lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.orc_f32_to_e4m3.restype = ctypes.c_uint8
         lib.orc_f32_to_e4m3.argtypes = [f32]
+        lib.orc_f32_to_i8.restype = ctypes.c_int8
+        lib.orc_f32_to_i8.argtypes = [f32]
         lib.orc_lookup.restype = i32
         lib.orc_lookup.argtypes = [P, i64, i32, ctypes.POINTER(ctypes.c_int)]
         lib.orc_reshape_and_cache.restype = i32
@@ -103,7 +105,9 @@ def _dtype_code(a: np.ndarray, declared: int | None = None) -> int:
         return BF16
     if a.dtype == np.uint8:
         return E4M3
-    raise TypeError(f"oracle: unsupported array dtype {a.dtype} (f32, bf16 as uint16, e4m3 as uint8)")
+    if a.dtype == np.int8:
+        return I8
+    raise TypeError(f"oracle: unsupported array dtype {a.dtype} (f32, bf16 as uint16, e4m3 as uint8, int8)")
 
 
 def _check(status: int, what: str, allow=()):
@@ -136,6 +140,13 @@ def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
     lib = _load()
     flat = np.ascontiguousarray(x, dtype=np.float32).ravel()
     return np.array([lib.orc_f32_to_e4m3(float(v)) for v in flat], dtype=np.uint8).reshape(np.shape(x))
+
+
+def f32_to_i8(y: np.ndarray) -> np.ndarray:
+    """Symmetric INT8 code of already-divided values y (RNE, clamped to +-127)."""
+    lib = _load()
+    flat = np.ascontiguousarray(y, dtype=np.float32).ravel()
+    return np.array([lib.orc_f32_to_i8(float(v)) for v in flat], dtype=np.int8).reshape(np.shape(y))
 
 
 def lookup(table: np.ndarray, p: int, block_size: int) -> tuple[int, int]:

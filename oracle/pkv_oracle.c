@@ -39,6 +39,8 @@
  *     fp32 scale per tensor: code = sat(RNE(x / scale)), value = code * scale;
  *     x / scale is an fp32 division, the precision the kernel uses to decide
  *     the code;
+ *   - INT8 is symmetric: code = clamp(RNE(x / scale), -127, 127), value =
+ *     code * scale, one fp32 scale per tensor;
  *   - bf16 values widen exactly; fp32 -> bf16 is round-to-nearest-even.
  */
 #include <math.h>
@@ -49,7 +51,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_I8 = 3 };
 
 enum {
     ORC_OK = 0,
@@ -152,6 +154,27 @@ uint8_t orc_f32_to_e4m3(float x)
     return (uint8_t)(sign | best);
 }
 
+/* Symmetric INT8 with a per-tensor scale ("从 PagedAttention 到 Chunked
+ * Prefill" §5.4; the INT8 row of "大模型推理的KV Cache优化全解"): the code is
+ * x / scale (an fp32 division) rounded to the nearest integer, ties to even,
+ * and clamped to [-127, 127]; the value is code * scale.  NaN maps to 0. */
+int8_t orc_f32_to_i8(float y)
+{
+    if (isnan(y))
+        return 0;
+    double r = rint((double)y); /* default rounding mode: ties to even */
+    if (r > 127.0)
+        r = 127.0;
+    if (r < -127.0)
+        r = -127.0;
+    return (int8_t)r;
+}
+
+static int narrow_dt(int dt)
+{
+    return dt == ORC_E4M3 || dt == ORC_I8;
+}
+
 static size_t elem_size(int dt)
 {
     return dt == ORC_F32 ? 4 : dt == ORC_BF16 ? 2 : 1;
@@ -170,6 +193,8 @@ static double load_elem(const void *base, int dt, size_t i, double fp8_scale)
         memcpy(&b, (const char *)base + 2 * i, 2);
         return orc_bf16_to_double(b);
     }
+    if (dt == ORC_I8)
+        return (double)((const int8_t *)base)[i] * fp8_scale;
     return orc_e4m3_to_double(((const uint8_t *)base)[i]) * fp8_scale;
 }
 
@@ -204,7 +229,7 @@ int orc_reshape_and_cache(const void *k_new, const void *v_new, int src_dt,
 {
     if (T < 0 || NB <= 0 || S <= 0 || Hkv <= 0 || D <= 0)
         return ORC_BAD_ARG;
-    if (src_dt == ORC_E4M3)
+    if (narrow_dt(src_dt))
         return ORC_BAD_ARG;
     int status = ORC_OK;
     const size_t row = (size_t)Hkv * D;
@@ -235,6 +260,9 @@ int orc_reshape_and_cache(const void *k_new, const void *v_new, int src_dt,
                 } else if (cache_dt == ORC_BF16) {
                     uint16_t b = orc_f32_to_bf16(x);
                     memcpy((char *)dst + 2 * di, &b, 2);
+                } else if (cache_dt == ORC_I8) {
+                    float y = x / scale;
+                    ((int8_t *)dst)[di] = orc_f32_to_i8(y);
                 } else {
                     float y = x / scale;
                     ((uint8_t *)dst)[di] = orc_f32_to_e4m3(y);
@@ -433,8 +461,8 @@ int orc_paged_attention_decode(double *out, const void *q, int q_dt,
         nseqs = B;
     const int G = Hq / Hkv;
     orc_cache c = {k_cache, v_cache, cache_dt,
-                   cache_dt == ORC_E4M3 ? k_scale : 1.0,
-                   cache_dt == ORC_E4M3 ? v_scale : 1.0, NB, S, Hkv, D};
+                   narrow_dt(cache_dt) ? k_scale : 1.0,
+                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D};
     int status = ORC_OK;
     const long nunits = (long)nseqs * Hkv;
 #ifdef _OPENMP
@@ -502,8 +530,8 @@ int orc_paged_prefill_chunk(double *out, const void *q, int q_dt, int NQ,
         nrows = NQ;
     const int G = Hq / Hkv;
     orc_cache c = {k_cache, v_cache, cache_dt,
-                   cache_dt == ORC_E4M3 ? k_scale : 1.0,
-                   cache_dt == ORC_E4M3 ? v_scale : 1.0, NB, S, Hkv, D};
+                   narrow_dt(cache_dt) ? k_scale : 1.0,
+                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D};
     int status = ORC_OK;
 #ifdef _OPENMP
     if (nthreads > 0)

@@ -14,7 +14,7 @@
 
 namespace pkv {
 
-// The kernel instantiations live in decode_{f32,bf16,fp8}_s{4,8,16,32}.cu.
+// The kernel instantiations live in decode_{f32,bf16,fp8,i8}_s{4,8,16,32}.cu.
 #define PKV_EXTERN(G_, D_, S_, KV_, QT_)                                                                    \
     extern template cudaError_t launch_paged_decode<G_, D_, S_, KV_, QT_>(                                   \
         const CUtensorMap&, const CUtensorMap&, const DecodeArgs&, int, int, size_t, cudaStream_t);
@@ -27,6 +27,7 @@ namespace pkv {
 PKV_EXTERN_ALL(KvF32, KvF32)
 PKV_EXTERN_ALL(KvBF16, KvBF16)
 PKV_EXTERN_ALL(KvE4M3, KvBF16)
+PKV_EXTERN_ALL(KvI8, KvBF16)
 #undef PKV_EXTERN_ALL
 #undef PKV_EXTERN_GD
 #undef PKV_EXTERN
@@ -141,7 +142,10 @@ static pkv_status tensor_map_sw128(CUtensorMap* map, const void* base, bool fp8,
 
 // ------------------------------------------------------------------ validation helpers
 
-static int elem_bytes(int dt) { return dt == PKV_F32 ? 4 : dt == PKV_BF16 ? 2 : dt == PKV_FP8_E4M3 ? 1 : 0; }
+static int elem_bytes(int dt) {
+    return dt == PKV_F32 ? 4 : dt == PKV_BF16 ? 2 : (dt == PKV_FP8_E4M3 || dt == PKV_INT8) ? 1 : 0;
+}
+static bool narrow(int dt) { return dt == PKV_FP8_E4M3 || dt == PKV_INT8; }
 
 static pkv_status check_cache(const pkv_cache_desc* c) {
     if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
@@ -155,9 +159,9 @@ static pkv_status check_cache(const pkv_cache_desc* c) {
         return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
     if (static_cast<int64_t>(c->num_blocks) * c->block_size > INT32_MAX)
         return fail(PKV_ERR_OUT_OF_RANGE, "num_blocks * block_size exceeds 2^31-1");
-    if (c->dtype == PKV_FP8_E4M3 &&
+    if (narrow(c->dtype) &&
         !(c->k_scale > 0.f && c->v_scale > 0.f && c->k_scale < 3.0e38f && c->v_scale < 3.0e38f))
-        return fail(PKV_ERR_INVALID_ARG, "FP8 cache needs finite positive k_scale / v_scale");
+        return fail(PKV_ERR_INVALID_ARG, "FP8 / INT8 caches need finite positive k_scale / v_scale");
     return PKV_OK;
 }
 
@@ -404,9 +408,9 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
         return fail(PKV_ERR_OUT_OF_RANGE, "num_seqs * max_blocks_per_seq * num_kv_heads must stay below 2^31");
     if (!(scale == scale) || scale == 0.f) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and non-zero");
     const bool combo_ok = (q_dtype == PKV_F32 && cache->dtype == PKV_F32) ||
-                          (q_dtype == PKV_BF16 && (cache->dtype == PKV_BF16 || cache->dtype == PKV_FP8_E4M3));
+                          (q_dtype == PKV_BF16 && (cache->dtype == PKV_BF16 || narrow(cache->dtype)));
     if (!combo_ok)
-        return fail(PKV_ERR_UNSUPPORTED, "q dtype %d with cache dtype %d (supported: f32/f32, bf16/bf16, bf16/fp8)",
+        return fail(PKV_ERR_UNSUPPORTED, "q dtype %d with cache dtype %d (supported: f32/f32, bf16/bf16|fp8|int8)",
                     q_dtype, cache->dtype);
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
@@ -461,8 +465,8 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.NB = cache->num_blocks;
     a.part_blocks = part_blocks;
     const float kLog2e = 1.4426950408889634f;
-    a.q_mul = scale * kLog2e * (cache->dtype == PKV_FP8_E4M3 ? cache->k_scale : 1.f);
-    a.o_mul = cache->dtype == PKV_FP8_E4M3 ? cache->v_scale : 1.f;
+    a.q_mul = scale * kLog2e * (narrow(cache->dtype) ? cache->k_scale : 1.f);
+    a.o_mul = narrow(cache->dtype) ? cache->v_scale : 1.f;
     a.kv_bytes = static_cast<uint32_t>(S * D * kv_es);
     a.q_bytes = static_cast<uint32_t>(G * D * q_es);
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
@@ -499,8 +503,10 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
         e = dispatch_s<KvF32, KvF32>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     else if (cache->dtype == PKV_BF16)
         e = dispatch_s<KvBF16, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
-    else
+    else if (cache->dtype == PKV_FP8_E4M3)
         e = dispatch_s<KvE4M3, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
+    else
+        e = dispatch_s<KvI8, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
     return PKV_OK;
 }
@@ -522,9 +528,9 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     if (num_q_heads % Hkv != 0)
         return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
     const int G = num_q_heads / Hkv;
-    if (q_dtype != PKV_BF16 || (cache->dtype != PKV_BF16 && cache->dtype != PKV_FP8_E4M3))
-        return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports bf16 queries with a bf16 or FP8 cache");
-    const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+    if (q_dtype != PKV_BF16 || (cache->dtype != PKV_BF16 && !narrow(cache->dtype)))
+        return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports bf16 queries with a bf16, FP8 or INT8 cache");
+    const bool fp8 = narrow(cache->dtype);
     if (D != 128) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports head_dim 128");
     if (S < 8) return fail(PKV_ERR_UNSUPPORTED, "prefill chunk supports block_size 8, 16, 32");
     if (G > 128 || 128 % G != 0) return fail(PKV_ERR_UNSUPPORTED, "GQA group %d must divide 128", G);
@@ -559,7 +565,8 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
     a.out_mul = fp8 ? cache->v_scale : 1.f;
     a.timeout_ns = 2000000000ull;
-    cudaError_t e = launch_paged_prefill(qm, km, vm, a, fp8, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_paged_prefill(qm, km, vm, a, fp8 ? (cache->dtype == PKV_INT8 ? 2 : 1) : 0,
+                                         static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
     return PKV_OK;
 }

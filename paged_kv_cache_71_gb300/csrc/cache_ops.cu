@@ -41,6 +41,14 @@ __device__ __forceinline__ void convert8(const uint8_t* src, uint8_t* dst, float
             w[i] = static_cast<uint32_t>(float_to_bf16_bits(f[2 * i])) |
                    (static_cast<uint32_t>(float_to_bf16_bits(f[2 * i + 1])) << 16);
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (DST == PKV_INT8) {
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float y = f[i] / scale;  // IEEE fp32 division, then RNE to an integer, clamped to +-127
+            w[i / 4] |= static_cast<uint32_t>(float_to_s8_sym(y)) << (8 * (i % 4));
+        }
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
     } else {
         uint32_t w[2] = {0u, 0u};
 #pragma unroll
@@ -61,7 +69,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint8_t* _
                                                                 int row_elems, float k_scale, float v_scale,
                                                                 int32_t* err) {
     constexpr int SES = (SRC == PKV_F32) ? 4 : 2;
-    constexpr int DES = (DST == PKV_F32) ? 4 : (DST == PKV_BF16) ? 2 : 1;
+    constexpr int DES = (DST == PKV_F32) ? 4 : (DST == PKV_BF16) ? 2 : 1;  // FP8 and INT8: one byte
     const int vec_per_row = row_elems / 8;
     const long long total = static_cast<long long>(T) * 2 * vec_per_row;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
@@ -107,6 +115,8 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, int s
     PKV_RC(PKV_BF16, PKV_F32)
     PKV_RC(PKV_BF16, PKV_BF16)
     PKV_RC(PKV_BF16, PKV_FP8_E4M3)
+    PKV_RC(PKV_F32, PKV_INT8)
+    PKV_RC(PKV_BF16, PKV_INT8)
 #undef PKV_RC
     return cudaErrorInvalidValue;
 }

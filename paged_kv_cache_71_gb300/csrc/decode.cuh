@@ -54,6 +54,10 @@ struct KvE4M3 {
     static constexpr int es = 1;
     static constexpr int code = PKV_FP8_E4M3;
 };
+struct KvI8 {
+    static constexpr int es = 1;
+    static constexpr int code = PKV_INT8;
+};
 
 // Load CH bytes of KV elements from shared memory and widen to fp32 pairs.
 template <class KV, int CH>
@@ -78,6 +82,22 @@ __device__ __forceinline__ void load_kv_chunk(const uint8_t* p, float2 (&x)[CH /
             uint2 v = *reinterpret_cast<const uint2*>(p);
             x[0] = bf16x2_to_float2(v.x);
             x[1] = bf16x2_to_float2(v.y);
+        }
+    } else if constexpr (KV::code == PKV_INT8) {
+        if constexpr (CH == 16) {
+            uint4 v = *reinterpret_cast<const uint4*>(p);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                x[2 * i] = s8x2_to_float2(w[i], 0);
+                x[2 * i + 1] = s8x2_to_float2(w[i], 2);
+            }
+        } else {
+            uint2 v = *reinterpret_cast<const uint2*>(p);
+            x[0] = s8x2_to_float2(v.x, 0);
+            x[1] = s8x2_to_float2(v.x, 2);
+            x[2] = s8x2_to_float2(v.y, 0);
+            x[3] = s8x2_to_float2(v.y, 2);
         }
     } else {
         if constexpr (CH == 16) {

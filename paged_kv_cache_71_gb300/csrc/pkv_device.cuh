@@ -127,6 +127,24 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t w) {
     return __half22float2(h);
 }
 
+// Signed bytes b (of w, at byte index i0 and i0 + 1) -> two floats, exactly.
+// The byte with its sign bit flipped is v + 128 in [0, 255]; placed as the
+// low mantissa bits of 2^23 it reads 2^23 + v + 128, so one subtraction of
+// 2^23 + 128 gives v (both steps exact in fp32).
+__device__ __forceinline__ float2 s8x2_to_float2(uint32_t w, int i0) {
+    const uint32_t f = w ^ 0x80808080u;
+    const float a = __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7540u + i0));
+    const float b = __uint_as_float(__byte_perm(f, 0x4B000000u, 0x7540u + i0 + 1));
+    return make_float2(a - 8388736.0f, b - 8388736.0f);
+}
+
+// fp32 -> symmetric int8: round to nearest even, clamp to [-127, 127].
+__device__ __forceinline__ uint8_t float_to_s8_sym(float x) {
+    int r = __float2int_rn(x);
+    r = r < -127 ? -127 : (r > 127 ? 127 : r);
+    return static_cast<uint8_t>(static_cast<int8_t>(r));
+}
+
 // fp32 -> E4M3 with saturation to +-448, round to nearest even.
 __device__ __forceinline__ uint8_t float_to_e4m3_sat(float x) {
     uint16_t r;

@@ -61,10 +61,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 }  // namespace
 
-template <bool FP8>
+// NARROW: 0 = bf16 cache; 1 = FP8 E4M3 codes; 2 = INT8 codes (both widened to bf16 on chip).
+template <int NARROW>
 __global__ void __launch_bounds__(128, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+    constexpr bool FP8 = NARROW != 0;  // a one-byte cache, staged and widened
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(128, 1)
         }
     };
 
-    // FP8: widen the staged codes of one key tile into the bf16 stage st (exact; the
+    // FP8 / INT8: widen the staged codes of one key tile into the bf16 stage st (exact; the
     // per-tensor scales are applied to the scores and to the output instead).
     // Thread t converts key row t of K and of V; V rows of keys past the end become 0.
     auto widen_fp8 = [&](int st, int nvalid) {
@@ -150,8 +152,14 @@ __global__ void __launch_bounds__(128, 1)
                     const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float2 f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
-                        const float2 f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                        float2 f0, f1;
+                        if constexpr (NARROW == 2) {
+                            f0 = s8x2_to_float2(ws[i], 0);
+                            f1 = s8x2_to_float2(ws[i], 2);
+                        } else {
+                            f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                            f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                        }
                         o[2 * i] = pack_bf16x2_rn(f0.x, f0.y);
                         o[2 * i + 1] = pack_bf16x2_rn(f1.x, f1.y);
                     }
@@ -370,9 +378,9 @@ size_t prefill_smem_bytes(bool fp8) {
 }
 
 cudaError_t launch_paged_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                 const PrefillArgs& a, bool fp8, cudaStream_t stream) {
-    const size_t smem = prefill_smem_bytes(fp8);
-    auto kern = fp8 ? paged_prefill_kernel<true> : paged_prefill_kernel<false>;
+                                 const PrefillArgs& a, int narrow, cudaStream_t stream) {
+    const size_t smem = prefill_smem_bytes(narrow != 0);
+    auto kern = narrow == 2 ? paged_prefill_kernel<2> : (narrow == 1 ? paged_prefill_kernel<1> : paged_prefill_kernel<0>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int rows_q = kRows / a.G;

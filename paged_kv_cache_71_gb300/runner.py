@@ -13,7 +13,7 @@ import torch
 from . import _binding as B
 from .workload import Workload
 
-_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8, "i8": torch.int8}
 
 
 def to_device(a: np.ndarray, dtype: str | None = None, device="cuda") -> torch.Tensor:

@@ -18,7 +18,8 @@ new block when the last one is full, and a write into a shared (refcount >
 Value distributions (all seeded with ``numpy.random.default_rng``):
 Q, K, V ~ N(0, 1) drawn in float32 and rounded once to the storage dtype;
 FP8 E4M3 caches hold random codes (uniform sign and mantissa, exponent
-field uniform in [4, 10]) with a per-tensor scale of 0.25, so that no
+field uniform in [4, 10]) with a per-tensor scale of 0.25, and INT8 caches
+random codes uniform in [-127, 127] with a scale of 1/32, so that no
 quantiser is involved in making them.
 """
 from __future__ import annotations
@@ -108,9 +109,10 @@ class BlockAllocator:
 
 # ---------------------------------------------------------------- value generation
 
-DTYPES = ("f32", "bf16", "e4m3")
-_ELEM = {"f32": 4, "bf16": 2, "e4m3": 1}
+DTYPES = ("f32", "bf16", "e4m3", "i8")
+_ELEM = {"f32": 4, "bf16": 2, "e4m3": 1, "i8": 1}
 FP8_SCALE = 0.25
+INT8_SCALE = 1.0 / 32.0
 
 
 def elem_size(dtype: str) -> int:
@@ -134,13 +136,16 @@ def _fill_chunk(base: int, c: int, a: int, b: int, dtype: str, out: np.ndarray) 
 
 
 def random_values(rng: np.random.Generator, shape, dtype: str, chunk: int = 1 << 24) -> np.ndarray:
-    """N(0,1) values stored as float32 / bf16 bits (uint16) / random E4M3 codes (uint8).
+    """N(0,1) values stored as float32 / bf16 bits (uint16); random E4M3 codes (uint8) or
+    symmetric INT8 codes uniform in [-127, 127] (int8).
 
     Large arrays are drawn in fixed-size chunks, each from its own generator
     seeded by (a draw of ``rng``, chunk index), on a thread pool: the result
     depends only on ``rng``'s state, not on the number of threads."""
     shape = tuple(int(s) for s in shape)
     n = int(np.prod(shape)) if shape else 1
+    if dtype == "i8":
+        return rng.integers(-127, 128, size=n, dtype=np.int8).reshape(shape)
     if dtype == "e4m3":
         sign = rng.integers(0, 2, size=n, dtype=np.uint8)
         expo = rng.integers(4, 11, size=n, dtype=np.uint8)
@@ -208,10 +213,10 @@ class Workload:
 
 
 CONFIG_NAMES = ("tiny", "llama2_7b", "llama3_8b_gqa", "prefix_shared", "llama70b_mixed_bf16",
-                "llama70b_mixed_fp8")
+                "llama70b_mixed_fp8", "llama3_8b_gqa_int8")
 
 CONFIG_SEEDS = {"tiny": 7100, "llama2_7b": 7101, "llama3_8b_gqa": 7102, "prefix_shared": 7103,
-                "llama70b_mixed_bf16": 7104, "llama70b_mixed_fp8": 7104}
+                "llama70b_mixed_bf16": 7104, "llama70b_mixed_fp8": 7104, "llama3_8b_gqa_int8": 7102}
 
 
 def _pool_size(total_blocks: int, slack: float = 0.05) -> int:
@@ -240,7 +245,7 @@ def _decode_batch(name, lens, Hq, Hkv, D, S, kv_dtype, q_dtype, seed, exact_pool
     k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, len(lens), Hq, kv_dtype, q_dtype)
     k_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
     v_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
-    scale = FP8_SCALE if kv_dtype == "e4m3" else 1.0
+    scale = {"e4m3": FP8_SCALE, "i8": INT8_SCALE}.get(kv_dtype, 1.0)
     return Workload(name, seed, Hq, Hkv, D, S, kv_dtype, q_dtype, scale, scale, q, k_cache, v_cache,
                     alloc.padded_tables(sids), lens.astype(np.int32), k_new, v_new,
                     np.array(slots, dtype=np.int64), np.zeros((0, 2), dtype=np.int64),
@@ -264,12 +269,14 @@ def lognormal_lengths(rng, n, median=1024.0, sigma=1.0, lo=16, hi=8192) -> np.nd
     return np.clip(np.round(np.exp(rng.normal(np.log(median), sigma, size=n))), lo, hi).astype(np.int64)
 
 
-def llama3_8b_gqa(seed: int = CONFIG_SEEDS["llama3_8b_gqa"], batch: int = 256) -> Workload:
+def llama3_8b_gqa(seed: int = CONFIG_SEEDS["llama3_8b_gqa"], batch: int = 256, kv_dtype: str = "bf16") -> Workload:
     """Batch 256, 32 q / 8 kv heads, D=128, bf16, S=16, lengths lognormal (median 1024,
-    sigma 1) clipped to [16, 8192]; plus the cache write of the 256 new tokens."""
+    sigma 1) clipped to [16, 8192]; plus the cache write of the 256 new tokens.
+    kv_dtype "i8" gives the same batch over a symmetric INT8 cache."""
     rng = np.random.default_rng(seed)
     lens = lognormal_lengths(rng, batch)
-    return _decode_batch("llama3_8b_gqa", lens, 32, 8, 128, 16, "bf16", "bf16", seed + 1000)
+    name = "llama3_8b_gqa" + ("_int8" if kv_dtype == "i8" else "")
+    return _decode_batch(name, lens, 32, 8, 128, 16, kv_dtype, "bf16", seed + 1000)
 
 
 def prefix_shared(seed: int = CONFIG_SEEDS["prefix_shared"], batch: int = 128, prefix: int = 800,
@@ -365,4 +372,6 @@ def make(name: str, **kw) -> Workload:
         return llama70b_mixed("bf16", **kw)
     if name == "llama70b_mixed_fp8":
         return llama70b_mixed("e4m3", seed=CONFIG_SEEDS["llama70b_mixed_fp8"], **kw)
+    if name == "llama3_8b_gqa_int8":
+        return llama3_8b_gqa(kv_dtype="i8", **kw)
     raise KeyError(name)

@@ -4,6 +4,7 @@ Tolerances (stated for the decode output against the fp64 oracle):
   fp32 KV: max |gpu - ref| <= 1e-5
   bf16 KV: |gpu - ref| <= 2e-2 + 2e-2 |ref|   (fp32 accumulation, bf16 output)
   fp8  KV: |gpu - ref| <= 6e-2                 (oracle reads the same dequantised codes)
+  int8 KV: |gpu - ref| <= 2e-2 + 2e-2 |ref|   (same dequantised codes, fp32 accumulation, bf16 output)
 Cache writes, block copies and indexing are compared bit for bit.
 """
 from __future__ import annotations
@@ -13,7 +14,7 @@ import torch
 
 import oracle
 
-TOL = {"f32": (1e-5, 0.0), "bf16": (2e-2, 2e-2), "e4m3": (6e-2, 0.0)}
+TOL = {"f32": (1e-5, 0.0), "bf16": (2e-2, 2e-2), "e4m3": (6e-2, 0.0), "i8": (2e-2, 2e-2)}
 
 
 def oracle_step(w, seqs=None, threads=0):
@@ -22,7 +23,7 @@ def oracle_step(w, seqs=None, threads=0):
     kc, vc = w.k_cache.copy(), w.v_cache.copy()
     if len(w.copy_pairs):
         oracle.copy_blocks(kc, vc, w.copy_pairs)
-    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3}[w.kv_dtype]
+    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}[w.kv_dtype]
     oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc, cache_dtype=cache_dt,
                              k_scale=w.k_scale, v_scale=w.v_scale)
     out = oracle.paged_attention_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,

@@ -13,7 +13,7 @@ from parity import host_bits
 
 pytestmark = pytest.mark.gpu
 
-_CODE = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3}
+_CODE = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}
 
 
 def _cache_pair(rng, NB, S, Hkv, D, dt):
@@ -21,7 +21,7 @@ def _cache_pair(rng, NB, S, Hkv, D, dt):
 
 
 @pytest.mark.parametrize("src", ["f32", "bf16"])
-@pytest.mark.parametrize("dst", ["f32", "bf16", "e4m3"])
+@pytest.mark.parametrize("dst", ["f32", "bf16", "e4m3", "i8"])
 @pytest.mark.parametrize("S,Hkv,D", [(4, 2, 64), (16, 8, 128), (32, 1, 64)])
 def test_reshape_and_cache_bit_exact(src, dst, S, Hkv, D):
     rng = np.random.default_rng(100 + S + D)
@@ -34,7 +34,7 @@ def test_reshape_and_cache_bit_exact(src, dst, S, Hkv, D):
     slots = rng.choice(NB * S, size=T, replace=False).astype(np.int64)
     slots[3] = -1          # padding token
     slots[7] = -5
-    ks, vs = (0.37, 1.9) if dst == "e4m3" else (1.0, 1.0)
+    ks, vs = {"e4m3": (0.37, 1.9), "i8": (0.05, 0.013)}.get(dst, (1.0, 1.0))
     ref_k, ref_v = kc.copy(), vc.copy()
     oracle.reshape_and_cache(kn, vn, slots, ref_k, ref_v, cache_dtype=_CODE[dst], k_scale=ks, v_scale=vs)
     dk, dv = to_device(kc), to_device(vc)
@@ -63,7 +63,7 @@ def test_reshape_and_cache_flags_slot_beyond_pool():
     np.testing.assert_array_equal(host_bits(dk), ref_k)
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16", "e4m3"])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "e4m3", "i8"])
 def test_copy_blocks_bit_exact(dt):
     rng = np.random.default_rng(9)
     NB, S, Hkv, D = 64, 16, 8, 128

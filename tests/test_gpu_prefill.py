@@ -75,6 +75,14 @@ def test_prefill_chunk_fp8_cache(NQ, q_start, Hq, Hkv, S):
     assert_close("e4m3", got, ref, f"fp8 prefill NQ={NQ} q_start={q_start}")
 
 
+def test_prefill_chunk_int8_cache():
+    q, kc, vc, table, kv_len = _chunk_case(75, 300, 16, 2, 16, seed=9, kv="i8")
+    scale = 1 / np.sqrt(128)
+    ref = oracle.paged_prefill_chunk(q, 300, kc, vc, table, kv_len, scale, k_scale=1 / 32, v_scale=1 / 16)
+    got = _run(q, kc, vc, table, 300, kv_len, scale, 1 / 32, 1 / 16)
+    assert_close("i8", got, ref, "int8 prefill")
+
+
 def test_prefill_poisoned_slots_do_not_leak():
     q, kc, vc, table, kv_len = _chunk_case(45, 70, 8, 1, 16, seed=3, poison=True)
     scale = 1 / np.sqrt(128)

@@ -434,3 +434,27 @@ def test_block_hashes_chain_and_prefix_property():
     d1 = oracle.fnv1a64(a[4:8].astype("<i4").tobytes())
     h1 = oracle.fnv1a64(h0.to_bytes(8, "little") + d1.to_bytes(8, "little"))
     assert int(ha[0]) == h0 and int(ha[1]) == h1
+
+
+def test_int8_encoder_matches_numpy_rint_and_clamp():
+    grid = np.concatenate([np.arange(-130, 130, 0.25), np.arange(-3, 3, 0.5) + 1e-7,
+                           np.array([127.5, -127.5, 1e9, -1e9, 0.0, -0.0])]).astype(np.float32)
+    ours = oracle.f32_to_i8(grid)
+    ref = np.clip(np.rint(grid.astype(np.float64)), -127, 127).astype(np.int8)
+    np.testing.assert_array_equal(ours, ref)
+
+
+def test_int8_cache_reads_code_times_scale():
+    rng = np.random.default_rng(17)
+    q, kc, vc, bt, cl, *_ = _scatter_problem(rng, [6, 11], 4, 2, 16, 4)
+    k8 = random_values(rng, kc.shape, "i8")
+    v8 = random_values(rng, vc.shape, "i8")
+    out = oracle.paged_attention_decode(q, k8, v8, bt, cl, 0.25, k_scale=1 / 32, v_scale=1 / 16)
+    ref = oracle.paged_attention_decode(q, (k8.astype(np.float32) / 32), (v8.astype(np.float32) / 16), bt, cl, 0.25)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+    # the cache write quantises x / scale with ties to even
+    kn = (rng.standard_normal((3, 2, 16)) * 2).astype(np.float32)
+    kq = np.zeros((2, 4, 2, 16), np.int8)
+    oracle.reshape_and_cache(kn, kn, np.array([0, 3, 6], np.int64), kq, kq.copy(), k_scale=1 / 32, v_scale=1.0)
+    y = (kn / np.float32(1 / 32)).astype(np.float32)
+    np.testing.assert_array_equal(kq[0, 0], np.clip(np.rint(y[0]), -127, 127))
