@@ -62,15 +62,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 }  // namespace
 
 // NARROW: 0 = bf16 cache; 1 = FP8 E4M3 codes; 2 = INT8 codes (both widened to bf16 on chip).
+// 256 threads: warp w works on TMEM lanes 32 (w % 4) .. + 31 (rows of the tile) and on the
+// half w / 4 of the columns -- keys 64 (w / 4) .. + 63 of S, head dims of O likewise.
 template <int NARROW>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
     constexpr bool FP8 = NARROW != 0;  // a one-byte cache, staged and widened
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
     const int h = blockIdx.y;
     const int rows_q = kRows / a.G;                                   // query tokens per CTA
     const int i0 = (gridDim.x - 1 - blockIdx.x) * rows_q;             // heaviest (latest) tiles first
@@ -78,6 +81,7 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t bar = sb + kOffBar;                                // 8 bytes per mbarrier
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 64);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 72);
+    float* row_x = reinterpret_cast<float*>(smem + kOffBar + 128);   // [2][128] per-half row maxima / sums
 
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(bar + 8 * i, 1);
@@ -93,9 +97,10 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem, tO = tmem + 128;
-    const uint32_t trow = static_cast<uint32_t>(warp * 32) << 16;    // this warp's TMEM lanes
+    const uint32_t trow = static_cast<uint32_t>(quad * 32) << 16;    // this warp's TMEM lanes
+    const int col0 = half * 64;                                       // this thread's 64 columns
 
-    const int r = tid;                        // this thread's row of the tile
+    const int r = quad * 32 + lane;           // this thread's row of the tile
     const int qi = i0 + r / a.G;              // its query token
     const int qpos = a.q_start + qi;          // its position
     const int last_q = min(i0 + rows_q, a.NQ) - 1;
@@ -103,16 +108,23 @@ __global__ void __launch_bounds__(128, 1)
     const int n_tiles = max_key / kKeys + 1;
     const int blocks_per_tile = kKeys / a.S;
 
-    // thread 0: copy the K and V tiles of key tile j (bf16: into stage j & 1; FP8: into the code staging area)
+    // Thread 0: copy the K and V tiles of key tile j (bf16: into stage j & 1; FP8/INT8: into the code
+    // staging area).  The tile's block-table entries are read first, all at once, so their latencies overlap.
     auto load_kv = [&](int j) {
         const int st = FP8 ? 0 : (j & 1);
         const uint32_t b = bar + 8 * (kBarKV0 + st);
+        int c2s[kKeys / 8];
+#pragma unroll
+        for (int bi = 0; bi < kKeys / 8; ++bi) {
+            const int idx = j * blocks_per_tile + bi;
+            c2s[bi] = (bi < blocks_per_tile && idx < a.n_table) ? a.block_table[idx] : -1;
+        }
         mbar_arrive_expect_tx(b, FP8 ? 2 * kHalf : 4 * kHalf);
         for (int bi = 0; bi < blocks_per_tile; ++bi) {
             const int idx = j * blocks_per_tile + bi;
+            const int phys = c2s[bi];
             int c2 = a.NB * a.S;  // beyond the pool: the copy fills zeros
             if (idx < a.n_table) {
-                const int phys = a.block_table[idx];
                 if (phys >= 0 && phys < a.NB) c2 = phys * a.S;
                 else raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
             }
@@ -133,42 +145,39 @@ __global__ void __launch_bounds__(128, 1)
 
     // FP8 / INT8: widen the staged codes of one key tile into the bf16 stage st (exact; the
     // per-tensor scales are applied to the scores and to the output instead).
-    // Thread t converts key row t of K and of V; V rows of keys past the end become 0.
+    // Thread t converts key row t % 128 of K (t < 128) or of V; V rows of keys past the end become 0.
     auto widen_fp8 = [&](int st, int nvalid) {
-        const int t = tid;
+        const int t = tid & 127, kv = tid >> 7;
+        const uint8_t* src = smem + kOffStage + kv * kHalf + t * 128;
+        uint8_t* dst0 = smem + (kv ? kOffV : kOffK) + st * 2 * kHalf + t * 128;
+        const bool zero = kv == 1 && t >= nvalid;
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-            const uint8_t* src = smem + kOffStage + kv * kHalf + t * 128;
-            uint8_t* dst0 = smem + (kv ? kOffV : kOffK) + st * 2 * kHalf + t * 128;
-            const bool zero = kv == 1 && t >= nvalid;
+        for (int c = 0; c < 8; ++c) {  // logical 16-code chunk: head dims 16c .. 16c + 15
+            uint32_t o[8];
+            if (zero) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {  // logical 16-code chunk: head dims 16c .. 16c + 15
-                uint32_t o[8];
-                if (zero) {
+                for (int i = 0; i < 8; ++i) o[i] = 0u;
+            } else {
+                const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ (t & 7)) * 16));
+                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = 0u;
-                } else {
-                    const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ (t & 7)) * 16));
-                    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float2 f0, f1;
-                        if constexpr (NARROW == 2) {
-                            f0 = s8x2_to_float2(ws[i], 0);
-                            f1 = s8x2_to_float2(ws[i], 2);
-                        } else {
-                            f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
-                            f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
-                        }
-                        o[2 * i] = pack_bf16x2_rn(f0.x, f0.y);
-                        o[2 * i + 1] = pack_bf16x2_rn(f1.x, f1.y);
+                for (int i = 0; i < 4; ++i) {
+                    float2 f0, f1;
+                    if constexpr (NARROW == 2) {
+                        f0 = s8x2_to_float2(ws[i], 0);
+                        f1 = s8x2_to_float2(ws[i], 2);
+                    } else {
+                        f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                        f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
                     }
+                    o[2 * i] = pack_bf16x2_rn(f0.x, f0.y);
+                    o[2 * i + 1] = pack_bf16x2_rn(f1.x, f1.y);
                 }
-                uint8_t* dst = dst0 + (c >> 2) * kHalf;
-                const int lc = 2 * (c & 3);
-                *reinterpret_cast<uint4*>(dst + ((lc ^ (t & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-                *reinterpret_cast<uint4*>(dst + (((lc + 1) ^ (t & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
             }
+            uint8_t* dst = dst0 + (c >> 2) * kHalf;
+            const int lc = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(dst + ((lc ^ (t & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + (((lc + 1) ^ (t & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
     };
 
@@ -184,8 +193,8 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (!mbar_wait_bounded(bar + 8 * kBarQ, 0, a.timeout_ns)) *abort_flag = 1;
 
-    float m_ref = -INFINITY;  // running max of this row (log2 units)
-    float l_run = 0.f;        // running sum of this row's (bf16-rounded) probabilities
+    float m_ref = -INFINITY;  // running max of this row (log2 units), same in both halves
+    float l_run = 0.f;        // running sum of this thread's half of the row's probabilities
     int issued_s = 0;         // S = Q K^T groups committed so far
     int issued_o = 0;         // P.V groups committed so far
     int kv_waited = 0;        // key tiles whose copies were waited for
@@ -202,8 +211,10 @@ __global__ void __launch_bounds__(128, 1)
             widen_fp8(st, nvalid);
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0 && j + 1 < n_tiles && !*abort_flag) load_kv(j + 1);  // the staging area is free again
-            if (j + 1 < n_tiles) kv_loaded = j + 2;
+            if (j + 1 < n_tiles) {
+                if (tid == 0 && !*abort_flag) load_kv(j + 1);  // the staging area is free again
+                kv_loaded = j + 2;
+            }
         } else {
             if (!mbar_wait_bounded(bar + 8 * (kBarKV0 + st), (j >> 1) & 1, a.timeout_ns)) *abort_flag = 1;
             kv_waited = j + 1;
@@ -236,24 +247,24 @@ __global__ void __launch_bounds__(128, 1)
         if (!mbar_wait_bounded(bar + 8 * kBarS, j & 1, a.timeout_ns)) *abort_flag = 1;
         tc_fence_after();
 
-        // ---- pass 1: this row's maximum over the tile.  Keys <= q_start + i0 are visible to every
-        // row of the CTA, so only tiles past that point (or past kv_len) need per-key masks.
+        // ---- this thread's 64 scores; keys <= q_start + i0 are visible to every row of the CTA,
+        // so only tiles past that point (or past kv_len) need per-key masks
+        float v[64];
+        tmem_ld64(tS + trow + col0, v);
         const bool masked = (tile0 + kKeys - 1 > a.q_start + i0) || (tile0 + kKeys > a.kv_len);
-        const int lim = min(a.kv_len, qpos + 1) - tile0;  // this row sees keys [tile0, tile0 + lim)
+        const int lim = min(a.kv_len, qpos + 1) - tile0 - col0;  // visible keys of this row in these columns
         float mraw = -INFINITY;
+        if (!masked) {
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 32) {
-            float v[32];
-            tmem_ld32(tS + trow + c, v);
-            if (!masked) {
+            for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, v[i]);
+        } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, v[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, (c + i < lim) ? v[i] : -INFINITY);
-            }
+            for (int i = 0; i < 64; ++i) mraw = fmaxf(mraw, (i < lim) ? v[i] : -INFINITY);
         }
-        const float mt = mraw * a.sm_log2;  // the scale is positive, so it keeps the order
+        row_x[half * 128 + r] = mraw;
+        __syncthreads();
+        // the scale is positive, so it keeps the order of the maxima
+        const float mt = fmaxf(mraw, row_x[(1 - half) * 128 + r]) * a.sm_log2;
 
         // ---- the previous P.V has finished: O may be rescaled and P overwritten
         if (j > 0) {
@@ -268,48 +279,37 @@ __global__ void __launch_bounds__(128, 1)
         if (j > 0 && __any_sync(kFull, need)) {
             const float m_new = need ? mt : m_ref;
             const float alpha = ex2_approx(m_ref - m_new);
+            float o[64];
+            tmem_ld64(tO + trow + col0, o);
 #pragma unroll
-            for (int c = 0; c < 128; c += 32) {
-                float o[32];
-                tmem_ld32(tO + trow + c, o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                tmem_st32(tO + trow + c, o);
-            }
+            for (int i = 0; i < 64; ++i) o[i] *= alpha;
+            tmem_st64(tO + trow + col0, o);
             l_run *= alpha;
             m_ref = m_new;
         } else if (need) {
             m_ref = mt;
         }
 
-        // ---- pass 2: probabilities as bf16 into the swizzled K-major P tile, and the row sum
+        // ---- probabilities as bf16 into this thread's swizzled 128-byte row of P half `half`
         float ls = 0.f;
         const float neg_m = -m_ref;
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 32) {
-            float v[32];
-            tmem_ld32(tS + trow + c, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float p0 = ex2_approx(fmaf(v[i], a.sm_log2, neg_m));
-                float p1 = ex2_approx(fmaf(v[i + 1], a.sm_log2, neg_m));
-                if (masked) {
-                    p0 = (c + i < lim) ? p0 : 0.f;
-                    p1 = (c + i + 1 < lim) ? p1 : 0.f;
-                }
-                ls += p0 + p1;
-                pk[i / 2] = pack_bf16x2_rn(p0, p1);
+        for (int i = 0; i < 64; i += 2) {
+            float p0 = ex2_approx(fmaf(v[i], a.sm_log2, neg_m));
+            float p1 = ex2_approx(fmaf(v[i + 1], a.sm_log2, neg_m));
+            if (masked) {
+                p0 = (i < lim) ? p0 : 0.f;
+                p1 = (i + 1 < lim) ? p1 : 0.f;
             }
-            const int hf = c >> 6;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int chunk = ((c & 63) >> 3) + q4;
-                const int phys = chunk ^ (r & 7);
-                *reinterpret_cast<uint4*>(smem + kOffP + hf * kHalf + r * 128 + phys * 16) =
-                    make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-            }
+            ls += p0 + p1;
+            pk[i / 2] = pack_bf16x2_rn(p0, p1);
         }
+        uint8_t* prow = smem + kOffP + half * kHalf + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         l_run += ls;
         fence_proxy_async_smem();
         tc_fence_before();
@@ -341,30 +341,31 @@ __global__ void __launch_bounds__(128, 1)
         // leave nothing in flight: the last S = Q K^T and every issued key-tile copy (all bounded)
         if (issued_s > 0) mbar_wait_bounded(bar + 8 * kBarS, (issued_s - 1) & 1, a.timeout_ns);
         for (int t = kv_waited; t < kv_loaded; ++t)
-            mbar_wait_bounded(bar + 8 * (kBarKV0 + (t & 1)), (t >> 1) & 1, a.timeout_ns);
+            mbar_wait_bounded(bar + 8 * (kBarKV0 + (FP8 ? 0 : (t & 1))), FP8 ? (t & 1) : ((t >> 1) & 1), a.timeout_ns);
     }
+    // ---- the row sum from both halves
+    row_x[half * 128 + r] = l_run;
+    __syncthreads();
+    const float l_row = l_run + row_x[(1 - half) * 128 + r];
     if (aborted || *abort_flag) {
         if (tid == 0) raise_error(a.err, PKV_DEVERR_TIMEOUT);
     } else {
-        // ---- out = O / l for this row
-        const float inv = l_run > 0.f ? a.out_mul / l_run : 0.f;
+        // ---- out = O / l for this row's 64 head dims
+        const float inv = l_row > 0.f ? a.out_mul / l_row : 0.f;
         const int g = r % a.G;
         uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
-                        ((static_cast<size_t>(qi) * a.Hq + static_cast<size_t>(h) * a.G + g) * 128) * 2;
+                        ((static_cast<size_t>(qi) * a.Hq + static_cast<size_t>(h) * a.G + g) * 128 + col0) * 2;
+        float o[64];
+        tmem_ld64(tO + trow + col0, o);  // warp-collective: every lane loads, valid rows store
+        if (qi < a.NQ) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 32) {
-            float o[32];
-            tmem_ld32(tO + trow + c, o);  // warp-collective: every lane loads, valid rows store
-            if (qi < a.NQ) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4 w;
-                    w.x = pack_bf16x2_rn(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
-                    w.y = pack_bf16x2_rn(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
-                    w.z = pack_bf16x2_rn(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
-                    w.w = pack_bf16x2_rn(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
-                    *reinterpret_cast<uint4*>(orow + (c + 8 * q4) * 2) = w;
-                }
+            for (int q4 = 0; q4 < 8; ++q4) {
+                uint4 w;
+                w.x = pack_bf16x2_rn(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                w.y = pack_bf16x2_rn(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                w.z = pack_bf16x2_rn(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                w.w = pack_bf16x2_rn(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
+                *reinterpret_cast<uint4*>(orow + q4 * 16) = w;
             }
         }
     }
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 size_t prefill_smem_bytes(bool fp8) {
-    return static_cast<size_t>(fp8 ? off_bar<true>() : off_bar<false>()) + 128 + 1024;
+    return static_cast<size_t>(fp8 ? off_bar<true>() : off_bar<false>()) + 128 + 1024 + 1024;
 }
 
 cudaError_t launch_paged_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -385,7 +386,7 @@ cudaError_t launch_paged_prefill(const CUtensorMap& qmap, const CUtensorMap& kma
     if (e != cudaSuccess) return e;
     const int rows_q = kRows / a.G;
     dim3 grid((a.NQ + rows_q - 1) / rows_q, a.Hkv);
-    kern<<<grid, 128, smem, stream>>>(qmap, kmap, vmap, a);
+    kern<<<grid, 256, smem, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
 }
 
