@@ -174,6 +174,36 @@ pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, in
                                    int32_t num_q_heads, float scale, int32_t* device_error, void* stream);
 
 /*
+ * Several prefill chunks of different sequences in one launch (varlen form of
+ * the chunked prefill in "3.3 批处理与内存管理", section "分块预填充", and of the
+ * mixed batches of "从 PagedAttention 到 Chunked Prefill" §3.2, where prefill
+ * chunks and decode tokens of different sequences share one step).  Chunk s owns query tokens [cu_q[s], cu_q[s+1]) of q/out; its token
+ * i sits at position q_starts[s] + i of sequence s, whose first kv_lens[s]
+ * keys are cached (the chunk's own keys included, so
+ * kv_lens[s] >= q_starts[s] + cu_q[s+1] - cu_q[s]).  Each chunk computes
+ * exactly what pkv_paged_prefill_chunk computes for it, with block table row
+ * s of block_tables ([num_seqs][max_blocks_per_seq]).  A decode token is a
+ * chunk of one query token.
+ *   q, out: [total_q_tokens][num_q_heads][128] bf16; rows not covered by any
+ *        chunk are not written.
+ *   cu_q: [num_seqs + 1] device int32, non-decreasing, cu_q[num_seqs] <= total_q_tokens.
+ *   q_starts, kv_lens: [num_seqs] device int32.
+ * These arrays are read on the device: a violation (cu_q not monotone or past
+ * total_q_tokens, kv_len too short, more table entries than max_blocks_per_seq)
+ * sets PKV_DEVERR_BAD_LENGTH and leaves that chunk's rows unwritten; a table
+ * entry outside the pool sets PKV_DEVERR_BAD_BLOCK.
+ * scale must be positive.
+ * Supported: bf16 queries, bf16 cache, head_dim 128, block_size 8/16/32, G dividing 128,
+ *   num_seqs <= 2048.  No workspace.
+ */
+pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
+                                    const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,
+                                    const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    int32_t num_seqs, int32_t num_q_heads, float scale,
+                                    int32_t* device_error, void* stream);
+
+/*
  * Copy whole physical blocks, for copy-on-write of shared blocks
  * ("3.3 批处理与内存管理", section "共享与写时复制": before a sequence writes
  * into a block whose reference count is above one, the engine copies the

@@ -67,11 +67,12 @@ def lib() -> ctypes.CDLL:
     L.pkv_paged_attention_decode_static_scratch.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32,
                                                             P, P]
     L.pkv_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, D, P, i32, i32, f32, P, P]
+    L.pkv_paged_prefill_varlen.argtypes = [P, P, i32, i32, P, P, P, P, P, D, P, i32, i32, i32, f32, P, P]
     L.pkv_swap_blocks.argtypes = [P, P, i32, P, P, i32, D, P, i32, P, P]
     L.pkv_block_hashes.argtypes = [P, P, i32, i32, P, P, ctypes.c_int64, P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
                  "pkv_copy_blocks", "pkv_paged_attention_decode_static_scratch", "pkv_paged_prefill_chunk",
-                 "pkv_swap_blocks", "pkv_block_hashes"):
+                 "pkv_paged_prefill_varlen", "pkv_swap_blocks", "pkv_block_hashes"):
         getattr(L, name).restype = ctypes.c_int
     L.pkv_status_string.argtypes = [ctypes.c_int]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -163,6 +164,17 @@ def pkv_paged_prefill_chunk(out, q, q_start: int, k_cache, v_cache, cache: Cache
                                          int(kv_len), int(q.shape[1]), float(scale), _ptr(device_error),
                                          _stream(stream)),
            "pkv_paged_prefill_chunk")
+
+
+def pkv_paged_prefill_varlen(out, q, cu_q, q_starts, kv_lens, k_cache, v_cache, cache: CacheDesc, block_tables,
+                             scale: float, device_error=None, stream=None) -> None:
+    """Several prefill chunks in one launch; q/out are [total_q_tokens][Hq][128], the index arrays on the device."""
+    _check(lib().pkv_paged_prefill_varlen(_ptr(out), _ptr(q), _dtype(q), int(q.shape[0]), _ptr(cu_q),
+                                          _ptr(q_starts), _ptr(kv_lens), _ptr(k_cache), _ptr(v_cache),
+                                          ctypes.byref(cache), _ptr(block_tables), int(block_tables.shape[1]),
+                                          int(kv_lens.shape[0]), int(q.shape[1]), float(scale),
+                                          _ptr(device_error), _stream(stream)),
+           "pkv_paged_prefill_varlen")
 
 
 STATIC_SCRATCH_BYTES = 12 * 1024 * 1024  # PKV_STATIC_SCRATCH_BYTES in include/pkv.h

@@ -565,8 +565,89 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
     a.out_mul = fp8 ? cache->v_scale : 1.f;
     a.timeout_ns = 2000000000ull;
-    cudaError_t e = launch_paged_prefill(qm, km, vm, a, fp8 ? (cache->dtype == PKV_INT8 ? 2 : 1) : 0,
-                                         static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (fp8) {
+        e = launch_paged_prefill(qm, km, vm, a, cache->dtype == PKV_INT8 ? 2 : 1, static_cast<cudaStream_t>(stream));
+    } else {
+        if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes())
+            return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
+        const int rows_q = 128 / G;
+        e = launch_paged_prefill_ws(qm, km, vm, a, (num_q_tokens + rows_q - 1) / rows_q,
+                                    static_cast<cudaStream_t>(stream));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
+    return PKV_OK;
+}
+
+PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
+                                            const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,
+                                            const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                            int32_t num_seqs, int32_t num_q_heads, float scale,
+                                            int32_t* device_error, void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    const int Hkv = cache->num_kv_heads, D = cache->head_dim, S = cache->block_size;
+    if (total_q_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (total_q_tokens=%d num_seqs=%d num_q_heads=%d MB=%d)",
+                    total_q_tokens, num_seqs, num_q_heads, max_blocks_per_seq);
+    if (num_q_heads % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
+    const int G = num_q_heads / Hkv;
+    if (q_dtype != PKV_BF16 || cache->dtype != PKV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "varlen prefill supports bf16 queries with a bf16 cache");
+    if (D != 128) return fail(PKV_ERR_UNSUPPORTED, "prefill supports head_dim 128");
+    if (S < 8) return fail(PKV_ERR_UNSUPPORTED, "prefill supports block_size 8, 16, 32");
+    if (G > 128 || 128 % G != 0) return fail(PKV_ERR_UNSUPPORTED, "GQA group %d must divide 128", G);
+    if (num_seqs > prefill_ws_max_seqs())
+        return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > %d chunks per call", num_seqs, prefill_ws_max_seqs());
+    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq > INT32_MAX)
+        return fail(PKV_ERR_OUT_OF_RANGE, "block table larger than 2^31-1 entries");
+    if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
+    if (!out || !q || !cu_q || !q_starts || !kv_lens || !k_cache || !v_cache || !block_tables)
+        return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(q_starts) |
+         reinterpret_cast<uintptr_t>(kv_lens) | reinterpret_cast<uintptr_t>(block_tables)) & 3u)
+        return fail(PKV_ERR_INVALID_ARG, "index arrays must be 4-byte aligned");
+    if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes())
+        return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
+    CUtensorMap qm, km, vm;
+    if ((st = tensor_map_sw128(&qm, q, false, 128, num_q_heads, total_q_tokens, G, 128 / G)) != PKV_OK) return st;
+    const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
+    if ((st = tensor_map_sw128(&km, k_cache, false, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, false, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    PrefillArgs a;
+    a.out = out;
+    a.block_table = block_tables;
+    a.err = device_error;
+    a.NQ = total_q_tokens;
+    a.q_start = 0;
+    a.kv_len = 0;
+    a.Hq = num_q_heads;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.S = S;
+    a.NB = cache->num_blocks;
+    a.n_table = max_blocks_per_seq;
+    a.sm_log2 = scale * 1.4426950408889634f;
+    a.out_mul = 1.f;
+    a.timeout_ns = 2000000000ull;
+    a.nseq = num_seqs;
+    a.MB = max_blocks_per_seq;
+    a.cu_q = cu_q;
+    a.q_starts = q_starts;
+    a.kv_lens = kv_lens;
+    // an upper bound of the row tiles: every chunk adds at most one partial tile
+    const int rows_q = 128 / G;
+    const int grid_x = total_q_tokens / rows_q + num_seqs;
+    cudaError_t e;
+    e = launch_paged_prefill_ws(qm, km, vm, a, grid_x, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_varlen launch");
     return PKV_OK;
 }

@@ -131,3 +131,111 @@ def test_llama70b_chunk_sampled_rows(name):
     got = to_host(out)
     assert np.isfinite(got).all()
     assert_close(w.kv_dtype, got[rows], ref, name)
+
+
+# ---------------------------------------------------------------- varlen: several chunks in one launch
+
+def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3):
+    """chunks: (q_start, n_q) per sequence; sequence s holds q_start + n_q cached tokens in one shared,
+    shuffled pool.  Returns host arrays and the per-chunk metadata."""
+    rng = np.random.default_rng(seed)
+    D = 128
+    kv_lens = np.array([qs + nq for qs, nq in chunks], np.int32)
+    need = sum(-(-int(L) // S) for L in kv_lens)
+    NB = need + 7
+    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    for s, L in enumerate(kv_lens):
+        alloc.add_seq(s, int(L))
+    tables = alloc.padded_tables(list(range(len(chunks))))
+    kc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
+    vc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
+    cu = np.zeros(len(chunks) + 1, np.int32)
+    cu[1:] = np.cumsum([nq for _, nq in chunks])
+    q = wl.random_values(rng, (int(cu[-1]) + tail_rows, Hq, D), "bf16")
+    q_starts = np.array([qs for qs, _ in chunks], np.int32)
+    return q, kc, vc, tables, cu, q_starts, kv_lens
+
+
+def _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale):
+    dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
+    out = torch.full_like(dq, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.pkv_paged_prefill_varlen(out, dq, to_device(cu), to_device(q_starts), to_device(kv_lens), dk, dv,
+                                 B.CacheDesc.for_cache(dk), to_device(tables), scale, err)
+    torch.cuda.synchronize()
+    return out, int(err.item())
+
+
+# prefill chunks from position 0 and from the middle of a sequence, decode tokens (a chunk of one query),
+# an empty chunk, ragged tiles, chunks that end exactly on a 128-key tile
+MIXED = [(0, 200), (300, 1), (129, 0), (1000, 57), (5, 33), (2047, 1), (128, 128), (77, 1), (0, 1)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,S", [(16, 4, 16), (16, 2, 8), (4, 4, 32), (64, 8, 16)])
+def test_prefill_varlen_mixed_batch_matches_oracle(Hq, Hkv, S):
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case(MIXED, Hq, Hkv, S, seed=Hq * 10 + S)
+    scale = 1 / np.sqrt(128)
+    out, err = _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale)
+    assert err == 0, hex(err)
+    got = to_host(out)
+    for s, (qs, nq) in enumerate(MIXED):
+        if nq == 0:
+            continue
+        n_tab = -(-int(kv_lens[s]) // S)
+        ref = oracle.paged_prefill_chunk(q[cu[s]:cu[s + 1]], qs, kc, vc, tables[s, :n_tab], int(kv_lens[s]), scale)
+        assert_close("bf16", got[cu[s]:cu[s + 1]], ref, f"varlen chunk {s} (q_start={qs}, n_q={nq}) G={Hq // Hkv}")
+    assert np.isnan(got[cu[-1]:]).all(), "rows outside every chunk were written"
+
+
+def test_prefill_varlen_one_chunk_equals_chunk_call():
+    """The same chunk through both entry points: identical bits (same tile arithmetic)."""
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case([(90, 75)], 16, 2, 16, seed=11, tail_rows=0)
+    scale = 0.07
+    out_v, err = _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale)
+    assert err == 0
+    dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
+    out_c = torch.full_like(dq, float("nan"))
+    pkv.pkv_paged_prefill_chunk(out_c, dq, 90, dk, dv, B.CacheDesc.for_cache(dk), to_device(tables[0]),
+                                int(kv_lens[0]), scale)
+    torch.cuda.synchronize()
+    assert torch.equal(out_v.view(torch.int16), out_c.view(torch.int16))
+
+
+def test_prefill_varlen_device_checks():
+    """Chunk metadata is read on the device: a bad chunk raises BAD_LENGTH and is skipped, the rest run."""
+    chunks = [(10, 20), (50, 30), (0, 40)]
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case(chunks, 8, 1, 16, seed=5, tail_rows=0)
+    scale = 1 / np.sqrt(128)
+    short = kv_lens.copy()
+    short[1] = 60  # < q_start + n_q = 80: the chunk's own keys are not all cached
+    out, err = _run_varlen(q, kc, vc, tables, cu, q_starts, short, scale)
+    assert err & 0x4
+    got = to_host(out)
+    assert np.isnan(got[cu[1]:cu[2]]).all()
+    for s in (0, 2):
+        ref = oracle.paged_prefill_chunk(q[cu[s]:cu[s + 1]], chunks[s][0], kc, vc, tables[s, :-(-int(kv_lens[s]) // 16)],
+                                         int(kv_lens[s]), scale)
+        assert_close("bf16", got[cu[s]:cu[s + 1]], ref, f"chunk {s} beside a bad chunk")
+    bad_cu = cu.copy()
+    bad_cu[3] = cu[3] + 5  # past total_q_tokens
+    out, err = _run_varlen(q, kc, vc, tables, bad_cu, q_starts, kv_lens, scale)
+    assert err & 0x4
+    assert np.isnan(to_host(out)[cu[2]:]).all()
+
+
+def test_prefill_varlen_host_checks():
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case([(0, 4)], 8, 1, 16, seed=2, tail_rows=0)
+    dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
+    out = torch.empty_like(dq)
+    d = B.CacheDesc.for_cache(dk)
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    pkv.pkv_paged_prefill_varlen(out, dq, to_device(cu[:1]), empty, empty, dk, dv, d, to_device(tables), 0.1)
+    many = torch.zeros(2049, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_prefill_varlen(out, dq, many, many, many, dk, dv, d, to_device(np.zeros((2049, 1), np.int32)),
+                                     0.1)
+    assert ei.value.status == 2
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_prefill_varlen(out, dq, to_device(cu), to_device(q_starts), to_device(kv_lens), dk, dv, d,
+                                     to_device(tables), -1.0)
+    assert ei.value.status == 1
