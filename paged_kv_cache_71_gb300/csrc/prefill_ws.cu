@@ -10,15 +10,17 @@
 // A CTA owns 128 query rows (128 / G tokens x the G query heads of one KV
 // head) of one chunk and walks the chunk's keys in tiles of 128:
 //   * warp 8 (producer) copies K and V tiles with TMA (128-byte swizzle,
-//     one block of the block table per copy) into a double-buffered ring;
+//     one block of the block table per copy) into separate rings (K three
+//     deep, V two deep), reading the block table one tile ahead;
 //   * warp 9 (one thread) issues the tcgen05 MMAs: S(j+1) = Q K(j+1)^T into
 //     the other of two TMEM S buffers as soon as its keys land, then
-//     O += P(j) V(j) once the softmax of tile j is done -- so the tensor
-//     pipe computes the next scores while the softmax warps work;
+//     O += P(j) V(j) with P read from TMEM once the softmax of tile j is done
+//     -- so the tensor pipe computes the next scores while the softmax works;
 //   * warps 0-7 (softmax) each own 64 columns of 32 rows: row maximum over
-//     the two halves of a row (pair barrier), exp2, bf16 P into the swizzled
-//     K-major tile the P.V MMA reads, running sums; O in TMEM is rescaled
-//     only when a row's maximum grows by more than 8 (log2 units).
+//     the two halves of a row (pair barrier), exp2, bf16 P written to one of
+//     two TMEM P buffers, running sums.  O in TMEM is rescaled only when a
+//     row's maximum grows by more than 8 (log2 units); only then does the
+//     softmax wait for the previous P.V.
 // Hand-offs are mbarriers (no CTA-wide barrier inside the loop).  Every wait
 // is bounded; on timeout a role records the error and leaves its loop, the
 // CTA drains its own MMAs and copies (bounded) and frees TMEM.
@@ -29,29 +31,33 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128, kKeys = 128, kHalf = 16384;
-constexpr int kOffQ = 0;                      // 2 halves of 64 head dims
-constexpr int kOffK = kOffQ + 2 * kHalf;      // 2 stages x 2 halves
-constexpr int kOffV = kOffK + 4 * kHalf;      // 2 stages x 2 halves
-constexpr int kOffP = kOffV + 4 * kHalf;      // 2 halves
-constexpr int kOffMeta = kOffP + 2 * kHalf;   // barriers, TMEM address, flags, row exchange, tile counts
-constexpr int kTmemCols = 512;                // S0: 0..127, S1: 128..255, O: 256..383
-constexpr int kSoftmax = 256;                 // softmax threads (warps 0-7)
-constexpr int kThreads = 320;                 // + producer warp 8 + MMA warp 9
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kOffQ = 0;                                  // 2 halves of 64 head dims
+constexpr int kOffK = kOffQ + 2 * kHalf;                  // kKStages x 2 halves
+constexpr int kOffV = kOffK + kKStages * 2 * kHalf;       // kVStages x 2 halves
+constexpr int kOffMeta = kOffV + kVStages * 2 * kHalf;    // barriers, TMEM address, flags, row exchange, tile counts
+constexpr int kTmemCols = 512;  // S0: 0..127, S1: 128..255, O: 256..383, P0: 384..447, P1: 448..511
+constexpr int kColO = 256, kColP = 384;
+constexpr int kSoftmax = 256;   // softmax threads (warps 0-7)
+constexpr int kThreads = 320;   // + producer warp 8 + MMA warp 9
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
 
 // mbarrier slots (8 bytes each)
-constexpr int kBarKvFull = 0;   // + stage: K/V copies landed (producer, expect_tx)
-constexpr int kBarKvEmpty = 2;  // + stage: S and P.V of the tile in that stage done (MMA commit)
-constexpr int kBarSFull = 4;    // + buffer: S written (MMA commit)
-constexpr int kBarSEmpty = 6;   // + buffer: S read by all softmax threads (256 arrivals)
-constexpr int kBarPFull = 8;    // P written, O rescaled (256 arrivals)
-constexpr int kBarODone = 9;    // O += P V done (MMA commit)
-constexpr int kBarQFull = 10;   // Q landed
-constexpr int kBarPair = 11;    // + 2 * quad + parity: the two warps of a row quadrant exchanged (64 arrivals)
-constexpr int kBarDrain = 19;   // final commit of the MMA thread
-constexpr int kNumBars = 20;
+constexpr int kBarKFull = 0;    // + stage (3): K copies landed (producer, expect_tx)
+constexpr int kBarKEmpty = 3;   // + stage (3): S of the tile in that stage done (MMA commit)
+constexpr int kBarVFull = 6;    // + stage (2): V copies landed
+constexpr int kBarVEmpty = 8;   // + stage (2): P.V of the tile in that stage done (MMA commit)
+constexpr int kBarSFull = 10;   // + buffer: S written (MMA commit)
+constexpr int kBarSEmpty = 12;  // + buffer: S read by all softmax threads (256 arrivals)
+constexpr int kBarPFull = 14;   // + buffer: P written (and O rescaled) by all softmax threads (256 arrivals)
+constexpr int kBarODone = 16;   // + buffer: O += P V of the tile using that P buffer done (MMA commit)
+constexpr int kBarQFull = 18;   // Q landed
+constexpr int kBarPair = 19;    // + 2 * quad + parity: the two warps of a row quadrant exchanged (64 arrivals)
+constexpr int kBarDrain = 27;   // final commit of the MMA thread
+constexpr int kNumBars = 28;
 constexpr int kMaxSeqs = 2048;  // chunks per launch (tile counts are kept in shared memory)
+static_assert(8 * kNumBars <= 232, "barrier slots overlap the TMEM address slot");
 
 __device__ __forceinline__ void tma_load_3d_nohint(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                                    uint32_t bar) {
@@ -82,9 +88,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rows_q = kRows / a.G;
 
     const uint32_t bar = sb + kOffMeta;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMeta + 192);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMeta + 196);
-    int* tile_info = reinterpret_cast<int*>(smem + kOffMeta + 200);   // s, i0 of this CTA (or -1)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMeta + 232);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMeta + 236);
+    int* tile_info = reinterpret_cast<int*>(smem + kOffMeta + 240);   // s, i0 of this CTA (or -1)
     float* row_x = reinterpret_cast<float*>(smem + kOffMeta + 256);    // [2 parity][2 half][128]
     int* tcount = reinterpret_cast<int*>(smem + kOffMeta + 256 + 2048);  // prefix of tiles per chunk
 
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const bool many = (i == kBarSEmpty || i == kBarSEmpty + 1 || i == kBarPFull);
+            const bool many = (i >= kBarSEmpty && i < kBarSEmpty + 2) || (i >= kBarPFull && i < kBarPFull + 2);
             const bool pair = i >= kBarPair && i < kBarPair + 8;
             mbar_init(bar + 8 * i, many ? kSoftmax : (pair ? 64 : 1));
         }
@@ -185,10 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;
+    const uint32_t tO = tmem + kColO;
 
     if (warp == 8) {
-        // ------------------------------------------------ producer: Q, then K/V tiles two ahead
+        // ------------------------------------------------ producer: Q, then K and V tiles ahead of use
         if (lane == 0) {
             prefetch_tensormap(&qmap);
             prefetch_tensormap(&kmap);
@@ -196,86 +202,110 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(bar + 8 * kBarQFull, 2 * kHalf);
             tma_load_3d_nohint(sb + kOffQ, &qmap, 0, h * a.G, q_base + i0, bar + 8 * kBarQFull);
             tma_load_3d_nohint(sb + kOffQ + kHalf, &qmap, 64, h * a.G, q_base + i0, bar + 8 * kBarQFull);
-            int issued = 0;
+            // rows of the pool for the blocks of one tile (beyond the pool: the copy fills zeros)
+            auto tile_rows = [&](int j, int (&c2)[kKeys / 8]) {
+#pragma unroll
+                for (int bi = 0; bi < kKeys / 8; ++bi) {
+                    const int idx = j * blocks_per_tile + bi;
+                    c2[bi] = (bi < blocks_per_tile && idx < n_table) ? table[idx] : -1;
+                }
+#pragma unroll
+                for (int bi = 0; bi < kKeys / 8; ++bi) {
+                    const int idx = j * blocks_per_tile + bi;
+                    int r = a.NB * a.S;
+                    if (bi < blocks_per_tile && idx < n_table) {
+                        if (c2[bi] >= 0 && c2[bi] < a.NB) r = c2[bi] * a.S;
+                        else raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
+                    }
+                    c2[bi] = r;
+                }
+            };
+            int rows[kKeys / 8];
+            tile_rows(0, rows);
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !mbar_wait_bounded(bar + 8 * (kBarKvEmpty + st), ((j - 2) >> 1) & 1, a.timeout_ns)) {
+                const int ks = j % kKStages, vs = j % kVStages;
+                if (j >= kKStages &&
+                    !mbar_wait_bounded(bar + 8 * (kBarKEmpty + ks), (j / kKStages - 1) & 1, a.timeout_ns)) {
                     *abort_flag = 1;
                     break;
                 }
                 if (*abort_flag) break;
-                int phys[kKeys / 8];
-#pragma unroll
-                for (int bi = 0; bi < kKeys / 8; ++bi) {
-                    const int idx = j * blocks_per_tile + bi;
-                    phys[bi] = (bi < blocks_per_tile && idx < n_table) ? table[idx] : -1;
-                }
-                const uint32_t b = bar + 8 * (kBarKvFull + st);
-                mbar_arrive_expect_tx(b, 4 * kHalf);
+                const uint32_t kb = bar + 8 * (kBarKFull + ks);
+                mbar_arrive_expect_tx(kb, 2 * kHalf);
                 for (int bi = 0; bi < blocks_per_tile; ++bi) {
-                    const int idx = j * blocks_per_tile + bi;
-                    int c2 = a.NB * a.S;  // beyond the pool: the copy fills zeros
-                    if (idx < n_table) {
-                        if (phys[bi] >= 0 && phys[bi] < a.NB) c2 = phys[bi] * a.S;
-                        else raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
-                    }
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const uint32_t off = st * 2 * kHalf + hf * kHalf + bi * a.S * 128;
-                        tma_load_3d_nohint(sb + kOffK + off, &kmap, hf * 64, h, c2, b);
-                        tma_load_3d_nohint(sb + kOffV + off, &vmap, hf * 64, h, c2, b);
-                    }
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d_nohint(sb + kOffK + ks * 2 * kHalf + hf * kHalf + bi * a.S * 128, &kmap, hf * 64,
+                                           h, rows[bi], kb);
                 }
-                issued = j + 1;
+                k_issued = j + 1;
+                if (j >= kVStages &&
+                    !mbar_wait_bounded(bar + 8 * (kBarVEmpty + vs), (j / kVStages - 1) & 1, a.timeout_ns)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t vb = bar + 8 * (kBarVFull + vs);
+                mbar_arrive_expect_tx(vb, 2 * kHalf);
+                for (int bi = 0; bi < blocks_per_tile; ++bi) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d_nohint(sb + kOffV + vs * 2 * kHalf + hf * kHalf + bi * a.S * 128, &vmap, hf * 64,
+                                           h, rows[bi], vb);
+                }
+                v_issued = j + 1;
+                if (j + 1 < n_tiles) tile_rows(j + 1, rows);  // the table read overlaps the next waits
             }
-            // its own last copies have landed before the CTA may finish (bounded)
-            for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
-                mbar_wait_bounded(bar + 8 * (kBarKvFull + (t & 1)), (t >> 1) & 1, a.timeout_ns);
+            // its own copies have landed before the CTA may finish (bounded)
+            for (int t = k_issued - kKStages < 0 ? 0 : k_issued - kKStages; t < k_issued; ++t)
+                mbar_wait_bounded(bar + 8 * (kBarKFull + t % kKStages), (t / kKStages) & 1, a.timeout_ns);
+            for (int t = v_issued - kVStages < 0 ? 0 : v_issued - kVStages; t < v_issued; ++t)
+                mbar_wait_bounded(bar + 8 * (kBarVFull + t % kVStages), (t / kVStages) & 1, a.timeout_ns);
             mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns);
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
             auto issue_s = [&](int j) {
-                const int st = j & 1;
+                const int ks = j % kKStages;
                 const uint32_t tS = tmem + 128 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t hf = kk >> 2, koff = (kk & 3) * 32;
                     const uint64_t ad = smem_desc_sw128(sb + kOffQ + hf * kHalf + koff, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sb + kOffK + st * 2 * kHalf + hf * kHalf + koff, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(sb + kOffK + ks * 2 * kHalf + hf * kHalf + koff, 16, 1024);
                     tc_mma_f16(tS, ad, bd, kIdescS, kk > 0);
                 }
                 tc_commit(bar + 8 * (kBarSFull + (j & 1)));
+                tc_commit(bar + 8 * (kBarKEmpty + ks));
             };
             bool ok = mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns) &&
-                      mbar_wait_bounded(bar + 8 * kBarKvFull, 0, a.timeout_ns);
+                      mbar_wait_bounded(bar + 8 * kBarKFull, 0, a.timeout_ns);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles) {
-                    const int b = (j + 1) & 1;
-                    ok = mbar_wait_bounded(bar + 8 * (kBarKvFull + b), ((j + 1) >> 1) & 1, a.timeout_ns) &&
-                         (j + 1 < 2 || mbar_wait_bounded(bar + 8 * (kBarSEmpty + b), ((j - 1) >> 1) & 1, a.timeout_ns));
+                    const int n = j + 1, b = n & 1;
+                    ok = mbar_wait_bounded(bar + 8 * (kBarKFull + n % kKStages), (n / kKStages) & 1, a.timeout_ns) &&
+                         (n < 2 || mbar_wait_bounded(bar + 8 * (kBarSEmpty + b), ((n - 2) >> 1) & 1, a.timeout_ns));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(j + 1);
+                    issue_s(n);
                 }
-                ok = mbar_wait_bounded(bar + 8 * kBarPFull, j & 1, a.timeout_ns);
+                const int b = j & 1, vs = j % kVStages;
+                ok = mbar_wait_bounded(bar + 8 * (kBarPFull + b), (j >> 1) & 1, a.timeout_ns) &&
+                     mbar_wait_bounded(bar + 8 * (kBarVFull + vs), (j / kVStages) & 1, a.timeout_ns);
                 if (!ok) break;
                 tc_fence_after();
-                const int st = j & 1;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t hf = kk >> 2, koff = (kk & 3) * 32;
-                    const uint64_t ad = smem_desc_sw128(sb + kOffP + hf * kHalf + koff, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sb + kOffV + st * 2 * kHalf + kk * 2048, kHalf, 1024);
-                    tc_mma_f16(tO, ad, bd, kIdescPV, (j > 0) || (kk > 0));
+                    const uint64_t bd = smem_desc_sw128(sb + kOffV + vs * 2 * kHalf + kk * 2048, kHalf, 1024);
+                    tc_mma_f16_ts(tO, tmem + kColP + 64 * b + 8 * kk, bd, kIdescPV, (j > 0) || (kk > 0));
                 }
-                tc_commit(bar + 8 * kBarODone);
-                tc_commit(bar + 8 * (kBarKvEmpty + st));
+                tc_commit(bar + 8 * (kBarODone + b));
+                tc_commit(bar + 8 * (kBarVEmpty + vs));
             }
             if (!ok) *abort_flag = 1;
         }
@@ -288,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t trow = static_cast<uint32_t>(quad * 32) << 16;
         const int col0 = half * 64;
         float m_ref = -INFINITY, l_run = 0.f;
-        int done = 0;  // tiles whose P.V was handed over
+        int done = 0;  // tiles whose P was handed over
         // exchange a value with the other warp of this row quadrant (bounded wait)
         auto exchange = [&](int k, float mine, float* rx) -> float {
             rx[half * 128 + r] = mine;
@@ -296,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(pb);
             if (!__all_sync(kFull, mbar_wait_bounded(pb, (k >> 1) & 1, a.timeout_ns))) *abort_flag = 1;
             return rx[(1 - half) * 128 + r];
+        };
+        // P.V of tile t (which used P buffer t & 1) has completed
+        auto wait_pv = [&](int t) -> bool {
+            return __all_sync(kFull, mbar_wait_bounded(bar + 8 * (kBarODone + (t & 1)), (t >> 1) & 1, a.timeout_ns));
         };
         for (int j = 0; j < n_tiles; ++j) {
             if (__any_sync(kFull, *abort_flag != 0)) break;
@@ -322,16 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float other = exchange(j, mraw, row_x + (j & 1) * 256);
             const float mt = fmaxf(mraw, other) * a.sm_log2;
-            // O may be rescaled and P overwritten only once P.V of the previous tile is done
-            if (j > 0) {
-                if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * kBarODone, (j - 1) & 1, a.timeout_ns))) {
+            const bool need = mt > m_ref + 8.f;
+            if (j > 0 && __any_sync(kFull, need)) {
+                // O may be rescaled only once the previous P.V is done (none is in flight then)
+                if (!wait_pv(j - 1)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-            }
-            const bool need = mt > m_ref + 8.f;
-            if (j > 0 && __any_sync(kFull, need)) {
                 const float m_new = need ? mt : m_ref;
                 const float alpha = ex2_approx(m_ref - m_new);
                 float o[64];
@@ -358,29 +390,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ls += p0 + p1;
                 pk[i / 2] = bf16x2_rn(p0, p1);
             }
-            uint8_t* prow = smem + kOffP + half * kHalf + r * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) * 16)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             l_run += ls;
-            // keys past kv_len in this tile: their V rows are not data, make them zero
+            // P buffer b is free once P.V of tile j - 2 is done
+            if (j >= 2 && !wait_pv(j - 2)) {
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            tmem_st32u(tmem + kColP + 64 * b + trow + half * 32, pk);
+            // keys past kv_len in this tile: their V rows are not data, make them zero once they have landed
             const int nvalid = min(kKeys, kv_len - tile0);
             if (nvalid < kKeys) {
+                const int vs = j % kVStages;
+                if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * (kBarVFull + vs), (j / kVStages) & 1,
+                                                         a.timeout_ns))) {
+                    *abort_flag = 1;
+                    break;
+                }
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int idx = tid; idx < (kKeys - nvalid) * 16; idx += kSoftmax) {
                     const int row = nvalid + idx / 16, hf = (idx / 8) & 1, ch = idx & 7;
-                    *reinterpret_cast<uint4*>(smem + kOffV + (j & 1) * 2 * kHalf + hf * kHalf + row * 128 + ch * 16) = z;
+                    *reinterpret_cast<uint4*>(smem + kOffV + vs * 2 * kHalf + hf * kHalf + row * 128 + ch * 16) = z;
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar + 8 * kBarPFull);
+            mbar_arrive(bar + 8 * (kBarPFull + b));
             done = j + 1;
         }
         // ---- the last P.V, the row sum over both halves, out = O / l
-        bool ok = !__any_sync(kFull, *abort_flag != 0) && done == n_tiles &&
-                  __all_sync(kFull, mbar_wait_bounded(bar + 8 * kBarODone, (n_tiles - 1) & 1, a.timeout_ns));
+        bool ok = !__any_sync(kFull, *abort_flag != 0) && done == n_tiles && wait_pv(n_tiles - 1);
         tc_fence_after();
         const float l_row = l_run + (ok ? exchange(n_tiles, l_run, row_x + (n_tiles & 1) * 256) : 0.f);
         float o[64];
