@@ -208,7 +208,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama3_8b_gqa")
     ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--batch", type=int, default=0, help="smaller batch of the Llama-3-8B workload (profiling)")
+    ap.add_argument("--batch", type=int, default=0, help="smaller decode batch of the Llama-3-8B or Llama-70B mixed workload (profiling)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the chunked-prefill kernel on a pool holding just the chunk's sequence")
     ap.add_argument("--swap-only", action="store_true",
@@ -244,7 +244,7 @@ def main():
 
     # every rank serves its own batch (sequences shard across GPUs; no exchange)
     kw = {"seed": wl.CONFIG_SEEDS[args.config] + 1000 * rank} if args.config != "llama70b_mixed_fp8" else {}
-    if args.batch and args.config == "llama3_8b_gqa":
+    if args.batch and args.config in ("llama3_8b_gqa", "llama70b_mixed_bf16", "llama70b_mixed_fp8"):
         kw["batch"] = args.batch
     w = wl.make(args.config, **kw)
     st = DeviceStep(w, num_splits=args.num_splits)

@@ -571,9 +571,7 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     } else {
         if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes())
             return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
-        const int rows_q = 128 / G;
-        e = launch_paged_prefill_ws(qm, km, vm, a, (num_q_tokens + rows_q - 1) / rows_q,
-                                    static_cast<cudaStream_t>(stream));
+        e = launch_paged_prefill_ws(qm, km, vm, a, static_cast<cudaStream_t>(stream));
     }
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
     return PKV_OK;
@@ -643,11 +641,7 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     a.cu_q = cu_q;
     a.q_starts = q_starts;
     a.kv_lens = kv_lens;
-    // an upper bound of the row tiles: every chunk adds at most one partial tile
-    const int rows_q = 128 / G;
-    const int grid_x = total_q_tokens / rows_q + num_seqs;
-    cudaError_t e;
-    e = launch_paged_prefill_ws(qm, km, vm, a, grid_x, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_paged_prefill_ws(qm, km, vm, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_varlen launch");
     return PKV_OK;
 }

@@ -26,7 +26,7 @@ int prefill_ws_max_seqs();
 
 // bf16 caches, warp-specialised, one or several chunks (prefill_ws.cu)
 cudaError_t launch_paged_prefill_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                    const PrefillArgs& a, int grid_x, cudaStream_t stream);
+                                    const PrefillArgs& a, cudaStream_t stream);
 
 cudaError_t launch_paged_prefill(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                  const PrefillArgs& a, int narrow, cudaStream_t stream);  // 0 bf16, 1 FP8, 2 INT8
