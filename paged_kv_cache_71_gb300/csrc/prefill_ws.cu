@@ -9,21 +9,28 @@
 //
 // A CTA owns two tiles of 128 query rows (each 128 / G tokens x the G query
 // heads of one KV head) of one chunk, A and B, and walks the chunk's keys in
-// tiles of 64, each K/V tile serving both query tiles:
-//   * warp 8 (producer) copies K and V tiles with TMA (128-byte swizzle,
-//     one block of the block table per copy) into two 4-deep rings, reading
-//     the block table one tile ahead;
-//   * warp 9 (one thread) issues the tcgen05 MMAs in the order
-//     P_A(j).V(j), S_A(j+1), P_B(j).V(j), S_B(j+1): while the softmax of one
-//     query tile runs, the tensor pipe works for the other (ping-pong);
+// tiles of 64, each K/V tile serving both query tiles.  TMEM holds, per
+// query tile, two score buffers (fp32, 64 keys; the bf16 P of a key tile is
+// written over the first half of its own score buffer) and the output
+// accumulator O (fp32, 128 dims):
+//   * warps 8 and 10 (producers) copy Q once and the K tiles (warp 8) and the
+//     V tiles (warp 10) with TMA (128-byte swizzle, one block of the block
+//     table per copy, one lane per block) into two 4-deep rings; block-table
+//     entries are read 32 at a time, a batch ahead;
+//   * warps 9 and 11 issue the tcgen05 MMAs (each warp runs its loop, one
+//     elected lane issues): warp 9 S_A(j), S_B(j) into the buffers that
+//     P(j-2) was read from, as soon as P(j-2).V has completed; warp 11
+//     P_A(j).V(j), P_B(j).V(j) once the softmax of tile j is done.  So the
+//     scores of the next tile are computed while the softmax works, and
+//     neither kind of MMA waits behind the other's issue;
 //   * warps 0-3 (query tile A) and 4-7 (tile B): one thread per row reads its
-//     64 scores from TMEM, keeps the running maximum and sum, writes bf16
-//     P to TMEM (read there by the P.V MMA) and rescales its O row in TMEM
-//     only when the row maximum grows by more than 8 (log2 units).
-// S(j+1) of a tile is committed after P.V(j) of the same tile, so seeing
-// S(j+1) also means O is no longer being written.  Hand-offs are mbarriers;
-// every wait is bounded; on timeout a role records the error and leaves its
-// loop, the CTA drains its own MMAs and copies (bounded) and frees TMEM.
+//     64 scores, keeps the running maximum and sum, writes bf16 P over them,
+//     and rescales its O row (after the previous P.V has completed) only
+//     when the row maximum grows by more than 8 (log2 units).
+// Hand-offs are mbarriers, one per buffer where a phase could otherwise be
+// overtaken; every wait is bounded; on timeout a role records the error and
+// leaves its loop, the CTA drains its own MMAs and copies (bounded) and
+// frees TMEM.
 #include "prefill.cuh"
 
 namespace pkv {
@@ -39,22 +46,22 @@ constexpr int kOffK = kOffQ + 4 * kQHalf;      // kStages x 2 halves
 constexpr int kOffV = kOffK + kStages * 2 * kKvHalf;
 constexpr int kOffMeta = kOffV + kStages * 2 * kKvHalf;
 constexpr int kTmemCols = 512;
-constexpr int kColS = 0;     // + 64 * tile: scores (fp32, 64 keys)
-constexpr int kColP = 128;   // + 32 * tile: probabilities (bf16 pairs, 64 keys)
+constexpr int kColS = 0;     // + 128 * tile + 64 * buffer: scores (fp32, 64 keys); P over the first 32 columns
 constexpr int kColO = 256;   // + 128 * tile: output accumulator (fp32, 128 dims)
 constexpr int kSoftmax = 256;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // + producer warps 8 (K) and 10 (V), MMA warps 9 (S) and 11 (P.V)
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kKeys, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
 
-// mbarrier slots (8 bytes each)
+// mbarrier slots (8 bytes each); "tb" = 2 * tile + buffer
 constexpr int kBarKFull = 0;                      // + stage: K copies landed (expect_tx)
 constexpr int kBarKEmpty = kBarKFull + kStages;   // + stage: the S MMAs that read it done
 constexpr int kBarVFull = kBarKEmpty + kStages;   // + stage: V copies landed
 constexpr int kBarVEmpty = kBarVFull + kStages;   // + stage: the P.V MMAs that read it done
-constexpr int kBarSFull = kBarVEmpty + kStages;   // + tile: S written (and the tile's earlier P.V done)
-constexpr int kBarPFull = kBarSFull + 2;          // + tile: P written, O rescaled (128 arrivals)
-constexpr int kBarQFull = kBarPFull + 2;
+constexpr int kBarSFull = kBarVEmpty + kStages;   // + tb: S written
+constexpr int kBarPFull = kBarSFull + 4;          // + tb: P written, O rescaled (128 arrivals)
+constexpr int kBarPVDone = kBarPFull + 4;         // + tb: P.V of the key tile that used buffer b done
+constexpr int kBarQFull = kBarPVDone + 4;
 constexpr int kBarFinal = kBarQFull + 1;          // every MMA done
 constexpr int kBarDrain = kBarFinal + 1;          // after an abort: every MMA issued so far done
 constexpr int kNumBars = kBarDrain + 1;
@@ -62,7 +69,7 @@ constexpr int kMetaTmem = 8 * kNumBars;           // TMEM base address
 constexpr int kMetaAbort = kMetaTmem + 4;
 constexpr int kMetaTile = kMetaAbort + 4;         // chunk, first token (or -1)
 constexpr int kMetaPart = kMetaTile + 8;          // per-warp partial sums of the CTA-count scan
-constexpr int kMetaCount = 256;                   // CTAs per chunk, prefix
+constexpr int kMetaCount = 512;                   // CTAs per chunk, prefix
 constexpr int kMaxSeqs = 2048;                    // chunks per launch
 static_assert(kMetaPart + 4 * (kThreads / 32) <= kMetaCount, "meta slots overlap");
 
@@ -182,10 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int blocks_per_tile = kKeys / a.S;
 
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) {
-            const bool many = i == kBarPFull || i == kBarPFull + 1;
-            mbar_init(bar + 8 * i, many ? kSoftmax / 2 : 1);
-        }
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(bar + 8 * i, (i >= kBarPFull && i < kBarPFull + 4) ? kSoftmax / 2 : i == kBarDrain ? 2 : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -198,135 +203,131 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
-        // ------------------------------------------------ producer: Q, then K and V tiles ahead of use
-        if (lane == 0) {
+    if (warp == 8 || warp == 10) {
+        // ------------------------------------------------ producer warps: warp 8 copies Q and the K tiles,
+        // warp 10 the V tiles.  Block-table entries come 32 at a time (one per lane, the next batch loaded a
+        // batch ahead) and are handed out by shuffle; lane bi issues the copies of block bi of a key tile.
+        const bool is_v = warp == 10;
+        if (!is_v && lane == 0) {
             prefetch_tensormap(&qmap);
             prefetch_tensormap(&kmap);
-            prefetch_tensormap(&vmap);
             const uint32_t qb = bar + 8 * kBarQFull;
             mbar_arrive_expect_tx(qb, (has_b ? 4 : 2) * kQHalf);
             for (int t = 0; t < (has_b ? 2 : 1); ++t)
                 for (int hf = 0; hf < 2; ++hf)
                     tma_load_3d_nohint(sb + kOffQ + (2 * t + hf) * kQHalf, &qmap, hf * 64, h * a.G,
                                        q_base + i0 + t * rows_q, qb);
-            // pool rows of the blocks of one key tile (beyond the pool: the copy fills zeros)
-            auto tile_rows = [&](int j, int (&c2)[kKeys / 8]) {
-#pragma unroll
-                for (int bi = 0; bi < kKeys / 8; ++bi) {
-                    const int idx = j * blocks_per_tile + bi;
-                    c2[bi] = (bi < blocks_per_tile && idx < n_table) ? table[idx] : -1;
-                }
-#pragma unroll
-                for (int bi = 0; bi < kKeys / 8; ++bi) {
-                    const int idx = j * blocks_per_tile + bi;
-                    int r = a.NB * a.S;
-                    if (bi < blocks_per_tile && idx < n_table) {
-                        if (c2[bi] >= 0 && c2[bi] < a.NB) r = c2[bi] * a.S;
-                        else raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
-                    }
-                    c2[bi] = r;
-                }
-            };
-            int rows[kKeys / 8];
-            tile_rows(0, rows);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % kStages;
-                const uint32_t ph = (j / kStages - 1) & 1;
-                if (j >= kStages && !mbar_wait_bounded(bar + 8 * (kBarKEmpty + st), ph, a.timeout_ns)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                if (*abort_flag) break;
-                const uint32_t kb = bar + 8 * (kBarKFull + st);
-                mbar_arrive_expect_tx(kb, 2 * kKvHalf);
-                for (int bi = 0; bi < blocks_per_tile; ++bi)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d_nohint(sb + kOffK + (2 * st + hf) * kKvHalf + bi * a.S * 128, &kmap, hf * 64, h,
-                                           rows[bi], kb);
-                k_issued = j + 1;
-                if (j >= kStages && !mbar_wait_bounded(bar + 8 * (kBarVEmpty + st), ph, a.timeout_ns)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                const uint32_t vb = bar + 8 * (kBarVFull + st);
-                mbar_arrive_expect_tx(vb, 2 * kKvHalf);
-                for (int bi = 0; bi < blocks_per_tile; ++bi)
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d_nohint(sb + kOffV + (2 * st + hf) * kKvHalf + bi * a.S * 128, &vmap, hf * 64, h,
-                                           rows[bi], vb);
-                v_issued = j + 1;
-                if (j + 1 < n_tiles) tile_rows(j + 1, rows);  // the table read overlaps the next waits
-            }
-            // its own copies have landed before the CTA may finish (bounded)
-            for (int t = k_issued - kStages < 0 ? 0 : k_issued - kStages; t < k_issued; ++t)
-                mbar_wait_bounded(bar + 8 * (kBarKFull + t % kStages), (t / kStages) & 1, a.timeout_ns);
-            for (int t = v_issued - kStages < 0 ? 0 : v_issued - kStages; t < v_issued; ++t)
-                mbar_wait_bounded(bar + 8 * (kBarVFull + t % kStages), (t / kStages) & 1, a.timeout_ns);
-            mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns);
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------ MMA issuer (one thread)
+        if (is_v && lane == 0) prefetch_tensormap(&vmap);
+        const CUtensorMap* map = is_v ? &vmap : &kmap;
+        const int full = is_v ? kBarVFull : kBarKFull, empty = is_v ? kBarVEmpty : kBarKEmpty;
+        const uint32_t dst0 = sb + (is_v ? kOffV : kOffK);
+        auto entry = [&](int idx) { return idx < n_table ? __ldg(table + idx) : -1; };
+        int cur_c = 0, cur = entry(lane), nxt = entry(32 + lane);
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % kStages;
+            const int idx0 = j * blocks_per_tile;  // blocks_per_tile divides 32: a tile stays in one batch
+            if ((idx0 >> 5) != cur_c) {
+                cur = nxt;
+                cur_c = idx0 >> 5;
+                nxt = entry((cur_c + 1) * 32 + lane);
+            }
+            const int e = __shfl_sync(kFull, cur, (idx0 + lane) & 31);
+            const bool mine = lane < blocks_per_tile;
+            int row = a.NB * a.S;  // beyond the pool: the copy fills zeros
+            if (mine && idx0 + lane < n_table) {
+                if (e >= 0 && e < a.NB) row = e * a.S;
+                else if (!is_v) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
+            }
+            if (j >= kStages && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (empty + st), (j / kStages - 1) & 1,
+                                                                     a.timeout_ns))) {
+                if (lane == 0) *abort_flag = 1;
+                break;
+            }
+            if (__any_sync(kFull, *abort_flag != 0)) break;
+            const uint32_t fb = bar + 8 * (full + st);
+            if (lane == 0) mbar_arrive_expect_tx(fb, 2 * kKvHalf);
+            __syncwarp();
+            if (mine)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d_nohint(dst0 + (2 * st + hf) * kKvHalf + lane * a.S * 128, map, hf * 64, h, row, fb);
+            issued = j + 1;
+        }
+        // its own copies have landed before the CTA may finish (bounded)
         if (lane == 0) {
+            for (int t = issued - kStages < 0 ? 0 : issued - kStages; t < issued; ++t)
+                mbar_wait_bounded(bar + 8 * (full + t % kStages), (t / kStages) & 1, a.timeout_ns);
+            if (!is_v) mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns);
+        }
+    } else if (warp == 9 || warp == 11) {
+        // ------------------------------------------------ MMA warps: warp 9 issues the S MMAs, warp 11 the P.V
+        // MMAs; each warp runs its loop as a whole and one elected lane issues (operands stay warp-uniform)
+        // descriptors are built once; an operand at byte offset x from the tile base is base + (x >> 4)
+        // (the 14-bit start-address field cannot carry: shared addresses stay below 256 KB)
+        const uint64_t d_kmaj = smem_desc_sw128(sb, 16, 1024);       // Q and K: K-major rows of 128 B
+        const uint64_t d_v = smem_desc_sw128(sb, kKvHalf, 1024);     // V: N-major, d-halves kKvHalf apart
+        auto wait4 = [&](uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) {
+            return __all_sync(kFull, mbar_spin4_bounded(b0, p0, b1, p1, b2, p2, b2, p2, a.timeout_ns));
+        };
+        bool ok = true;
+        if (warp == 9) {
+            // S(j) of both query tiles into buffer j & 1, which P(j-2) was read from
             auto issue_s = [&](int t, int j) {
-                const int st = j % kStages;
+                const uint64_t a0 = d_kmaj + ((kOffQ + 2 * t * kQHalf) >> 4);
+                const uint64_t b0 = d_kmaj + ((kOffK + 2 * (j % kStages) * kKvHalf) >> 4);
+                const uint32_t d = tmem + kColS + 128 * t + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t hf = kk >> 2, koff = (kk & 3) * 32;
-                    const uint64_t ad = smem_desc_sw128(sb + kOffQ + (2 * t + hf) * kQHalf + koff, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(sb + kOffK + (2 * st + hf) * kKvHalf + koff, 16, 1024);
-                    tc_mma_f16(tmem + kColS + 64 * t, ad, bd, kIdescS, kk > 0);
+                    const uint32_t off_a = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+                    const uint32_t off_b = ((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4;
+                    tc_mma_f16_warp(d, a0 + off_a, b0 + off_b, kIdescS, kk > 0);
                 }
-                tc_commit(bar + 8 * (kBarSFull + t));
+                tc_commit_warp(bar + 8 * (kBarSFull + 2 * t + (j & 1)));
             };
-            auto issue_pv = [&](int t, int j) {
-                const int st = j % kStages;
-#pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(sb + kOffV + 2 * st * kKvHalf + kk * 2048, kKvHalf, 1024);
-                    tc_mma_f16_ts(tmem + kColO + 128 * t, tmem + kColP + 32 * t + 8 * kk, bd, kIdescPV,
-                                  (j > 0) || (kk > 0));
+            const uint32_t qb = bar + 8 * kBarQFull;
+            for (int j = 0; j < n_tiles; ++j) {
+                const uint32_t kb = bar + 8 * (kBarKFull + j % kStages), kph = (j / kStages) & 1;
+                if (j < 2) {
+                    ok = wait4(qb, 0, qb, 0, kb, kph);
+                } else {
+                    const uint32_t pva = bar + 8 * (kBarPVDone + (j & 1));
+                    const uint32_t pvb = has_b ? pva + 16 : pva, pph = ((j - 2) >> 1) & 1;
+                    ok = wait4(pva, pph, pvb, pph, kb, kph);
                 }
-            };
-            bool ok = mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns) &&
-                      mbar_wait_bounded(bar + 8 * kBarKFull, 0, a.timeout_ns);
-            if (ok) {
+                if (!ok) break;
                 tc_fence_after();
-                issue_s(0, 0);
-                if (has_b) issue_s(1, 0);
-                tc_commit(bar + 8 * kBarKEmpty);
+                issue_s(0, j);
+                if (has_b) issue_s(1, j);
+                tc_commit_warp(bar + 8 * (kBarKEmpty + j % kStages));
             }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j % kStages, n = j + 1;
-                ok = mbar_wait_bounded(bar + 8 * kBarPFull, j & 1, a.timeout_ns) &&
-                     mbar_wait_bounded(bar + 8 * (kBarVFull + st), (j / kStages) & 1, a.timeout_ns);
+        } else {
+            // P(j).V(j) of both query tiles once their softmax is done
+            auto issue_pv = [&](int t, int j) {
+                const uint64_t b0 = d_v + ((kOffV + 2 * (j % kStages) * kKvHalf) >> 4);
+                const uint32_t d = tmem + kColO + 128 * t, p = tmem + kColS + 128 * t + 64 * (j & 1);
+                const uint32_t acc0 = j > 0;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+                tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
+            };
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % kStages, b = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                const uint32_t pa = bar + 8 * (kBarPFull + b), pb = has_b ? bar + 8 * (kBarPFull + 2 + b) : pa;
+                ok = wait4(pa, ph, pb, ph, bar + 8 * (kBarVFull + st), (j / kStages) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(0, j);
-                if (n < n_tiles) {
-                    ok = mbar_wait_bounded(bar + 8 * (kBarKFull + n % kStages), (n / kStages) & 1, a.timeout_ns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(0, n);
-                }
-                if (has_b) {
-                    ok = mbar_wait_bounded(bar + 8 * (kBarPFull + 1), j & 1, a.timeout_ns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(1, j);
-                }
-                tc_commit(bar + 8 * (kBarVEmpty + st));
-                if (n < n_tiles) {
-                    if (has_b) issue_s(1, n);
-                    tc_commit(bar + 8 * (kBarKEmpty + n % kStages));
-                }
+                if (has_b) issue_pv(1, j);
+                tc_commit_warp(bar + 8 * (kBarVEmpty + st));
             }
-            if (ok) tc_commit(bar + 8 * kBarFinal);
-            else *abort_flag = 1;
+            // the last P.V follows every S MMA (it needed that tile's softmax), so this covers all MMAs
+            if (ok) tc_commit_warp(bar + 8 * kBarFinal);
         }
+        if (!ok && lane == 0) *abort_flag = 1;
     } else {
         // ------------------------------------------------ softmax: warps 0-3 query tile A, 4-7 tile B
         const int t = warp >> 2, quad = warp & 3;
@@ -335,21 +336,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qi = qt0 + r / a.G;
         const int qpos = q_start + qi;
         const uint32_t trow = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + kColS + 64 * t + trow, tP = tmem + kColP + 32 * t + trow;
         const uint32_t tO = tmem + kColO + 128 * t + trow;
         float m_ref = -INFINITY, l_run = 0.f;
         int done = 0;
         const bool active = t == 0 || has_b;
+        bool s_ready = false;  // the next tile's scores were seen complete ahead of time
         for (int j = 0; active && j < n_tiles; ++j) {
-            if (__any_sync(kFull, *abort_flag != 0)) break;
-            const int tile0 = j * kKeys;
-            if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * (kBarSFull + t), j & 1, a.timeout_ns))) {
+            const int tile0 = j * kKeys, b = j & 1;
+            const uint32_t tS = tmem + kColS + 128 * t + 64 * b + trow;
+            if (!__all_sync(kFull, s_ready) &&
+                !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (kBarSFull + 2 * t + b), (j >> 1) & 1,
+                                                     a.timeout_ns))) {
                 *abort_flag = 1;
                 break;
             }
             tc_fence_after();
             float v[64];
             tmem_ld64(tS, v);
+            // test the next tile's scores now; the answer is used only when that tile starts
+            s_ready = j + 1 < n_tiles && mbar_test(bar + 8 * (kBarSFull + 2 * t + (b ^ 1)), ((j + 1) >> 1) & 1);
             const bool masked = (tile0 + kKeys - 1 > q_start + qt0) || (tile0 + kKeys > kv_len);
             const int lim = min(kv_len, qpos + 1) - tile0;
             float mx[8];
@@ -386,9 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[i / 2] = bf16x2_rn(p0, p1);
             }
             l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-            tmem_st32u(tP, pk);
+            tmem_st32u(tS, pk);  // P over the scores just read (this thread's lane only)
             if (rescale) {
-                // the tile's previous P.V completed before its S(j) was committed: O is at rest
+                // O may be touched only once the previous P.V of this query tile has completed
+                if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * (kBarPVDone + 2 * t + ((j - 1) & 1)),
+                                                         ((j - 1) >> 1) & 1, a.timeout_ns))) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     float o[64];
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
             }
             tc_fence_before();
-            mbar_arrive(bar + 8 * (kBarPFull + t));
+            mbar_arrive(bar + 8 * (kBarPFull + 2 * t + b));
             done = j + 1;
         }
         // ---- every MMA done, out = O / l
@@ -450,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- drain: nothing of this CTA may still be in flight when TMEM is freed and the CTA exits
     __syncthreads();
-    if (warp == 9 && lane == 0 && *abort_flag) {
-        tc_commit(bar + 8 * kBarDrain);  // arrives once every MMA issued so far has completed
+    if ((warp == 9 || warp == 11) && *abort_flag) {
+        tc_commit_warp(bar + 8 * kBarDrain);  // arrives once every MMA this warp issued has completed
         mbar_wait_bounded(bar + 8 * kBarDrain, 0, a.timeout_ns);
     }
     __syncthreads();
