@@ -107,6 +107,21 @@ __device__ __forceinline__ bool mbar_test4(uint32_t b0, uint32_t p0, uint32_t b1
     return ok != 0;
 }
 
+// Non-blocking test of two mbarrier phases at once.
+__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q, [%3], %4;\n\t"
+        "and.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
+        : "memory");
+    return ok != 0;
+}
+
 // Spin (without suspending) until a phase completes, giving up after `limit_ns` (returns false).  For
 // hand-offs on the critical path, where a suspended waiter would wake late.
 __device__ __forceinline__ bool mbar_spin_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -114,6 +129,17 @@ __device__ __forceinline__ bool mbar_spin_bounded(uint32_t bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_test(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// As above for two phases at once.
+__device__ __forceinline__ bool mbar_spin2_bounded(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                                   uint64_t limit_ns) {
+    if (mbar_test2(b0, p0, b1, p1)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_test2(b0, p0, b1, p1)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

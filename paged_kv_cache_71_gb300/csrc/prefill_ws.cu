@@ -268,9 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (the 14-bit start-address field cannot carry: shared addresses stay below 256 KB)
         const uint64_t d_kmaj = smem_desc_sw128(sb, 16, 1024);       // Q and K: K-major rows of 128 B
         const uint64_t d_v = smem_desc_sw128(sb, kKvHalf, 1024);     // V: N-major, d-halves kKvHalf apart
-        auto wait4 = [&](uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) {
-            return __all_sync(kFull, mbar_spin4_bounded(b0, p0, b1, p1, b2, p2, b2, p2, a.timeout_ns));
-        };
         bool ok = true;
         if (warp == 9) {
             // S(j) of both query tiles into buffer j & 1, which P(j-2) was read from
@@ -287,19 +284,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_warp(bar + 8 * (kBarSFull + 2 * t + (j & 1)));
             };
             const uint32_t qb = bar + 8 * kBarQFull;
-            for (int j = 0; j < n_tiles; ++j) {
+            for (int j = 0; ok && j < n_tiles; ++j) {
                 const uint32_t kb = bar + 8 * (kBarKFull + j % kStages), kph = (j / kStages) & 1;
-                if (j < 2) {
-                    ok = wait4(qb, 0, qb, 0, kb, kph);
-                } else {
-                    const uint32_t pva = bar + 8 * (kBarPVDone + (j & 1));
-                    const uint32_t pvb = has_b ? pva + 16 : pva, pph = ((j - 2) >> 1) & 1;
-                    ok = wait4(pva, pph, pvb, pph, kb, kph);
+                for (int t = 0; t < (has_b ? 2 : 1); ++t) {
+                    // query tile t: Q and K(j) landed, and P_t(j-2).V done with the buffer
+                    ok = j < 2 ? __all_sync(kFull, mbar_spin2_bounded(qb, 0, kb, kph, a.timeout_ns))
+                               : __all_sync(kFull, mbar_spin2_bounded(bar + 8 * (kBarPVDone + 2 * t + (j & 1)),
+                                                                      ((j - 2) >> 1) & 1, kb, kph, a.timeout_ns));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(t, j);
                 }
                 if (!ok) break;
-                tc_fence_after();
-                issue_s(0, j);
-                if (has_b) issue_s(1, j);
                 tc_commit_warp(bar + 8 * (kBarKEmpty + j % kStages));
             }
         } else {
@@ -313,15 +309,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
                 tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
             };
-            for (int j = 0; j < n_tiles; ++j) {
+            for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kStages, b = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                const uint32_t pa = bar + 8 * (kBarPFull + b), pb = has_b ? bar + 8 * (kBarPFull + 2 + b) : pa;
-                ok = wait4(pa, ph, pb, ph, bar + 8 * (kBarVFull + st), (j / kStages) & 1);
+                const uint32_t ph = (j >> 1) & 1, vb = bar + 8 * (kBarVFull + st), vph = (j / kStages) & 1;
+                for (int t = 0; t < (has_b ? 2 : 1); ++t) {
+                    // query tile t: its softmax of tile j done and V(j) landed
+                    ok = __all_sync(kFull, mbar_spin2_bounded(bar + 8 * (kBarPFull + 2 * t + b), ph, vb, vph,
+                                                              a.timeout_ns));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(t, j);
+                }
                 if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, j);
-                if (has_b) issue_pv(1, j);
                 tc_commit_warp(bar + 8 * (kBarVEmpty + st));
             }
             // the last P.V follows every S MMA (it needed that tile's softmax), so this covers all MMAs
