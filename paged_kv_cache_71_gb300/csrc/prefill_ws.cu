@@ -82,6 +82,13 @@ __device__ __forceinline__ void tma_load_3d_nohint(uint32_t dst, const CUtensorM
         : "memory");
 }
 
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -361,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
             if (!masked) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], v[i]);
+                for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], v[i], v[i + 1]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], (i < lim) ? v[i] : -INFINITY);
@@ -375,21 +382,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_new = need ? mt : m_ref;
             const float alpha = ex2_approx(m_ref - m_new);
             m_ref = m_new;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            const float neg_m = -m_ref;
+            // exponent arguments and running sums on packed fp32 pairs (two elements per instruction)
+            const float2 sc2 = make_float2(a.sm_log2, a.sm_log2), nm2 = make_float2(-m_ref, -m_ref);
+            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 64; i += 2) {
-                float p0 = ex2_approx(fmaf(v[i], a.sm_log2, neg_m));
-                float p1 = ex2_approx(fmaf(v[i + 1], a.sm_log2, neg_m));
+                const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), sc2, nm2);
+                float p0 = ex2_approx(x.x);
+                float p1 = ex2_approx(x.y);
                 if (masked) {
                     p0 = (i < lim) ? p0 : 0.f;
                     p1 = (i + 1 < lim) ? p1 : 0.f;
                 }
-                ls[(i >> 1) & 3] += p0 + p1;
+                ls2[(i >> 1) & 1] = __fadd2_rn(ls2[(i >> 1) & 1], make_float2(p0, p1));
                 pk[i / 2] = bf16x2_rn(p0, p1);
             }
-            l_run = l_run * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            const float2 lsum = __fadd2_rn(ls2[0], ls2[1]);
+            l_run = l_run * alpha + (lsum.x + lsum.y);
             tmem_st32u(tS, pk);  // P over the scores just read (this thread's lane only)
             if (rescale) {
                 // O may be touched only once the previous P.V of this query tile has completed
