@@ -76,6 +76,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+constexpr unsigned kSpinSleepNs = 20;  // pause between the tests of a spinning wait
+
 // Non-blocking test of one mbarrier phase (never suspends the thread).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -128,6 +130,7 @@ __device__ __forceinline__ bool mbar_spin_bounded(uint32_t bar, uint32_t parity,
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        __nanosleep(kSpinSleepNs);  // yield the issue slot to the warps doing the math
         if (mbar_test(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -139,6 +142,7 @@ __device__ __forceinline__ bool mbar_spin2_bounded(uint32_t b0, uint32_t p0, uin
     if (mbar_test2(b0, p0, b1, p1)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        __nanosleep(kSpinSleepNs);
         if (mbar_test2(b0, p0, b1, p1)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -150,6 +154,7 @@ __device__ __forceinline__ bool mbar_spin4_bounded(uint32_t b0, uint32_t p0, uin
     if (mbar_test4(b0, p0, b1, p1, b2, p2, b3, p3)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        __nanosleep(kSpinSleepNs);
         if (mbar_test4(b0, p0, b1, p1, b2, p2, b3, p3)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
