@@ -344,7 +344,7 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, steps=3, max_seconds=20.0)
+        cpu = time_oracle(w, steps=1000, max_seconds=12.0)
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
 
