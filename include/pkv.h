@@ -192,9 +192,11 @@ pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, in
  * total_q_tokens, kv_len too short, more table entries than max_blocks_per_seq)
  * sets PKV_DEVERR_BAD_LENGTH and leaves that chunk's rows unwritten; a table
  * entry outside the pool sets PKV_DEVERR_BAD_BLOCK.
+ * An FP8 or INT8 cache is widened to bf16 on chip (exactly), its per-tensor
+ * scales applied to the scores and the output, as in pkv_paged_prefill_chunk.
  * scale must be positive.
- * Supported: bf16 queries, bf16 cache, head_dim 128, block_size 8/16/32, G dividing 128,
- *   num_seqs <= 2048.  No workspace.
+ * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
+ *   G dividing 128, num_seqs <= 2048.  No workspace.
  */
 pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
                                     const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,

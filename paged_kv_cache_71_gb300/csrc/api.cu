@@ -542,8 +542,6 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
     DeviceInfo di;
     if ((st = device_info(&di)) != PKV_OK) return st;
-    if (static_cast<size_t>(di.smem_optin) < prefill_smem_bytes(fp8))
-        return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
     CUtensorMap qm, km, vm;
     if ((st = tensor_map_sw128(&qm, q, false, 128, num_q_heads, num_q_tokens, G, 128 / G)) != PKV_OK) return st;
     const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
@@ -565,14 +563,10 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
     a.out_mul = fp8 ? cache->v_scale : 1.f;
     a.timeout_ns = 2000000000ull;
-    cudaError_t e;
-    if (fp8) {
-        e = launch_paged_prefill(qm, km, vm, a, cache->dtype == PKV_INT8 ? 2 : 1, static_cast<cudaStream_t>(stream));
-    } else {
-        if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes())
-            return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
-        e = launch_paged_prefill_ws(qm, km, vm, a, static_cast<cudaStream_t>(stream));
-    }
+    const int nk = cache->dtype == PKV_INT8 ? 2 : fp8 ? 1 : 0;
+    if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes(nk))
+        return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
+    cudaError_t e = launch_paged_prefill_ws(qm, km, vm, a, nk, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_chunk launch");
     return PKV_OK;
 }
@@ -593,8 +587,10 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     if (num_q_heads % Hkv != 0)
         return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
     const int G = num_q_heads / Hkv;
-    if (q_dtype != PKV_BF16 || cache->dtype != PKV_BF16)
-        return fail(PKV_ERR_UNSUPPORTED, "varlen prefill supports bf16 queries with a bf16 cache");
+    if (q_dtype != PKV_BF16 || (cache->dtype != PKV_BF16 && !narrow(cache->dtype)))
+        return fail(PKV_ERR_UNSUPPORTED, "varlen prefill supports bf16 queries with a bf16, FP8 or INT8 cache");
+    const bool fp8 = narrow(cache->dtype);
+    const int nk = cache->dtype == PKV_INT8 ? 2 : fp8 ? 1 : 0;
     if (D != 128) return fail(PKV_ERR_UNSUPPORTED, "prefill supports head_dim 128");
     if (S < 8) return fail(PKV_ERR_UNSUPPORTED, "prefill supports block_size 8, 16, 32");
     if (G > 128 || 128 % G != 0) return fail(PKV_ERR_UNSUPPORTED, "GQA group %d must divide 128", G);
@@ -613,13 +609,13 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
     DeviceInfo di;
     if ((st = device_info(&di)) != PKV_OK) return st;
-    if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes())
+    if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes(nk))
         return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the prefill tile");
     CUtensorMap qm, km, vm;
     if ((st = tensor_map_sw128(&qm, q, false, 128, num_q_heads, total_q_tokens, G, 128 / G)) != PKV_OK) return st;
     const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
-    if ((st = tensor_map_sw128(&km, k_cache, false, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
-    if ((st = tensor_map_sw128(&vm, v_cache, false, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&km, k_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
     PrefillArgs a;
     a.out = out;
     a.block_table = block_tables;
@@ -633,15 +629,15 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     a.S = S;
     a.NB = cache->num_blocks;
     a.n_table = max_blocks_per_seq;
-    a.sm_log2 = scale * 1.4426950408889634f;
-    a.out_mul = 1.f;
+    a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
+    a.out_mul = fp8 ? cache->v_scale : 1.f;
     a.timeout_ns = 2000000000ull;
     a.nseq = num_seqs;
     a.MB = max_blocks_per_seq;
     a.cu_q = cu_q;
     a.q_starts = q_starts;
     a.kv_lens = kv_lens;
-    cudaError_t e = launch_paged_prefill_ws(qm, km, vm, a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_paged_prefill_ws(qm, km, vm, a, nk, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_varlen launch");
     return PKV_OK;
 }

@@ -39,12 +39,21 @@ namespace {
 
 constexpr int kRows = 128, kKeys = 64;
 constexpr int kQHalf = kRows * 128;            // 64 head dims of 128 rows, bytes
-constexpr int kKvHalf = kKeys * 128;           // 64 head dims of 64 keys, bytes
-constexpr int kStages = 4;                     // K and V ring depth
+constexpr int kKvHalf = kKeys * 128;           // 64 head dims of 64 keys, bytes (bf16)
+constexpr int kStgSlot = kKeys * 128;          // one key tile of one-byte codes (128 head dims), bytes
 constexpr int kOffQ = 0;                       // tile A: 2 halves, tile B: 2 halves
-constexpr int kOffK = kOffQ + 4 * kQHalf;      // kStages x 2 halves
-constexpr int kOffV = kOffK + kStages * 2 * kKvHalf;
-constexpr int kOffMeta = kOffV + kStages * 2 * kKvHalf;
+
+// Shared-memory plan per cache kind (NARROW: 0 bf16, 1 FP8 E4M3 codes, 2 INT8 codes).  One-byte caches
+// land in a two-slot staging ring per operand and are widened to bf16 by the producer warps.
+template <int NARROW>
+struct Plan {
+    static constexpr int kStages = NARROW ? 3 : 4;                  // bf16 K and V ring depth
+    static constexpr int kOffK = kOffQ + 4 * kQHalf;                // kStages x 2 halves
+    static constexpr int kOffV = kOffK + kStages * 2 * kKvHalf;
+    static constexpr int kOffStg = kOffV + kStages * 2 * kKvHalf;   // K: 2 slots, then V: 2 slots
+    static constexpr int kOffMeta = kOffStg + (NARROW ? 4 * kStgSlot : 0);
+};
+constexpr int kMaxStages = 4;
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;     // + 128 * tile + 64 * buffer: scores (fp32, 64 keys); P over the first 32 columns
 constexpr int kColO = 256;   // + 128 * tile: output accumulator (fp32, 128 dims)
@@ -54,17 +63,18 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(128, kKeys, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
 
 // mbarrier slots (8 bytes each); "tb" = 2 * tile + buffer
-constexpr int kBarKFull = 0;                      // + stage: K copies landed (expect_tx)
-constexpr int kBarKEmpty = kBarKFull + kStages;   // + stage: the S MMAs that read it done
-constexpr int kBarVFull = kBarKEmpty + kStages;   // + stage: V copies landed
-constexpr int kBarVEmpty = kBarVFull + kStages;   // + stage: the P.V MMAs that read it done
-constexpr int kBarSFull = kBarVEmpty + kStages;   // + tb: S written
+constexpr int kBarKFull = 0;                         // + stage: K in the bf16 ring (copies landed / widened)
+constexpr int kBarKEmpty = kBarKFull + kMaxStages;   // + stage: the S MMAs that read it done
+constexpr int kBarVFull = kBarKEmpty + kMaxStages;   // + stage: V in the bf16 ring
+constexpr int kBarVEmpty = kBarVFull + kMaxStages;   // + stage: the P.V MMAs that read it done
+constexpr int kBarSFull = kBarVEmpty + kMaxStages;   // + tb: S written
 constexpr int kBarPFull = kBarSFull + 4;          // + tb: P written, O rescaled (128 arrivals)
 constexpr int kBarPVDone = kBarPFull + 4;         // + tb: P.V of the key tile that used buffer b done
 constexpr int kBarQFull = kBarPVDone + 4;
 constexpr int kBarFinal = kBarQFull + 1;          // every MMA done
 constexpr int kBarDrain = kBarFinal + 1;          // after an abort: every MMA issued so far done
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarStg = kBarDrain + 1;            // + 2 * (V ? 1 : 0) + slot: one-byte codes landed in staging
+constexpr int kNumBars = kBarStg + 4;
 constexpr int kMetaTmem = 8 * kNumBars;           // TMEM base address
 constexpr int kMetaAbort = kMetaTmem + 4;
 constexpr int kMetaTile = kMetaAbort + 4;         // chunk, first token (or -1)
@@ -97,9 +107,12 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 
 }  // namespace
 
+template <int NARROW>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+    constexpr int kStages = Plan<NARROW>::kStages, kOffK = Plan<NARROW>::kOffK, kOffV = Plan<NARROW>::kOffV;
+    constexpr int kOffStg = Plan<NARROW>::kOffStg, kOffMeta = Plan<NARROW>::kOffMeta;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -231,41 +244,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst0 = sb + (is_v ? kOffV : kOffK);
         auto entry = [&](int idx) { return idx < n_table ? __ldg(table + idx) : -1; };
         int cur_c = 0, cur = entry(lane), nxt = entry(32 + lane);
-        int issued = 0;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % kStages;
-            const int idx0 = j * blocks_per_tile;  // blocks_per_tile divides 32: a tile stays in one batch
+        // this lane's pool row for block `lane` of key tile jj (tiles asked for in increasing order)
+        auto tile_row = [&](int jj) {
+            const int idx0 = jj * blocks_per_tile;  // blocks_per_tile divides 32: a tile stays in one batch
             if ((idx0 >> 5) != cur_c) {
                 cur = nxt;
                 cur_c = idx0 >> 5;
                 nxt = entry((cur_c + 1) * 32 + lane);
             }
             const int e = __shfl_sync(kFull, cur, (idx0 + lane) & 31);
-            const bool mine = lane < blocks_per_tile;
             int row = a.NB * a.S;  // beyond the pool: the copy fills zeros
-            if (mine && idx0 + lane < n_table) {
+            if (lane < blocks_per_tile && idx0 + lane < n_table) {
                 if (e >= 0 && e < a.NB) row = e * a.S;
                 else if (!is_v) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
             }
-            if (j >= kStages && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (empty + st), (j / kStages - 1) & 1,
-                                                                     a.timeout_ns))) {
-                if (lane == 0) *abort_flag = 1;
-                break;
-            }
-            if (__any_sync(kFull, *abort_flag != 0)) break;
-            const uint32_t fb = bar + 8 * (full + st);
-            if (lane == 0) mbar_arrive_expect_tx(fb, 2 * kKvHalf);
-            __syncwarp();
-            if (mine)
+            return row;
+        };
+        // a free stage of the bf16 ring for key tile j
+        auto wait_free = [&](int j) {
+            return j < kStages || __all_sync(kFull, mbar_spin_bounded(bar + 8 * (empty + j % kStages),
+                                                                     (j / kStages - 1) & 1, a.timeout_ns));
+        };
+        int issued = 0, staged = 0, widened = 0;
+        if constexpr (NARROW == 0) {
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % kStages;
+                const int row = tile_row(j);
+                if (!wait_free(j)) {
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
+                if (__any_sync(kFull, *abort_flag != 0)) break;
+                const uint32_t fb = bar + 8 * (full + st);
+                if (lane == 0) mbar_arrive_expect_tx(fb, 2 * kKvHalf);
+                __syncwarp();
+                if (lane < blocks_per_tile)
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d_nohint(dst0 + (2 * st + hf) * kKvHalf + lane * a.S * 128, map, hf * 64, h, row, fb);
-            issued = j + 1;
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d_nohint(dst0 + (2 * st + hf) * kKvHalf + lane * a.S * 128, map, hf * 64, h, row,
+                                           fb);
+                issued = j + 1;
+            }
+        } else {
+            // one-byte codes: copy tile j+1 into its staging slot, then widen tile j into the bf16 ring
+            // (exact: every E4M3 and INT8 code is a bf16 value; the per-tensor scales go to the scores and
+            // the output).  128 codes per key row, rows in 128-byte swizzled lines like the bf16 halves.
+            const int sbar = kBarStg + (is_v ? 2 : 0);
+            const uint32_t stg0 = sb + kOffStg + (is_v ? 2 : 0) * kStgSlot;
+            auto stage = [&](int jj, int row) {
+                const uint32_t fb = bar + 8 * (sbar + (jj & 1));
+                if (lane == 0) mbar_arrive_expect_tx(fb, kStgSlot);
+                __syncwarp();
+                if (lane < blocks_per_tile)
+                    tma_load_3d_nohint(stg0 + (jj & 1) * kStgSlot + lane * a.S * 128, map, 0, h, row, fb);
+            };
+            auto widen = [&](int slot, int st) {
+                const uint8_t* src0 = smem + kOffStg + ((is_v ? 2 : 0) + slot) * kStgSlot;
+                uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * 2 * kKvHalf;
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = lane + 32 * rr, sw = r & 7;
+                    const uint8_t* src = src0 + r * 128;
+                    uint8_t* dst = dstb + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {  // 16 codes: head dims 16c .. 16c + 15
+                        const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ sw) * 16));
+                        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float2 f0, f1;
+                            if constexpr (NARROW == 2) {
+                                f0 = s8x2_to_float2(ws[i], 0);
+                                f1 = s8x2_to_float2(ws[i], 2);
+                            } else {
+                                f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                                f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                            }
+                            o[2 * i] = bf16x2_rn(f0.x, f0.y);
+                            o[2 * i + 1] = bf16x2_rn(f1.x, f1.y);
+                        }
+                        uint8_t* dh = dst + (c >> 2) * kKvHalf;
+                        const int lc = 2 * (c & 3);
+                        *reinterpret_cast<uint4*>(dh + ((lc ^ sw) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(dh + (((lc + 1) ^ sw) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            };
+            stage(0, tile_row(0));
+            staged = 1;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j % kStages;
+                if (j + 1 < n_tiles) {  // its slot was widened at j - 1 (and fenced): free for the copy
+                    stage(j + 1, tile_row(j + 1));
+                    staged = j + 2;
+                }
+                if (!__all_sync(kFull, mbar_spin_bounded(bar + 8 * (sbar + (j & 1)), (j >> 1) & 1, a.timeout_ns)) ||
+                    !wait_free(j)) {
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
+                widened = j + 1;
+                if (__any_sync(kFull, *abort_flag != 0)) break;
+                widen(j & 1, st);
+                fence_proxy_async_smem();  // the MMA (async proxy) reads what was written; the next copy overwrites
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar + 8 * (full + st));
+            }
         }
         // its own copies have landed before the CTA may finish (bounded)
         if (lane == 0) {
             for (int t = issued - kStages < 0 ? 0 : issued - kStages; t < issued; ++t)
                 mbar_wait_bounded(bar + 8 * (full + t % kStages), (t / kStages) & 1, a.timeout_ns);
+            for (int t = widened; t < staged; ++t)
+                mbar_wait_bounded(bar + 8 * (kBarStg + (is_v ? 2 : 0) + (t & 1)), (t >> 1) & 1, a.timeout_ns);
             if (!is_v) mbar_wait_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns);
         }
     } else if (warp == 9 || warp == 11) {
@@ -481,14 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-size_t prefill_ws_smem_bytes() { return static_cast<size_t>(kOffMeta) + kMetaCount + 4 * (kMaxSeqs + 1) + 1024; }
+template <int NARROW>
+static size_t ws_smem_bytes() {
+    return static_cast<size_t>(Plan<NARROW>::kOffMeta) + kMetaCount + 4 * (kMaxSeqs + 1) + 1024;
+}
+
+size_t prefill_ws_smem_bytes(int narrow) { return narrow ? ws_smem_bytes<1>() : ws_smem_bytes<0>(); }
 
 int prefill_ws_max_seqs() { return kMaxSeqs; }
 
-cudaError_t launch_paged_prefill_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                                    const PrefillArgs& a, cudaStream_t stream) {
-    const size_t smem = prefill_ws_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int NARROW>
+static cudaError_t launch_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             const PrefillArgs& a, cudaStream_t stream) {
+    const size_t smem = ws_smem_bytes<NARROW>();
+    cudaError_t e = cudaFuncSetAttribute(paged_prefill_ws_kernel<NARROW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // CTAs: one per 2 * 128 / G tokens of each chunk; in the varlen form an upper bound (each chunk adds at
@@ -497,8 +595,18 @@ cudaError_t launch_paged_prefill_ws(const CUtensorMap& qmap, const CUtensorMap& 
     const int grid_x = a.cu_q == nullptr ? (a.NQ + cta_q - 1) / cta_q : a.NQ / cta_q + a.nseq;
     if (grid_x <= 0) return cudaSuccess;
     dim3 grid(grid_x, a.Hkv);
-    paged_prefill_ws_kernel<<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+    paged_prefill_ws_kernel<NARROW><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_paged_prefill_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                    const PrefillArgs& a, int narrow, cudaStream_t stream) {
+    switch (narrow) {
+        case 0: return launch_ws<0>(qmap, kmap, vmap, a, stream);
+        case 1: return launch_ws<1>(qmap, kmap, vmap, a, stream);
+        case 2: return launch_ws<2>(qmap, kmap, vmap, a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pkv

@@ -135,7 +135,7 @@ def test_llama70b_chunk_sampled_rows(name):
 
 # ---------------------------------------------------------------- varlen: several chunks in one launch
 
-def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3):
+def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3, kv="bf16"):
     """chunks: (q_start, n_q) per sequence; sequence s holds q_start + n_q cached tokens in one shared,
     shuffled pool.  Returns host arrays and the per-chunk metadata."""
     rng = np.random.default_rng(seed)
@@ -147,8 +147,8 @@ def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3):
     for s, L in enumerate(kv_lens):
         alloc.add_seq(s, int(L))
     tables = alloc.padded_tables(list(range(len(chunks))))
-    kc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
-    vc = wl.random_values(rng, (NB, S, Hkv, D), "bf16")
+    kc = wl.random_values(rng, (NB, S, Hkv, D), kv)
+    vc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     cu = np.zeros(len(chunks) + 1, np.int32)
     cu[1:] = np.cumsum([nq for _, nq in chunks])
     q = wl.random_values(rng, (int(cu[-1]) + tail_rows, Hq, D), "bf16")
@@ -156,12 +156,12 @@ def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3):
     return q, kc, vc, tables, cu, q_starts, kv_lens
 
 
-def _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale):
+def _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale, k_scale=1.0, v_scale=1.0):
     dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
     out = torch.full_like(dq, float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.pkv_paged_prefill_varlen(out, dq, to_device(cu), to_device(q_starts), to_device(kv_lens), dk, dv,
-                                 B.CacheDesc.for_cache(dk), to_device(tables), scale, err)
+                                 B.CacheDesc.for_cache(dk, k_scale, v_scale), to_device(tables), scale, err)
     torch.cuda.synchronize()
     return out, int(err.item())
 
@@ -185,6 +185,24 @@ def test_prefill_varlen_mixed_batch_matches_oracle(Hq, Hkv, S):
         ref = oracle.paged_prefill_chunk(q[cu[s]:cu[s + 1]], qs, kc, vc, tables[s, :n_tab], int(kv_lens[s]), scale)
         assert_close("bf16", got[cu[s]:cu[s + 1]], ref, f"varlen chunk {s} (q_start={qs}, n_q={nq}) G={Hq // Hkv}")
     assert np.isnan(got[cu[-1]:]).all(), "rows outside every chunk were written"
+
+
+@pytest.mark.parametrize("kv,k_scale,v_scale", [("e4m3", 0.25, 0.5), ("i8", 1 / 32, 1 / 16)])
+def test_prefill_varlen_one_byte_caches(kv, k_scale, v_scale):
+    """The mixed batch over an FP8 or INT8 cache: codes widened on chip, scales on scores and output."""
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case(MIXED, 16, 4, 16, seed=29, kv=kv)
+    scale = 1 / np.sqrt(128)
+    out, err = _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale, k_scale, v_scale)
+    assert err == 0, hex(err)
+    got = to_host(out)
+    cdt = oracle.E4M3 if kv == "e4m3" else oracle.I8
+    for s, (qs, nq) in enumerate(MIXED):
+        if nq == 0:
+            continue
+        n_tab = -(-int(kv_lens[s]) // 16)
+        ref = oracle.paged_prefill_chunk(q[cu[s]:cu[s + 1]], qs, kc, vc, tables[s, :n_tab], int(kv_lens[s]), scale,
+                                         cache_dtype=cdt, k_scale=k_scale, v_scale=v_scale)
+        assert_close(kv, got[cu[s]:cu[s + 1]], ref, f"{kv} varlen chunk {s}")
 
 
 def test_prefill_varlen_one_chunk_equals_chunk_call():
