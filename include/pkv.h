@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef enum {
     PKV_OK = 0,
@@ -76,6 +76,14 @@ typedef struct {
     int32_t dtype;         /* pkv_dtype of the cache elements */
     float k_scale;         /* FP8 / INT8: stored code * k_scale is the key value; 1 otherwise */
     float v_scale;         /* FP8 / INT8: same for values */
+    /* FP8 / INT8, optional: device arrays of num_kv_heads fp32 scales, one per KV head (the
+     * finer granularity of the KV-quantisation discussion in "从 PagedAttention 到 Chunked
+     * Prefill" §5.4 and the KV-cache optimisation overview's technique table).  When set,
+     * KV head h uses k_head_scales[h] / v_head_scales[h] in place of k_scale / v_scale, in
+     * the cache write and in every read.  NULL: the per-tensor scale.  Values must be finite
+     * and positive (device data, not checked: other values give non-finite outputs). */
+    const float* k_head_scales;
+    const float* v_head_scales;
 } pkv_cache_desc;
 
 /*

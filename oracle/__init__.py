@@ -68,7 +68,7 @@ def _load():
         lib.orc_lookup.restype = i32
         lib.orc_lookup.argtypes = [P, i64, i32, ctypes.POINTER(ctypes.c_int)]
         lib.orc_reshape_and_cache.restype = i32
-        lib.orc_reshape_and_cache.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, f32, f32]
+        lib.orc_reshape_and_cache.argtypes = [P, P, i32, P, i32, P, P, i32, i32, i32, i32, i32, f32, f32, P, P]
         lib.orc_copy_blocks.restype = i32
         lib.orc_copy_blocks.argtypes = [P, P, ctypes.c_size_t, i32, P, i32]
         lib.orc_swap_blocks.restype = i32
@@ -78,10 +78,10 @@ def _load():
         lib.orc_block_hashes.restype = None
         lib.orc_block_hashes.argtypes = [P, P, i32, i32, P, P]
         lib.orc_paged_attention_decode.restype = i32
-        lib.orc_paged_attention_decode.argtypes = [P, P, i32, P, P, i32, f64, f64, i32, i32, i32, i32,
+        lib.orc_paged_attention_decode.argtypes = [P, P, i32, P, P, i32, f64, f64, P, P, i32, i32, i32, i32,
                                                    P, i32, P, i32, i32, f64, P, i32, i32]
         lib.orc_paged_prefill_chunk.restype = i32
-        lib.orc_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, i32, f64, f64, i32, i32, i32,
+        lib.orc_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, i32, f64, f64, P, P, i32, i32, i32,
                                                 i32, P, i32, i32, f64, P, i32, i32]
         lib.orc_max_threads.restype = i32
         lib.orc_max_threads.argtypes = []
@@ -160,21 +160,27 @@ def lookup(table: np.ndarray, p: int, block_size: int) -> tuple[int, int]:
 
 # ---------------------------------------------------------------- kernels' definitions
 
+def _head_scales(x, dtype):
+    return None if x is None else np.ascontiguousarray(x, dtype=dtype)
+
+
 def reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache, *, src_dtype=None,
-                      cache_dtype=None, k_scale=1.0, v_scale=1.0):
+                      cache_dtype=None, k_scale=1.0, v_scale=1.0, k_head_scales=None, v_head_scales=None):
     """Write new tokens into host byte images of the caches, in place.
 
     k_new/v_new: [T, Hkv, D] (float32, or uint16 holding bf16 bits);
-    caches: [NB, S, Hkv, D] (float32 / uint16 bf16 / uint8 e4m3).
+    caches: [NB, S, Hkv, D] (float32 / uint16 bf16 / uint8 e4m3 / int8).
+    k_head_scales / v_head_scales: optional fp32 [Hkv], replacing the per-tensor scales per KV head.
     Returns 0, or 2 if some slot was beyond the pool (those tokens skipped)."""
     lib = _load()
     T, Hkv, D = k_new.shape
     NB, S = k_cache.shape[:2]
     assert k_cache.shape == (NB, S, Hkv, D) and v_cache.shape == k_cache.shape
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    khs, vhs = _head_scales(k_head_scales, np.float32), _head_scales(v_head_scales, np.float32)
     st = lib.orc_reshape_and_cache(_ptr(k_new), _ptr(v_new), _dtype_code(k_new, src_dtype), _ptr(sm), T,
                                    _ptr(k_cache), _ptr(v_cache), _dtype_code(k_cache, cache_dtype),
-                                   NB, S, Hkv, D, float(k_scale), float(v_scale))
+                                   NB, S, Hkv, D, float(k_scale), float(v_scale), _ptr(khs), _ptr(vhs))
     return _check(st, "reshape_and_cache", allow=(2,))
 
 
@@ -225,7 +231,7 @@ def block_hashes(tokens, cu_tokens, block_size):
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale, *,
                            q_dtype=None, cache_dtype=None, k_scale=1.0, v_scale=1.0,
-                           seqs=None, threads=0) -> np.ndarray:
+                           k_head_scales=None, v_head_scales=None, seqs=None, threads=0) -> np.ndarray:
     """Textbook fp64 attention of each sequence's query over its paged K/V.
 
     q: [B, Hq, D]; caches [NB, S, Hkv, D]; block_tables [B, MB] int32;
@@ -239,9 +245,11 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
     sel = None if seqs is None else np.ascontiguousarray(seqs, dtype=np.int32)
     n = B if sel is None else sel.shape[0]
     out = np.empty((n, Hq, D), dtype=np.float64)
+    khs, vhs = _head_scales(k_head_scales, np.float64), _head_scales(v_head_scales, np.float64)
     st = lib.orc_paged_attention_decode(_ptr(out), _ptr(q), _dtype_code(q, q_dtype), _ptr(k_cache),
                                         _ptr(v_cache), _dtype_code(k_cache, cache_dtype), float(k_scale),
-                                        float(v_scale), NB, S, Hkv, D, _ptr(bt), bt.shape[1], _ptr(cl), B, Hq,
+                                        float(v_scale), _ptr(khs), _ptr(vhs), NB, S, Hkv, D, _ptr(bt),
+                                        bt.shape[1], _ptr(cl), B, Hq,
                                         float(scale), _ptr(sel), n, int(threads))
     _check(st, "paged_attention_decode")
     return out
@@ -249,7 +257,7 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scal
 
 def paged_prefill_chunk(q, q_start, k_cache, v_cache, block_table, kv_len, scale, *,
                         q_dtype=None, cache_dtype=None, k_scale=1.0, v_scale=1.0,
-                        rows=None, threads=0) -> np.ndarray:
+                        k_head_scales=None, v_head_scales=None, rows=None, threads=0) -> np.ndarray:
     """Causal fp64 attention of a chunk of NQ query tokens (positions
     q_start..q_start+NQ-1) over one sequence's paged K/V.  Returns
     float64 [len(rows) or NQ, Hq, D]."""
@@ -261,9 +269,11 @@ def paged_prefill_chunk(q, q_start, k_cache, v_cache, block_table, kv_len, scale
     sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     n = NQ if sel is None else sel.shape[0]
     out = np.empty((n, Hq, D), dtype=np.float64)
+    khs, vhs = _head_scales(k_head_scales, np.float64), _head_scales(v_head_scales, np.float64)
     st = lib.orc_paged_prefill_chunk(_ptr(out), _ptr(q), _dtype_code(q, q_dtype), NQ, int(q_start),
                                      _ptr(k_cache), _ptr(v_cache), _dtype_code(k_cache, cache_dtype),
-                                     float(k_scale), float(v_scale), NB, S, Hkv, D, _ptr(tb), int(kv_len),
+                                     float(k_scale), float(v_scale), _ptr(khs), _ptr(vhs), NB, S, Hkv, D,
+                                     _ptr(tb), int(kv_len),
                                      Hq, float(scale), _ptr(sel), n, int(threads))
     _check(st, "paged_prefill_chunk")
     return out

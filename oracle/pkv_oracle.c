@@ -41,6 +41,8 @@
  *     the code;
  *   - INT8 is symmetric: code = clamp(RNE(x / scale), -127, 127), value =
  *     code * scale, one fp32 scale per tensor;
+ *   - per-head scales (optional, FP8 and INT8): one fp32 scale per KV head
+ *     replaces the per-tensor scale of that head, in the write and the read;
  *   - bf16 values widen exactly; fp32 -> bf16 is round-to-nearest-even.
  */
 #include <math.h>
@@ -219,13 +221,16 @@ int orc_lookup(const int32_t *table, int64_t p, int S, int *offset)
  * (block, offset) as block * S + offset.  k_new/v_new: [T][Hkv][D] of
  * src_dt; caches: [NB][S][Hkv][D] of cache_dt.  Same dtype: bit copy.
  * bf16 -> f32 widens; f32 -> bf16 rounds to nearest even; -> E4M3 stores
- * sat(RNE(x / scale)) with the division in fp32.
+ * sat(RNE(x / scale)) with the division in fp32, scale being the per-head
+ * scale of the element's KV head when k_head_scales / v_head_scales are
+ * given (NULL: the per-tensor scale).
  * Returns ORC_BAD_SLOT (after writing every valid token) if any slot is
  * beyond the pool. */
 int orc_reshape_and_cache(const void *k_new, const void *v_new, int src_dt,
                           const int64_t *slot, int T, void *k_cache,
                           void *v_cache, int cache_dt, int NB, int S, int Hkv,
-                          int D, float k_scale, float v_scale)
+                          int D, float k_scale, float v_scale,
+                          const float *k_head_scales, const float *v_head_scales)
 {
     if (T < 0 || NB <= 0 || S <= 0 || Hkv <= 0 || D <= 0)
         return ORC_BAD_ARG;
@@ -246,8 +251,9 @@ int orc_reshape_and_cache(const void *k_new, const void *v_new, int src_dt,
         for (int kv = 0; kv < 2; ++kv) {
             const void *src = kv ? v_new : k_new;
             void *dst = kv ? v_cache : k_cache;
-            float scale = kv ? v_scale : k_scale;
+            const float *head_scales = kv ? v_head_scales : k_head_scales;
             for (size_t e = 0; e < row; ++e) {
+                float scale = head_scales ? head_scales[e / (size_t)D] : (kv ? v_scale : k_scale);
                 size_t si = (size_t)i * row + e, di = dst0 + e;
                 if (src_dt == cache_dt) {
                     size_t es = elem_size(src_dt);
@@ -385,8 +391,9 @@ void orc_block_hashes(const int32_t *tokens, const int64_t *cu_tokens, int B, in
 typedef struct {
     const void *k_cache, *v_cache;
     int cache_dt;
-    double k_scale, v_scale; /* 1 unless cache_dt is E4M3 */
+    double k_scale, v_scale; /* 1 unless cache_dt is E4M3 or INT8 */
     int NB, S, Hkv, D;
+    const double *k_head, *v_head; /* per-KV-head scales replacing k_scale / v_scale, or NULL */
 } orc_cache;
 
 /* Gather positions [0, L) of KV head h of one sequence into contiguous
@@ -400,9 +407,11 @@ static int gather(const orc_cache *c, const int32_t *table, int L, int h,
         if (blk < 0 || blk >= c->NB)
             return ORC_BAD_BLOCK;
         size_t base = (((size_t)blk * c->S + (size_t)off) * c->Hkv + (size_t)h) * c->D;
+        double ks = c->k_head ? c->k_head[h] : c->k_scale;
+        double vs = c->v_head ? c->v_head[h] : c->v_scale;
         for (int d = 0; d < c->D; ++d) {
-            K[(size_t)p * c->D + d] = load_elem(c->k_cache, c->cache_dt, base + d, c->k_scale);
-            V[(size_t)p * c->D + d] = load_elem(c->v_cache, c->cache_dt, base + d, c->v_scale);
+            K[(size_t)p * c->D + d] = load_elem(c->k_cache, c->cache_dt, base + d, ks);
+            V[(size_t)p * c->D + d] = load_elem(c->v_cache, c->cache_dt, base + d, vs);
         }
     }
     return ORC_OK;
@@ -449,6 +458,8 @@ static void attend(const double *qv, const double *K, const double *V, int n,
 int orc_paged_attention_decode(double *out, const void *q, int q_dt,
                                const void *k_cache, const void *v_cache,
                                int cache_dt, double k_scale, double v_scale,
+                               const double *k_head_scales,
+                               const double *v_head_scales,
                                int NB, int S, int Hkv, int D,
                                const int32_t *block_tables, int MB,
                                const int32_t *context_lens, int B, int Hq,
@@ -462,7 +473,9 @@ int orc_paged_attention_decode(double *out, const void *q, int q_dt,
     const int G = Hq / Hkv;
     orc_cache c = {k_cache, v_cache, cache_dt,
                    narrow_dt(cache_dt) ? k_scale : 1.0,
-                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D};
+                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D,
+                   narrow_dt(cache_dt) ? k_head_scales : NULL,
+                   narrow_dt(cache_dt) ? v_head_scales : NULL};
     int status = ORC_OK;
     const long nunits = (long)nseqs * Hkv;
 #ifdef _OPENMP
@@ -518,7 +531,8 @@ int orc_paged_attention_decode(double *out, const void *q, int q_dt,
 int orc_paged_prefill_chunk(double *out, const void *q, int q_dt, int NQ,
                             int q_start, const void *k_cache,
                             const void *v_cache, int cache_dt, double k_scale,
-                            double v_scale, int NB, int S, int Hkv, int D,
+                            double v_scale, const double *k_head_scales,
+                            const double *v_head_scales, int NB, int S, int Hkv, int D,
                             const int32_t *table, int kv_len, int Hq,
                             double scale, const int32_t *rows, int nrows,
                             int nthreads)
@@ -531,7 +545,9 @@ int orc_paged_prefill_chunk(double *out, const void *q, int q_dt, int NQ,
     const int G = Hq / Hkv;
     orc_cache c = {k_cache, v_cache, cache_dt,
                    narrow_dt(cache_dt) ? k_scale : 1.0,
-                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D};
+                   narrow_dt(cache_dt) ? v_scale : 1.0, NB, S, Hkv, D,
+                   narrow_dt(cache_dt) ? k_head_scales : NULL,
+                   narrow_dt(cache_dt) ? v_head_scales : NULL};
     int status = ORC_OK;
 #ifdef _OPENMP
     if (nthreads > 0)

@@ -38,12 +38,16 @@ class CacheDesc(ctypes.Structure):
     """Mirror of pkv_cache_desc."""
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
-                ("v_scale", ctypes.c_float)]
+                ("v_scale", ctypes.c_float), ("k_head_scales", ctypes.c_void_p), ("v_head_scales", ctypes.c_void_p)]
 
     @classmethod
-    def for_cache(cls, k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0) -> "CacheDesc":
+    def for_cache(cls, k_cache: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0, k_head_scales=None,
+                  v_head_scales=None) -> "CacheDesc":
+        """Descriptor of a [NB][S][Hkv][D] cache; the optional per-head scales are fp32 device tensors [Hkv]
+        (kept alive by the caller)."""
         NB, S, Hkv, D = k_cache.shape
-        return cls(NB, S, Hkv, D, _DTYPE_CODE[k_cache.dtype], float(k_scale), float(v_scale))
+        return cls(NB, S, Hkv, D, _DTYPE_CODE[k_cache.dtype], float(k_scale), float(v_scale),
+                   _ptr(k_head_scales), _ptr(v_head_scales))
 
 
 _lib = None

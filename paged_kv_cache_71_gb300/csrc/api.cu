@@ -162,6 +162,10 @@ static pkv_status check_cache(const pkv_cache_desc* c) {
     if (narrow(c->dtype) &&
         !(c->k_scale > 0.f && c->v_scale > 0.f && c->k_scale < 3.0e38f && c->v_scale < 3.0e38f))
         return fail(PKV_ERR_INVALID_ARG, "FP8 / INT8 caches need finite positive k_scale / v_scale");
+    if ((c->k_head_scales || c->v_head_scales) && !narrow(c->dtype))
+        return fail(PKV_ERR_INVALID_ARG, "per-head scales apply to FP8 / INT8 caches only");
+    if ((reinterpret_cast<uintptr_t>(c->k_head_scales) | reinterpret_cast<uintptr_t>(c->v_head_scales)) & 3u)
+        return fail(PKV_ERR_INVALID_ARG, "per-head scale arrays must be 4-byte aligned");
     return PKV_OK;
 }
 
@@ -263,7 +267,8 @@ PKV_API pkv_status pkv_reshape_and_cache(const void* k_new, const void* v_new, i
     const int64_t pool_slots = static_cast<int64_t>(cache->num_blocks) * cache->block_size;
     const int row = cache->num_kv_heads * cache->head_dim;
     cudaError_t e = launch_reshape_and_cache(k_new, v_new, src_dtype, slot_mapping, num_tokens, k_cache, v_cache,
-                                             cache->dtype, pool_slots, row, cache->k_scale, cache->v_scale,
+                                             cache->dtype, pool_slots, row, cache->head_dim, cache->k_scale,
+                                             cache->v_scale, cache->k_head_scales, cache->v_head_scales,
                                              device_error, di.sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
     return PKV_OK;
@@ -467,6 +472,9 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     const float kLog2e = 1.4426950408889634f;
     a.q_mul = scale * kLog2e * (narrow(cache->dtype) ? cache->k_scale : 1.f);
     a.o_mul = narrow(cache->dtype) ? cache->v_scale : 1.f;
+    a.q_base = scale * kLog2e;
+    a.k_head = cache->k_head_scales;
+    a.v_head = cache->v_head_scales;
     a.kv_bytes = static_cast<uint32_t>(S * D * kv_es);
     a.q_bytes = static_cast<uint32_t>(G * D * q_es);
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
@@ -562,6 +570,9 @@ PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_d
     a.n_table = (kv_len + S - 1) / S;
     a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
     a.out_mul = fp8 ? cache->v_scale : 1.f;
+    a.sm_base = scale * 1.4426950408889634f;
+    a.k_head = cache->k_head_scales;
+    a.v_head = cache->v_head_scales;
     a.timeout_ns = 2000000000ull;
     const int nk = cache->dtype == PKV_INT8 ? 2 : fp8 ? 1 : 0;
     if (static_cast<size_t>(di.smem_optin) < prefill_ws_smem_bytes(nk))
@@ -631,6 +642,9 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     a.n_table = max_blocks_per_seq;
     a.sm_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
     a.out_mul = fp8 ? cache->v_scale : 1.f;
+    a.sm_base = scale * 1.4426950408889634f;
+    a.k_head = cache->k_head_scales;
+    a.v_head = cache->v_head_scales;
     a.timeout_ns = 2000000000ull;
     a.nseq = num_seqs;
     a.MB = max_blocks_per_seq;

@@ -66,8 +66,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint8_t* _
                                                                 const int64_t* __restrict__ slots, int T,
                                                                 uint8_t* __restrict__ k_cache,
                                                                 uint8_t* __restrict__ v_cache, int64_t pool_slots,
-                                                                int row_elems, float k_scale, float v_scale,
-                                                                int32_t* err) {
+                                                                int row_elems, int head_dim, float k_scale,
+                                                                float v_scale, const float* __restrict__ k_head,
+                                                                const float* __restrict__ v_head, int32_t* err) {
     constexpr int SES = (SRC == PKV_F32) ? 4 : 2;
     constexpr int DES = (DST == PKV_F32) ? 4 : (DST == PKV_BF16) ? 2 : 1;  // FP8 and INT8: one byte
     const int vec_per_row = row_elems / 8;
@@ -86,13 +87,16 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint8_t* _
         }
         const uint8_t* src = (kv ? v_new : k_new) + (static_cast<size_t>(i) * row_elems + vec * 8) * SES;
         uint8_t* dst = (kv ? v_cache : k_cache) + (static_cast<size_t>(slot) * row_elems + vec * 8) * DES;
-        convert8<SRC, DST>(src, dst, kv ? v_scale : k_scale);
+        // per-head scales (when given) replace the per-tensor ones: the 8 elements lie in head (vec * 8) / D
+        const float* hs = kv ? v_head : k_head;
+        convert8<SRC, DST>(src, dst, hs ? __ldg(hs + (vec * 8) / head_dim) : (kv ? v_scale : k_scale));
     }
 }
 
 cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, int src_dtype, const int64_t* slots,
                                      int T, void* k_cache, void* v_cache, int dst_dtype, int64_t pool_slots,
-                                     int row_elems, float k_scale, float v_scale, int32_t* err, int num_sms,
+                                     int row_elems, int head_dim, float k_scale, float v_scale,
+                                     const float* k_head, const float* v_head, int32_t* err, int num_sms,
                                      cudaStream_t stream) {
     const long long total = static_cast<long long>(T) * 2 * (row_elems / 8);
     const int block = 256;
@@ -106,7 +110,8 @@ cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, int s
 #define PKV_RC(S_, D_)                                                                                          \
     if (src_dtype == S_ && dst_dtype == D_) {                                                                   \
         reshape_and_cache_kernel<S_, D_><<<grid, block, 0, stream>>>(kn, vn, slots, T, kc, vc, pool_slots,      \
-                                                                    row_elems, k_scale, v_scale, err);          \
+                                                                    row_elems, head_dim, k_scale, v_scale,      \
+                                                                    k_head, v_head, err);                       \
         return cudaGetLastError();                                                                              \
     }
     PKV_RC(PKV_F32, PKV_F32)

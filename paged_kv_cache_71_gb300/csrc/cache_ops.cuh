@@ -7,7 +7,8 @@ namespace pkv {
 
 cudaError_t launch_reshape_and_cache(const void* k_new, const void* v_new, int src_dtype, const int64_t* slots,
                                      int T, void* k_cache, void* v_cache, int dst_dtype, int64_t pool_slots,
-                                     int row_elems, float k_scale, float v_scale, int32_t* err, int num_sms,
+                                     int row_elems, int head_dim, float k_scale, float v_scale,
+                                     const float* k_head, const float* v_head, int32_t* err, int num_sms,
                                      cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* mapping, int num_pairs, int num_blocks,

@@ -213,6 +213,9 @@ struct DecodeArgs {
     int part_blocks;      // atoms of the work split (>= 1)
     float q_mul;          // scale * log2(e) * k_scale
     float o_mul;          // v_scale
+    float q_base;         // scale * log2(e)
+    const float* k_head;  // per-KV-head scales replacing k_scale / v_scale (nullable)
+    const float* v_head;
     int depth;            // pipeline stages per warp
     uint32_t kv_bytes;    // one K (or V) tile: S * D * es
     uint32_t q_bytes;     // G query rows: G * D * q_es
@@ -569,6 +572,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
             if (first) {
                 seg_first = mc & kMetaFirst;
                 const uint8_t* qs = sp + 2 * a.kv_bytes;
+                const float qm = a.k_head ? a.q_base * __ldg(a.k_head + (ma & 1023)) : a.q_mul;
 #pragma unroll
                 for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -576,8 +580,8 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
 #pragma unroll
                         for (int e = 0; e < EPC; e += 2) {
                             const int d = (c * LPT + lg) * EPC + e;
-                            q2[g][(c * EPC + e) / 2] = make_float2(load_q_elem<QT>(qs, g * D + d) * a.q_mul,
-                                                                   load_q_elem<QT>(qs, g * D + d + 1) * a.q_mul);
+                            q2[g][(c * EPC + e) / 2] = make_float2(load_q_elem<QT>(qs, g * D + d) * qm,
+                                                                   load_q_elem<QT>(qs, g * D + d + 1) * qm);
                             o2[g][(c * EPC + e) / 2] = make_float2(0.f, 0.f);
                         }
                 first = false;
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
             if (tp == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float inv = (l_all[g] > 0.f) ? a.o_mul / l_all[g] : 0.f;
+                    const float inv = (l_all[g] > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / l_all[g] : 0.f;
                     uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
                                     (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
 #pragma unroll
@@ -731,7 +735,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
         if (tp == 0) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float inv = (Ls[g] > 0.f) ? a.o_mul / Ls[g] : 0.f;
+                const float inv = (Ls[g] > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / Ls[g] : 0.f;
                 uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
                                 (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
 #pragma unroll

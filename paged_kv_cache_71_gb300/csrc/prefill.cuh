@@ -17,6 +17,9 @@ struct PrefillArgs {
     const int32_t* kv_lens = nullptr;
     float sm_log2;               // scale * log2(e) (* k_scale for FP8 / INT8 caches)
     float out_mul;               // v_scale for FP8 / INT8 caches, else 1
+    float sm_base = 0.f;         // scale * log2(e)
+    const float* k_head = nullptr;  // per-KV-head scales replacing k_scale / v_scale (nullable)
+    const float* v_head = nullptr;
     uint64_t timeout_ns;
 };
 

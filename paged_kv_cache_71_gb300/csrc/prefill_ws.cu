@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l_run = 0.f;
         int done = 0;
         const bool active = t == 0 || has_b;
+        // score scale (log2 units) and output factor of this KV head: per-head scales when given
+        const float sm_log2 = a.k_head ? a.sm_base * __ldg(a.k_head + h) : a.sm_log2;
+        const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.out_mul;
         bool s_ready = false;  // the next tile's scores were seen complete ahead of time
         for (int j = 0; active && j < n_tiles; ++j) {
             const int tile0 = j * kKeys, b = j & 1;
@@ -467,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float mt = mraw * a.sm_log2;
+            const float mt = mraw * sm_log2;
             const bool need = mt > m_ref + 8.f;
             // O is rescaled (below) only when some row of the warp needs it; rows that do not keep alpha = 1
             const bool rescale = j > 0 && __any_sync(kFull, need);
@@ -475,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float alpha = ex2_approx(m_ref - m_new);
             m_ref = m_new;
             // exponent arguments and running sums on packed fp32 pairs (two elements per instruction)
-            const float2 sc2 = make_float2(a.sm_log2, a.sm_log2), nm2 = make_float2(-m_ref, -m_ref);
+            const float2 sc2 = make_float2(sm_log2, sm_log2), nm2 = make_float2(-m_ref, -m_ref);
             float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[32];
 #pragma unroll
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (active) {
             const bool store = ok && qi < NQ;
-            const float inv = l_run > 0.f ? a.out_mul / l_run : 0.f;
+            const float inv = l_run > 0.f ? out_mul / l_run : 0.f;
             uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
                             (static_cast<size_t>(q_base + qi) * a.Hq + static_cast<size_t>(h) * a.G + r % a.G) * 256;
 #pragma unroll

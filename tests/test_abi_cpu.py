@@ -18,7 +18,7 @@ def test_library_exports_every_declared_entry_point():
 
 
 def test_status_strings_and_version():
-    assert pkv.pkv_abi_version() == 1
+    assert pkv.pkv_abi_version() == 2  # the cache descriptor carries optional per-head scales
     for code, name in B.STATUS_NAMES.items():
         assert pkv.pkv_status_string(code) == name
     assert pkv.pkv_status_string(99) == "PKV_ERR_UNKNOWN"
@@ -33,6 +33,8 @@ def _desc(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(head_dim=96), 2), (dict(block_size=12), 2), (dict(block_size=64), 2), (dict(num_blocks=0), 1),
     (dict(dtype=7), 1), (dict(dtype=B.PKV_FP8_E4M3, k_scale=0.0), 1), (dict(num_kv_heads=-1), 1),
+    (dict(k_head_scales=4096), 1),                           # per-head scales on a bf16 cache
+    (dict(dtype=B.PKV_INT8, v_head_scales=4098), 1),         # misaligned per-head scale array
 ])
 def test_cache_descriptor_checks(kw, status):
     L = pkv.lib()

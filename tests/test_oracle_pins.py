@@ -458,3 +458,59 @@ def test_int8_cache_reads_code_times_scale():
     oracle.reshape_and_cache(kn, kn, np.array([0, 3, 6], np.int64), kq, kq.copy(), k_scale=1 / 32, v_scale=1.0)
     y = (kn / np.float32(1 / 32)).astype(np.float32)
     np.testing.assert_array_equal(kq[0, 0], np.clip(np.rint(y[0]), -127, 127))
+
+
+def test_per_head_scales_write_codes_by_kv_head():
+    """Head h of every token is quantised with its own scale: inputs built as (d + 1) * s_h give codes d + 1 in
+    every head, which a wrong head index (or the per-tensor scale) would not."""
+    Hkv, D, S = 3, 8, 4
+    s_h = np.array([0.5, 0.125, 2.0], np.float32)
+    kn = ((np.arange(D, dtype=np.float32) + 1)[None, None, :] * s_h[None, :, None]).repeat(2, axis=0)
+    vn = -kn
+    kc = np.zeros((2, S, Hkv, D), np.int8)
+    vc = np.zeros_like(kc)
+    oracle.reshape_and_cache(kn, vn, np.array([1, 6], np.int64), kc, vc, k_scale=1.0, v_scale=1.0,
+                             k_head_scales=s_h, v_head_scales=s_h)
+    want = np.arange(1, D + 1, dtype=np.int8)
+    for slot in (1, 6):
+        for h in range(Hkv):
+            np.testing.assert_array_equal(kc[slot // S, slot % S, h], want)
+            np.testing.assert_array_equal(vc[slot // S, slot % S, h], -want)
+    # the E4M3 encoder takes the same per-head division
+    k8 = np.zeros((2, S, Hkv, D), np.uint8)
+    oracle.reshape_and_cache(kn, vn, np.array([1, 6], np.int64), k8, k8.copy(), cache_dtype=oracle.E4M3,
+                             k_scale=1.0, v_scale=1.0, k_head_scales=s_h, v_head_scales=s_h)
+    np.testing.assert_array_equal(oracle.e4m3_to_f64(k8[0, 1, 2]), np.arange(1, D + 1))
+
+
+def test_per_head_scales_decode_closed_form():
+    """Two cached tokens per head: key codes 0 and c, value codes a and b.  With per-head scales ks_h, vs_h the
+    output of head h is vs_h * (a + b * e^z) / (1 + e^z), z = scale * (q . c) * ks_h."""
+    Hkv, G, D, S = 2, 2, 4, 4
+    ks = np.array([0.25, 1.0]); vs = np.array([0.5, 3.0])
+    kc = np.zeros((1, S, Hkv, D), np.int8)
+    vc = np.zeros((1, S, Hkv, D), np.int8)
+    kc[0, 1, :, :] = np.array([1, 2, 0, -1], np.int8)
+    vc[0, 0, :, :] = np.array([4, 0, -2, 1], np.int8)
+    vc[0, 1, :, :] = np.array([-3, 5, 1, 0], np.int8)
+    q = np.tile(np.array([1.0, 0.5, 2.0, -1.0], np.float32), (1, Hkv * G, 1))
+    scale = 0.7
+    out = oracle.paged_attention_decode(q, kc, vc, np.zeros((1, 1), np.int32), np.array([2], np.int32), scale,
+                                        cache_dtype=oracle.I8, k_head_scales=ks, v_head_scales=vs)
+    qc = float(np.dot(q[0, 0].astype(np.float64), kc[0, 1, 0].astype(np.float64)))
+    for h in range(Hkv):
+        z = scale * qc * ks[h]
+        w1 = math.exp(z) / (1 + math.exp(z))
+        want = vs[h] * ((1 - w1) * vc[0, 0, h].astype(np.float64) + w1 * vc[0, 1, h].astype(np.float64))
+        for g in range(G):
+            np.testing.assert_allclose(out[0, h * G + g], want, rtol=1e-13, atol=1e-13)
+    # equal per-head scales reproduce the per-tensor path exactly (decode and prefill)
+    same = oracle.paged_attention_decode(q, kc, vc, np.zeros((1, 1), np.int32), np.array([2], np.int32), scale,
+                                         cache_dtype=oracle.I8, k_scale=0.25, v_scale=0.5,
+                                         k_head_scales=np.full(Hkv, 0.25), v_head_scales=np.full(Hkv, 0.5))
+    tensor = oracle.paged_attention_decode(q, kc, vc, np.zeros((1, 1), np.int32), np.array([2], np.int32), scale,
+                                           cache_dtype=oracle.I8, k_scale=0.25, v_scale=0.5)
+    np.testing.assert_array_equal(same, tensor)
+    pf = oracle.paged_prefill_chunk(q, 1, kc, vc, np.zeros(1, np.int32), 2, scale, cache_dtype=oracle.I8,
+                                    k_head_scales=ks, v_head_scales=vs)
+    np.testing.assert_allclose(pf, out, rtol=1e-13, atol=1e-13)  # the last position sees both tokens
