@@ -213,6 +213,9 @@ def main():
                     help="time only the chunked-prefill kernel on a pool holding just the chunk's sequence")
     ap.add_argument("--swap-only", action="store_true",
                     help="time swap_blocks between the device pool and pinned host memory (Llama-3-8B block geometry)")
+    ap.add_argument("--varlen", action="store_true",
+                    help="the Llama-70B mixed step (48 decode tokens + one 512-token chunk) as one varlen prefill "
+                         "launch, timed beside the decode + chunk kernels")
     ap.add_argument("--hash-only", action="store_true",
                     help="time the chained block content hashes of the Llama-3-8B batch's token ids")
     ap.add_argument("--no-e2e", action="store_true")
@@ -228,6 +231,8 @@ def main():
         return run_reference(args, ws, rank)
     if args.prefill_only:
         return run_prefill_only(args, local)
+    if args.varlen:
+        return run_varlen(args, local)
     if args.swap_only:
         return run_swap_only(args, local)
     if args.hash_only:
@@ -425,6 +430,69 @@ def run_prefill_only(args, local):
                       "us": round(us, 1), "flops": flops, "kv_dtype": kv, "steps": args.steps,
                       "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                                    "unit": "TFLOP/s", "frac": round(tflops / peak, 4)}}), flush=True)
+
+
+def run_varlen(args, local):
+    """The mixed step of the Llama-70B workload (48 decode sequences, one token each, plus the 512-token chunk at
+    positions 8192..8703; 64 q / 8 kv heads, bf16 or FP8 KV) as ONE pkv_paged_prefill_varlen launch, in which a
+    decode token is a chunk of one query.  Timed beside the two-kernel form of the same step (split-KV decode +
+    chunk tile), and the two outputs compared."""
+    import torch
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300 import workload as wl
+    from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
+    torch.cuda.set_device(local)
+    name = args.config if args.config.startswith("llama70b_mixed") else "llama70b_mixed_bf16"
+    kw = {"batch": args.batch} if args.batch else {}
+    w = wl.make(name, **kw)
+    st = DeviceStep(w, num_splits=args.num_splits)
+    st.write()
+    torch.cuda.synchronize()
+    pf = w.prefill
+    B_ = w.num_seqs
+    lens = w.context_lens.astype(np.int64)
+    # chunks: the 48 decode tokens (query at position L-1, L keys) then the prefill chunk
+    cu = np.concatenate([np.arange(B_ + 1), [B_ + pf.q.shape[0]]]).astype(np.int32)
+    q_starts = np.concatenate([lens - 1, [pf.q_start]]).astype(np.int32)
+    kv_lens = np.concatenate([lens, [pf.kv_len]]).astype(np.int32)
+    MB = max(w.block_tables.shape[1], pf.block_table.shape[0])
+    tables = np.full((B_ + 1, MB), -1, np.int32)
+    tables[:B_, : w.block_tables.shape[1]] = w.block_tables
+    tables[B_, : pf.block_table.shape[0]] = pf.block_table
+    q_all = torch.cat([st.q, st.pf_q], dim=0).contiguous()
+    out_all = torch.empty_like(q_all)
+    d_cu, d_qs, d_kv, d_tab = to_device(cu), to_device(q_starts), to_device(kv_lens), to_device(tables)
+
+    def one_launch():
+        B.pkv_paged_prefill_varlen(out_all, q_all, d_cu, d_qs, d_kv, st.k_cache, st.v_cache, st.cache, d_tab,
+                                   w.scale, st.err)
+
+    def two_kernels():
+        st.attend()
+        st.prefill()
+
+    def time_it(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps * 1e3
+
+    us_one = time_it(one_launch)
+    us_two = time_it(two_kernels)
+    if st.device_error():
+        raise RuntimeError(f"device error word {st.device_error():#x}")
+    ref = torch.cat([st.out, st.pf_out], dim=0).float()
+    diff = float((out_all.float() - ref).abs().max())
+    print(json.dumps({"metric": "mixed step (48 decode tokens + 512-token chunk) in one varlen launch",
+                      "value": round(B_ / (us_one * 1e-6), 1), "unit": "seq-steps/s", "us": round(us_one, 1),
+                      "two_kernel_us": round(us_two, 1), "kv_dtype": w.kv_dtype, "steps": args.steps,
+                      "max_abs_diff_vs_two_kernel_path": round(diff, 5), "config": {"workload": name}}), flush=True)
 
 
 def run_swap_only(args, local, nblocks: int = 2048):
