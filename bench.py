@@ -82,6 +82,20 @@ def measured_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "of fallback"
 
 
+# fp32 FMA ceiling of the CUDA-core decode: 152 SMs x 128 fp32 lanes x 2 flops x the 2070 MHz maximum SM clock
+# (GB300's unit counts and clock).  Decode does 2 * G FMAs per cached K/V element (G for q.k, G for p.v).
+GB300_SMS, FP32_LANES_PER_SM, SM_MAX_HZ = 152, 128, 2.07e9
+FP32_FMA_TFLOPS = GB300_SMS * FP32_LANES_PER_SM * 2 * SM_MAX_HZ / 1e12
+
+
+def decode_fma_flops(w) -> int:
+    """fp32 flops of the decode arithmetic: every cached K and V element of every (sequence, KV head) meets the
+    G query heads of its group once (q.k for K, p.v for V): 2 * G flops per element."""
+    G = w.num_q_heads // w.num_kv_heads
+    elems = int(sum(int(L) for L in w.context_lens)) * w.num_kv_heads * w.head_dim * 2
+    return 2 * G * elems
+
+
 DECODE_SOURCES = ("decode.cuh", "pkv_device.cuh", "decode_bf16_s16.cu")
 
 
@@ -346,6 +360,16 @@ def main():
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name), "peak_source": peak_src,
             "kernel": "paged_decode_kernel", "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
+    # the binding ceiling: reading the K/V at the HBM peak needs (flops per byte) x peak of fp32 FMA work; where
+    # that exceeds the CUDA cores' FMA peak (large G, one-byte caches) the kernel is bound by arithmetic instead
+    flops = decode_fma_flops(w)
+    fma_needed = flops / alg * peak * 1e9 / 1e12  # TFLOP/s at the HBM peak
+    if fma_needed > FP32_FMA_TFLOPS:
+        achieved_tf = flops / (dec_avg / 1e3) / 1e12
+        roof.update({"bound": "alu", "achieved": round(achieved_tf, 2), "peak": round(FP32_FMA_TFLOPS, 2),
+                     "unit": "TFLOP/s", "frac": round(achieved_tf / FP32_FMA_TFLOPS, 4),
+                     "peak_source": "fp32 FMA peak from unit counts and clock", "algorithmic_flops": flops,
+                     "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / peak, 4)})
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -44,3 +44,19 @@ def test_prefill_flops_closed_form():
     # sum_{i<512} (8193 + i) = 512 * 8193 + 511 * 512 / 2
     keys = 512 * 8193 + 511 * 256
     assert bench.prefill_flops(W()) == 4 * 128 * 64 * keys == 141742309376
+
+
+def test_decode_ceiling_switches_to_fma_where_arithmetic_binds():
+    """2 * G flops per cached element: the Llama-3-8B batch (G = 4, bf16) needs far less fp32 FMA work than the CUDA
+    cores give when its K/V streams at the HBM peak; the FP8 Llama-70B step (G = 8, one-byte codes) needs more."""
+    import bench
+    from paged_kv_cache_71_gb300 import workload as wl
+    hbm = 6663.6e9
+    for name, alu in (("llama3_8b_gqa", False), ("llama70b_mixed_fp8", True)):
+        w = wl.make(name, batch=8)
+        G = w.num_q_heads // w.num_kv_heads
+        elems = int(w.context_lens.sum()) * w.num_kv_heads * w.head_dim * 2
+        assert bench.decode_fma_flops(w) == 2 * G * elems
+        need = bench.decode_fma_flops(w) / bench.decode_algorithmic_bytes(w) * hbm / 1e12
+        assert (need > bench.FP32_FMA_TFLOPS) == alu
+    assert abs(bench.FP32_FMA_TFLOPS - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
