@@ -31,6 +31,8 @@
 // overtaken; every wait is bounded; on timeout a role records the error and
 // leaves its loop, the CTA drains its own MMAs and copies (bounded) and
 // frees TMEM.
+#include <type_traits>
+
 #include "prefill.cuh"
 
 namespace pkv {
@@ -477,22 +479,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_new = need ? mt : m_ref;
             const float alpha = ex2_approx(m_ref - m_new);
             m_ref = m_new;
-            // exponent arguments and running sums on packed fp32 pairs (two elements per instruction)
+            // exponent arguments and running sums on packed fp32 pairs (two elements per instruction); the
+            // masked form (edge tiles only) is a separate instance so the common path carries no selects
             const float2 sc2 = make_float2(sm_log2, sm_log2), nm2 = make_float2(-m_ref, -m_ref);
             float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             uint32_t pk[32];
+            auto exp_pack = [&](auto with_mask) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), sc2, nm2);
-                float p0 = ex2_approx(x.x);
-                float p1 = ex2_approx(x.y);
-                if (masked) {
-                    p0 = (i < lim) ? p0 : 0.f;
-                    p1 = (i + 1 < lim) ? p1 : 0.f;
+                for (int i = 0; i < 64; i += 2) {
+                    const float2 x = __ffma2_rn(make_float2(v[i], v[i + 1]), sc2, nm2);
+                    float p0 = ex2_approx(x.x);
+                    float p1 = ex2_approx(x.y);
+                    if constexpr (decltype(with_mask)::value) {
+                        p0 = (i < lim) ? p0 : 0.f;
+                        p1 = (i + 1 < lim) ? p1 : 0.f;
+                    }
+                    ls2[(i >> 1) & 1] = __fadd2_rn(ls2[(i >> 1) & 1], make_float2(p0, p1));
+                    pk[i / 2] = bf16x2_rn(p0, p1);
                 }
-                ls2[(i >> 1) & 1] = __fadd2_rn(ls2[(i >> 1) & 1], make_float2(p0, p1));
-                pk[i / 2] = bf16x2_rn(p0, p1);
-            }
+            };
+            if (masked) exp_pack(std::true_type{});
+            else exp_pack(std::false_type{});
             const float2 lsum = __fadd2_rn(ls2[0], ls2[1]);
             l_run = l_run * alpha + (lsum.x + lsum.y);
             tmem_st32u(tS, pk);  // P over the scores just read (this thread's lane only)
