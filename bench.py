@@ -214,6 +214,33 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload_kwargs(config: str, rank: int, batch: int = 0) -> dict:
+    """Arguments of the workload a rank serves: every rank holds its own batch (its own sequences, pool and
+    seed), so sequences shard across GPUs with no exchange in the data path."""
+    from paged_kv_cache_71_gb300 import workload as wl
+    kw = {"seed": wl.CONFIG_SEEDS[config] + 1000 * rank} if config != "llama70b_mixed_fp8" else {}
+    if config == "llama70b_mixed_fp8" and rank:
+        kw["seed"] = wl.CONFIG_SEEDS[config] + 1000 * rank
+    if batch and config in ("llama3_8b_gqa", "llama70b_mixed_bf16", "llama70b_mixed_fp8"):
+        kw["batch"] = batch
+    return kw
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The job's time is its slowest rank's: all-reduce MAX (no-op without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ws: int, seqs_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job seq-steps/s: the sequences all ranks served per step over the slowest rank's step time."""
+    return ws * seqs_per_rank / (ms_per_step / 1e3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -262,10 +289,7 @@ def main():
     from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
 
     # every rank serves its own batch (sequences shard across GPUs; no exchange)
-    kw = {"seed": wl.CONFIG_SEEDS[args.config] + 1000 * rank} if args.config != "llama70b_mixed_fp8" else {}
-    if args.batch and args.config in ("llama3_8b_gqa", "llama70b_mixed_bf16", "llama70b_mixed_fp8"):
-        kw["batch"] = args.batch
-    w = wl.make(args.config, **kw)
+    w = wl.make(args.config, **rank_workload_kwargs(args.config, rank, args.batch))
     st = DeviceStep(w, num_splits=args.num_splits)
     stream = torch.cuda.current_stream()
     launches_per_step = 2 + (1 if st.copy_pairs is not None else 0)
@@ -312,12 +336,9 @@ def main():
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     prefill_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)] if has_prefill else None
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
-    value = ws * w.num_seqs / (ms_per_step / 1e3)
+    value = job_throughput(ws, w.num_seqs, ms_per_step)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -345,12 +366,8 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / args.steps
-        if dist:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": ws * w.num_seqs / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist, "cuda")
+        e2e = {"value": job_throughput(ws, w.num_seqs, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
     peak, peak_src = measured_peaks()
