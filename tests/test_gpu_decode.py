@@ -191,3 +191,39 @@ def test_full_size_batches_sampled(name):
     st1 = _run(w, 1)
     o1 = to_host(st1.out)
     assert np.abs(o1 - out).max() < (6e-2 if w.kv_dtype == "e4m3" else 3e-2)
+
+
+def test_largest_batch_and_one_more_is_rejected():
+    """num_seqs = 8192 (the largest batch one call takes) with short ragged contexts; 8193 is refused on the host."""
+    rng = np.random.default_rng(8192)
+    lens = rng.integers(1, 40, size=8192)
+    w = _random_workload(lens, 8, 2, 64, 8, "bf16", "bf16", seed=81)
+    st = _run(w)
+    assert st.device_error() == 0
+    seqs = [0, 1, 4095, 8190, 8191]
+    kc, vc, ref = oracle_step(w, seqs=seqs)
+    assert_close("bf16", to_host(st.out)[seqs], ref, "8192 sequences, sampled")
+    q = torch.zeros((8193, 8, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.pkv_paged_attention_decode(torch.empty_like(q), q, st.k_cache, st.v_cache, st.cache,
+                                       torch.zeros((8193, 1), dtype=torch.int32, device="cuda"),
+                                       torch.ones(8193, dtype=torch.int32, device="cuda"), 0.1, num_splits=1)
+    assert ei.value.status == 2
+
+
+def test_one_very_long_sequence_splits():
+    """A single 131072-token sequence (8192 blocks): the split-KV plan spreads it over every SM and merges."""
+    w = _random_workload([131072], 8, 2, 128, 16, "bf16", "bf16", seed=131)
+    kc, vc, ref = oracle_step(w)
+    for ns in (0, 1, 64):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        assert_close("bf16", to_host(st.out), ref, f"131072-token sequence, splits={ns}")
+
+
+def test_unsupported_group_is_refused():
+    w = _random_workload([20, 7], 32, 2, 128, 16, "bf16", "bf16", seed=16)  # G = 16
+    with pytest.raises(pkv.PkvError) as ei:
+        st = DeviceStep(w, num_splits=1)
+        st.attend()
+    assert ei.value.status == 2

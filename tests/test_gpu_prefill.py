@@ -257,3 +257,17 @@ def test_prefill_varlen_host_checks():
         pkv.pkv_paged_prefill_varlen(out, dq, to_device(cu), to_device(q_starts), to_device(kv_lens), dk, dv, d,
                                      to_device(tables), -1.0)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("NQ,q_start,Hq,Hkv,S", [
+    (19, 60, 32, 2, 16),      # G = 16: 8 tokens per 128-row query tile
+    (11, 200, 64, 2, 8),      # G = 32: 4 tokens per tile
+    (1, 0, 8, 1, 16),         # one query at position 0 (a single key)
+    (1, 5000, 16, 2, 32),     # one query deep into the sequence (a decode-like chunk)
+])
+def test_prefill_chunk_edge_shapes(NQ, q_start, Hq, Hkv, S):
+    q, kc, vc, table, kv_len = _chunk_case(NQ, q_start, Hq, Hkv, S, seed=3 * NQ + q_start)
+    scale = 1 / np.sqrt(128)
+    ref = oracle.paged_prefill_chunk(q, q_start, kc, vc, table, kv_len, scale)
+    got = _run(q, kc, vc, table, q_start, kv_len, scale)
+    assert_close("bf16", got, ref, f"prefill NQ={NQ} q_start={q_start} G={Hq // Hkv} S={S}")
