@@ -16,7 +16,10 @@
 //   * warps 8 and 10 (producers) copy Q once and the K tiles (warp 8) and the
 //     V tiles (warp 10) with TMA (128-byte swizzle, one block of the block
 //     table per copy, one lane per block) into two 4-deep rings; block-table
-//     entries are read 32 at a time, a batch ahead;
+//     entries are read 32 at a time, a batch ahead.  For FP8 / INT8 caches
+//     the codes go to a two-slot staging ring per operand and are widened to
+//     bf16 into a 3-deep ring, half the rows by the producer and half by the
+//     MMA warp that consumes the operand;
 //   * warps 9 and 11 issue the tcgen05 MMAs (each warp runs its loop, one
 //     elected lane issues): warp 9 S_A(j), S_B(j) into the buffers that
 //     P(j-2) was read from, as soon as P(j-2).V has completed; warp 11
@@ -76,7 +79,8 @@ constexpr int kBarQFull = kBarPVDone + 4;
 constexpr int kBarFinal = kBarQFull + 1;          // every MMA done
 constexpr int kBarDrain = kBarFinal + 1;          // after an abort: every MMA issued so far done
 constexpr int kBarStg = kBarDrain + 1;            // + 2 * (V ? 1 : 0) + slot: one-byte codes landed in staging
-constexpr int kNumBars = kBarStg + 4;
+constexpr int kBarStgFree = kBarStg + 4;          // + 2 * (V ? 1 : 0) + slot: the MMA warp's half of it widened
+constexpr int kNumBars = kBarStgFree + 4;
 constexpr int kMetaTmem = 8 * kNumBars;           // TMEM base address
 constexpr int kMetaAbort = kMetaTmem + 4;
 constexpr int kMetaTile = kMetaAbort + 4;         // chunk, first token (or -1)
@@ -211,8 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int blocks_per_tile = kKeys / a.S;
 
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i)
-            mbar_init(bar + 8 * i, (i >= kBarPFull && i < kBarPFull + 4) ? kSoftmax / 2 : i == kBarDrain ? 2 : 1);
+        // the bf16 instance never waits on the staging-free barriers
+        for (int i = 0; i < (NARROW ? kNumBars : kBarStgFree); ++i) {
+            int count = (i >= kBarPFull && i < kBarPFull + 4) ? kSoftmax / 2 : i == kBarDrain ? 2 : 1;
+            // one-byte caches: a bf16 K or V stage is complete when both warps widened their halves
+            if (NARROW && ((i >= kBarKFull && i < kBarKFull + kMaxStages) || (i >= kBarVFull && i < kBarVFull + kMaxStages)))
+                count = 2;
+            mbar_init(bar + 8 * i, count);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -224,6 +234,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // One-byte caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into bf16 stage st
+    // (exact: every E4M3 and INT8 code is a bf16 value; the per-tensor or per-head scales go to the scores and the
+    // output).  128 codes per key row, in 128-byte swizzled lines like the bf16 halves.  Each of the two warps
+    // that serve an operand (its producer and its MMA warp) widens one half of the rows.
+    auto widen_rows = [&](bool is_v, int slot, int st, int rr) {
+        const uint8_t* src = smem + kOffStg + ((is_v ? 2 : 0) + slot) * kStgSlot;
+        uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * 2 * kKvHalf;
+        const int r = lane + 32 * rr, sw = r & 7;
+        src += r * 128;
+        uint8_t* dst = dstb + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16 codes: head dims 16c .. 16c + 15
+            const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ sw) * 16));
+            const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float2 f0, f1;
+                if constexpr (NARROW == 2) {
+                    f0 = s8x2_to_float2(ws[i], 0);
+                    f1 = s8x2_to_float2(ws[i], 2);
+                } else {
+                    f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                    f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                }
+                o[2 * i] = bf16x2_rn(f0.x, f0.y);
+                o[2 * i + 1] = bf16x2_rn(f1.x, f1.y);
+            }
+            uint8_t* dh = dst + (c >> 2) * kKvHalf;
+            const int lc = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(dh + ((lc ^ sw) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dh + (((lc + 1) ^ sw) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    };
 
     if (warp == 8 || warp == 10) {
         // ------------------------------------------------ producer warps: warp 8 copies Q and the K tiles,
@@ -288,10 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = j + 1;
             }
         } else {
-            // one-byte codes: copy tile j+1 into its staging slot, then widen tile j into the bf16 ring
-            // (exact: every E4M3 and INT8 code is a bf16 value; the per-tensor scales go to the scores and
-            // the output).  128 codes per key row, rows in 128-byte swizzled lines like the bf16 halves.
-            const int sbar = kBarStg + (is_v ? 2 : 0);
+            // one-byte codes: copy tile j+1 into its staging slot (once the MMA warp has widened its half of tile
+            // j-1 from there), then widen the first half of the rows of tile j into the bf16 ring
+            const int sbar = kBarStg + (is_v ? 2 : 0), fbar = kBarStgFree + (is_v ? 2 : 0);
             const uint32_t stg0 = sb + kOffStg + (is_v ? 2 : 0) * kStgSlot;
             auto stage = [&](int jj, int row) {
                 const uint32_t fb = bar + 8 * (sbar + (jj & 1));
@@ -300,44 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane < blocks_per_tile)
                     tma_load_3d_nohint(stg0 + (jj & 1) * kStgSlot + lane * a.S * 128, map, 0, h, row, fb);
             };
-            auto widen = [&](int slot, int st) {
-                const uint8_t* src0 = smem + kOffStg + ((is_v ? 2 : 0) + slot) * kStgSlot;
-                uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * 2 * kKvHalf;
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int r = lane + 32 * rr, sw = r & 7;
-                    const uint8_t* src = src0 + r * 128;
-                    uint8_t* dst = dstb + r * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {  // 16 codes: head dims 16c .. 16c + 15
-                        const uint4 wv = *reinterpret_cast<const uint4*>(src + ((c ^ sw) * 16));
-                        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-                        uint32_t o[8];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            float2 f0, f1;
-                            if constexpr (NARROW == 2) {
-                                f0 = s8x2_to_float2(ws[i], 0);
-                                f1 = s8x2_to_float2(ws[i], 2);
-                            } else {
-                                f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
-                                f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
-                            }
-                            o[2 * i] = bf16x2_rn(f0.x, f0.y);
-                            o[2 * i + 1] = bf16x2_rn(f1.x, f1.y);
-                        }
-                        uint8_t* dh = dst + (c >> 2) * kKvHalf;
-                        const int lc = 2 * (c & 3);
-                        *reinterpret_cast<uint4*>(dh + ((lc ^ sw) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4*>(dh + (((lc + 1) ^ sw) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                }
-            };
             stage(0, tile_row(0));
             staged = 1;
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kStages;
-                if (j + 1 < n_tiles) {  // its slot was widened at j - 1 (and fenced): free for the copy
+                if (j + 1 < n_tiles) {
+                    // slot (j+1) & 1 last held tile j-1: this warp widened its half at j-1 (and fenced)
+                    if (j >= 1 && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (fbar + ((j - 1) & 1)),
+                                                                      ((j - 1) >> 1) & 1, a.timeout_ns))) {
+                        if (lane == 0) *abort_flag = 1;
+                        break;
+                    }
                     stage(j + 1, tile_row(j + 1));
                     staged = j + 2;
                 }
@@ -348,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 widened = j + 1;
                 if (__any_sync(kFull, *abort_flag != 0)) break;
-                widen(j & 1, st);
+                widen_rows(is_v, j & 1, st, 0);
                 fence_proxy_async_smem();  // the MMA (async proxy) reads what was written; the next copy overwrites
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar + 8 * (full + st));
@@ -370,6 +387,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t d_kmaj = smem_desc_sw128(sb, 16, 1024);       // Q and K: K-major rows of 128 B
         const uint64_t d_v = smem_desc_sw128(sb, kKvHalf, 1024);     // V: N-major, d-halves kKvHalf apart
         bool ok = true;
+        // one-byte caches: this warp widens the second half of the rows of key tile jj of its operand (K for the
+        // S warp, V for the P.V warp) once its codes landed and its bf16 stage is free, then frees the staging slot
+        auto widen_half = [&](bool is_v, int jj) -> bool {
+            const int full = is_v ? kBarVFull : kBarKFull, empty = is_v ? kBarVEmpty : kBarKEmpty;
+            const int stg = kBarStg + (is_v ? 2 : 0), stf = kBarStgFree + (is_v ? 2 : 0);
+            const int st = jj % kStages;
+            if (!__all_sync(kFull, mbar_spin_bounded(bar + 8 * (stg + (jj & 1)), (jj >> 1) & 1, a.timeout_ns)))
+                return false;
+            if (jj >= kStages && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (empty + st), (jj / kStages - 1) & 1,
+                                                                      a.timeout_ns)))
+                return false;
+            widen_rows(is_v, jj & 1, st, 1);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar + 8 * (full + st));
+                mbar_arrive(bar + 8 * (stf + (jj & 1)));
+            }
+            return true;
+        };
         if (warp == 9) {
             // S(j) of both query tiles into buffer j & 1, which P(j-2) was read from
             auto issue_s = [&](int t, int j) {
@@ -385,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_warp(bar + 8 * (kBarSFull + 2 * t + (j & 1)));
             };
             const uint32_t qb = bar + 8 * kBarQFull;
+            if constexpr (NARROW != 0) ok = widen_half(false, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const uint32_t kb = bar + 8 * (kBarKFull + j % kStages), kph = (j / kStages) & 1;
                 for (int t = 0; t < (has_b ? 2 : 1); ++t) {
@@ -398,6 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 tc_commit_warp(bar + 8 * (kBarKEmpty + j % kStages));
+                // the next tile's half of K, while the tensor pipe works on S(j)
+                if constexpr (NARROW != 0) {
+                    if (j + 1 < n_tiles) ok = widen_half(false, j + 1);
+                }
             }
         } else {
             // P(j).V(j) of both query tiles once their softmax is done
@@ -410,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
                 tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
             };
+            if constexpr (NARROW != 0) ok = widen_half(true, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kStages, b = j & 1;
                 const uint32_t ph = (j >> 1) & 1, vb = bar + 8 * (kBarVFull + st), vph = (j / kStages) & 1;
@@ -423,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 tc_commit_warp(bar + 8 * (kBarVEmpty + st));
+                // the next tile's half of V, while the tensor pipe works on P(j).V
+                if constexpr (NARROW != 0) {
+                    if (j + 1 < n_tiles) ok = widen_half(true, j + 1);
+                }
             }
             // the last P.V follows every S MMA (it needed that tile's softmax), so this covers all MMAs
             if (ok) tc_commit_warp(bar + 8 * kBarFinal);
