@@ -194,6 +194,9 @@ struct DecodeShape {
     static constexpr int NCH = RB / CH;                              // chunks per lane and row
     static constexpr int EPC = CH / KV::es;                          // elements per chunk
     static constexpr int DUP = LPT / G;                              // lanes holding the same score
+    // select-free score reduction (heads XOR-permuted per lane): measured 7% faster for G = 8, while the
+    // HBM-bound G <= 4 instances ran 1-2% slower with it
+    static constexpr bool XPERM = G >= 8;
     static_assert(LPT <= 32 && G <= LPT, "lane mapping");
     static_assert(EPC % 2 == 0 && DPL % 2 == 0, "pairs");
     static_assert(DPL == NCH * EPC, "chunking");
@@ -262,9 +265,13 @@ struct WorkSplit {
     }
 };
 
-// Reduce-scatter of V[0..N) over the lanes of an aligned LPT-lane group:
-// afterwards each lane holds the full sum for index lg / (LPT / G).
-template <int N, int OFF>
+// Reduce-scatter of V[0..N) over the lanes of an aligned LPT-lane group, afterwards each lane holding the full
+// sum for head gl = lg / (LPT / G).
+//   XPERM: the lanes keep their heads in XOR-permuted order, slot i of a lane holding head i ^ gl.  At every
+//   halving step both partners then keep slots [0, N/2) and send slots [N/2, N) (the upper half of a lane's slots
+//   is exactly the half of the heads its partner keeps), so no lane-dependent select is needed.
+//   Otherwise slot i holds head i and the upper partner of each step swaps halves with two selects per value.
+template <int N, int OFF, bool XPERM>
 __device__ __forceinline__ float reduce_scatter(float* v, int lane) {
     if constexpr (OFF == 0) {
         return v[0];
@@ -272,14 +279,18 @@ __device__ __forceinline__ float reduce_scatter(float* v, int lane) {
         const bool upper = (lane & OFF) != 0;
 #pragma unroll
         for (int i = 0; i < N / 2; ++i) {
-            const float send = upper ? v[i] : v[i + N / 2];
-            const float keep = upper ? v[i + N / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, OFF);
+            if constexpr (XPERM) {
+                v[i] += __shfl_xor_sync(kFull, v[i + N / 2], OFF);
+            } else {
+                const float send = upper ? v[i] : v[i + N / 2];
+                const float keep = upper ? v[i + N / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(kFull, send, OFF);
+            }
         }
-        return reduce_scatter<N / 2, OFF / 2>(v, lane);
+        return reduce_scatter<N / 2, OFF / 2, XPERM>(v, lane);
     } else {
         v[0] += __shfl_xor_sync(kFull, v[0], OFF);
-        return reduce_scatter<1, OFF / 2>(v, lane);
+        return reduce_scatter<1, OFF / 2, XPERM>(v, lane);
     }
 }
 
@@ -501,7 +512,7 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                         float v[G];
 #pragma unroll
                         for (int g = 0; g < G; ++g) v[g] = acc[g].x + acc[g].y;
-                        const float sc = reduce_scatter<G, LPT / 2>(v, lane);
+                        const float sc = reduce_scatter<G, LPT / 2, SH::XPERM>(v, lane);
                         sr[r] = (!M || t < tv) ? sc : -INFINITY;
                     }
                     // ---- tile max over all tokens (butterfly over the token groups)
@@ -580,8 +591,10 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
 #pragma unroll
                         for (int e = 0; e < EPC; e += 2) {
                             const int d = (c * LPT + lg) * EPC + e;
-                            q2[g][(c * EPC + e) / 2] = make_float2(load_q_elem<QT>(qs, g * D + d) * qm,
-                                                                   load_q_elem<QT>(qs, g * D + d + 1) * qm);
+                            // with XPERM slot g holds head g ^ gl (the order the reduce-scatter of the scores expects)
+                            const int hq = (SH::XPERM ? (g ^ gl) : g) * D + d;
+                            q2[g][(c * EPC + e) / 2] = make_float2(load_q_elem<QT>(qs, hq) * qm,
+                                                                   load_q_elem<QT>(qs, hq + 1) * qm);
                             o2[g][(c * EPC + e) / 2] = make_float2(0.f, 0.f);
                         }
                 first = false;
