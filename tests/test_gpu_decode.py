@@ -221,6 +221,27 @@ def test_one_very_long_sequence_splits():
         assert_close("bf16", to_host(st.out), ref, f"131072-token sequence, splits={ns}")
 
 
+@pytest.mark.parametrize("G", [4, 8])
+def test_int8_long_sequence_of_small_codes(G):
+    """One 32768-token INT8 sequence reduced by one worker and by the split plan: small codes in [-3, 3] with
+    unit scales, then only the extreme codes -127 and 127, stay within the INT8 tolerance."""
+    for lo, hi, seed in ((-3, 3, 90 + G), (-127, 127, 95 + G)):
+        w = _random_workload([32768, 3, 40], 2 * G, 2, 128, 16, "i8", "bf16", seed=seed)
+        rng = np.random.default_rng(seed)
+        if hi == 3:
+            w.k_cache = rng.integers(lo, hi + 1, w.k_cache.shape).astype(np.int8)
+            w.v_cache = rng.integers(lo, hi + 1, w.v_cache.shape).astype(np.int8)
+        else:
+            w.k_cache = rng.choice(np.array([lo, hi], np.int8), w.k_cache.shape)
+            w.v_cache = rng.choice(np.array([lo, hi], np.int8), w.v_cache.shape)
+        w.k_scale = w.v_scale = 1.0 / 16 if hi == 127 else 1.0
+        _, _, ref = oracle_step(w)
+        for ns in (1, 0):
+            st = _run(w, ns)
+            assert st.device_error() == 0
+            assert_close("i8", to_host(st.out), ref, f"INT8 codes in [{lo}, {hi}], G={G}, splits={ns}")
+
+
 def test_unsupported_group_is_refused():
     w = _random_workload([20, 7], 32, 2, 128, 16, "bf16", "bf16", seed=16)  # G = 16
     with pytest.raises(pkv.PkvError) as ei:
