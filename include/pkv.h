@@ -66,6 +66,8 @@ typedef enum {
 #define PKV_DEVERR_BAD_BLOCK 0x2    /* block id < 0 or >= num_blocks where one must be read */
 #define PKV_DEVERR_BAD_LENGTH 0x4   /* context_len < 0 or > max_blocks_per_seq * block_size */
 #define PKV_DEVERR_TIMEOUT 0x8      /* a bounded wait on an async copy gave up */
+#define PKV_DEVERR_Q_RANGE 0x10     /* a query value beyond the f16 range (|q| >= 65520) in a prefill over an
+                                       FP8 or INT8 cache, whose tensor-core products run on f16 operands */
 
 /* Description of one layer's K and V cache pools. */
 typedef struct {
@@ -169,8 +171,10 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
  * with K/V gathered through block_table (one sequence, ceil(kv_len / S)
  * entries).  Runs on the tensor cores: bf16 inputs, fp32 accumulation, the
  * softmax weights rounded to bf16 for the P.V product.  An FP8 or INT8 cache
- * is widened to bf16 on chip (exactly) and its per-tensor scales are applied
- * to the scores and the output.
+ * is widened to f16 on chip (exactly), the queries are taken to f16 (exact for
+ * |q| in [2^-14, 65504]; a value of 65520 or more sets PKV_DEVERR_Q_RANGE), the
+ * softmax weights are rounded to f16, and the per-tensor or per-head scales
+ * are applied to the scores and the output.
  *   q, out: [num_q_tokens][num_q_heads][128] bf16.
  * scale must be positive.
  * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
@@ -200,8 +204,9 @@ pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, in
  * total_q_tokens, kv_len too short, more table entries than max_blocks_per_seq)
  * sets PKV_DEVERR_BAD_LENGTH and leaves that chunk's rows unwritten; a table
  * entry outside the pool sets PKV_DEVERR_BAD_BLOCK.
- * An FP8 or INT8 cache is widened to bf16 on chip (exactly), its per-tensor
- * scales applied to the scores and the output, as in pkv_paged_prefill_chunk.
+ * An FP8 or INT8 cache is widened to f16 on chip (exactly), with f16 queries
+ * and softmax weights and its scales applied to the scores and the output, as
+ * in pkv_paged_prefill_chunk.
  * scale must be positive.
  * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
  *   G dividing 128, num_seqs <= 2048.  No workspace.

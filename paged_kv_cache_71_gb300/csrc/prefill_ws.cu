@@ -18,8 +18,9 @@
 //     table per copy, one lane per block) into two 4-deep rings; block-table
 //     entries are read 32 at a time, a batch ahead.  For FP8 / INT8 caches
 //     the codes go to a two-slot staging ring per operand and are widened to
-//     bf16 into a 3-deep ring, half the rows by the producer and half by the
-//     MMA warp that consumes the operand;
+//     f16 into a 3-deep ring, half the rows by the producer and half by the
+//     MMA warp that consumes the operand; the MMAs of those caches run on f16
+//     operands (Q converted in place once, P packed as f16);
 //   * warps 9 and 11 issue the tcgen05 MMAs (each warp runs its loop, one
 //     elected lane issues): warp 9 S_A(j), S_B(j) into the buffers that
 //     P(j-2) was read from, as soon as P(j-2).V has completed; warp 11
@@ -49,7 +50,7 @@ constexpr int kStgSlot = kKeys * 128;          // one key tile of one-byte codes
 constexpr int kOffQ = 0;                       // tile A: 2 halves, tile B: 2 halves
 
 // Shared-memory plan per cache kind (NARROW: 0 bf16, 1 FP8 E4M3 codes, 2 INT8 codes).  One-byte caches
-// land in a two-slot staging ring per operand and are widened to bf16 by the producer warps.
+// land in a two-slot staging ring per operand and are widened to f16 by the producer and MMA warps.
 template <int NARROW>
 struct Plan {
     static constexpr int kStages = NARROW ? 3 : 4;                  // bf16 K and V ring depth
@@ -64,8 +65,18 @@ constexpr int kColS = 0;     // + 128 * tile + 64 * buffer: scores (fp32, 64 key
 constexpr int kColO = 256;   // + 128 * tile: output accumulator (fp32, 128 dims)
 constexpr int kSoftmax = 256;
 constexpr int kThreads = 384;  // + producer warps 8 (K) and 10 (V), MMA warps 9 (S) and 11 (P.V)
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, kKeys, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, true);
+// Instruction descriptor for kind::f16 with f16 A and B (bits 7-9 = 0, 10-12 = 0; bf16 sets both to 1), fp32
+// accumulator, A K-major, B K- or MN-major (bit 16), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+// MMA operand types: bf16 for bf16 caches; f16 for one-byte caches (their codes widen to f16 in one step, and Q
+// and P are taken to f16 to match)
+template <int NARROW>
+constexpr uint32_t kIdescS = NARROW ? idesc_f16_f32(128, kKeys, false) : idesc_bf16_f32(128, kKeys, false);
+template <int NARROW>
+constexpr uint32_t kIdescPV = NARROW ? idesc_f16_f32(128, 128, true) : idesc_bf16_f32(128, 128, true);
 
 // mbarrier slots (8 bytes each); "tb" = 2 * tile + buffer
 constexpr int kBarKFull = 0;                         // + stage: K in the bf16 ring (copies landed / widened)
@@ -80,7 +91,8 @@ constexpr int kBarFinal = kBarQFull + 1;          // every MMA done
 constexpr int kBarDrain = kBarFinal + 1;          // after an abort: every MMA issued so far done
 constexpr int kBarStg = kBarDrain + 1;            // + 2 * (V ? 1 : 0) + slot: one-byte codes landed in staging
 constexpr int kBarStgFree = kBarStg + 4;          // + 2 * (V ? 1 : 0) + slot: the MMA warp's half of it widened
-constexpr int kNumBars = kBarStgFree + 4;
+constexpr int kBarQConv = kBarStgFree + 4;        // one-byte caches: Q converted to f16 (8 softmax warps)
+constexpr int kNumBars = kBarQConv + 1;
 constexpr int kMetaTmem = 8 * kNumBars;           // TMEM base address
 constexpr int kMetaAbort = kMetaTmem + 4;
 constexpr int kMetaTile = kMetaAbort + 4;         // chunk, first token (or -1)
@@ -108,6 +120,29 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two E4M3 codes (low byte first) -> f16x2, exactly (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t w) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(w));
+    return r;
+}
+
+// Signed bytes i0, i0 + 1 of w -> f16x2, exactly.  f = w ^ 0x80808080 holds u = byte + 128; u placed in the low
+// mantissa bits of 0x6400 (1024) reads 1024 + u, and one packed subtraction of 1152 leaves the byte's value.
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint32_t f, int i0) {
+    const uint32_t h = __byte_perm(f, 0x64646464u, 0x5040u | (static_cast<uint32_t>(i0 + 1) << 8) |
+                                                        static_cast<uint32_t>(i0));
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
     return r;
 }
 
@@ -218,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the bf16 instance never waits on the staging-free barriers
         for (int i = 0; i < (NARROW ? kNumBars : kBarStgFree); ++i) {
             int count = (i >= kBarPFull && i < kBarPFull + 4) ? kSoftmax / 2 : i == kBarDrain ? 2 : 1;
+            if (i == kBarQConv) count = kSoftmax / 32;
             // one-byte caches: a bf16 K or V stage is complete when both warps widened their halves
             if (NARROW && ((i >= kBarKFull && i < kBarKFull + kMaxStages) || (i >= kBarVFull && i < kBarVFull + kMaxStages)))
                 count = 2;
@@ -235,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // One-byte caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into bf16 stage st
-    // (exact: every E4M3 and INT8 code is a bf16 value; the per-tensor or per-head scales go to the scores and the
+    // One-byte caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into f16 stage st
+    // (exact: every E4M3 and INT8 code is an f16 value; the per-tensor or per-head scales go to the scores and the
     // output).  128 codes per key row, in 128-byte swizzled lines like the bf16 halves.  Each of the two warps
     // that serve an operand (its producer and its MMA warp) widens one half of the rows.
     auto widen_rows = [&](bool is_v, int slot, int st, int rr) {
@@ -252,16 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                float2 f0, f1;
                 if constexpr (NARROW == 2) {
-                    f0 = s8x2_to_float2(ws[i], 0);
-                    f1 = s8x2_to_float2(ws[i], 2);
+                    const uint32_t f = ws[i] ^ 0x80808080u;
+                    o[2 * i] = s8x2_to_f16x2(f, 0);
+                    o[2 * i + 1] = s8x2_to_f16x2(f, 2);
                 } else {
-                    f0 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] & 0xffffu));
-                    f1 = e4m3x2_to_float2(static_cast<uint16_t>(ws[i] >> 16));
+                    o[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] & 0xffffu));
+                    o[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] >> 16));
                 }
-                o[2 * i] = bf16x2_rn(f0.x, f0.y);
-                o[2 * i + 1] = bf16x2_rn(f1.x, f1.y);
             }
             uint8_t* dh = dst + (c >> 2) * kKvHalf;
             const int lc = 2 * (c & 3);
@@ -417,11 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off_a = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
                     const uint32_t off_b = ((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4;
-                    tc_mma_f16_warp(d, a0 + off_a, b0 + off_b, kIdescS, kk > 0);
+                    tc_mma_f16_warp(d, a0 + off_a, b0 + off_b, kIdescS<NARROW>, kk > 0);
                 }
                 tc_commit_warp(bar + 8 * (kBarSFull + 2 * t + (j & 1)));
             };
-            const uint32_t qb = bar + 8 * kBarQFull;
+            // Q landed (bf16 caches) or converted to f16 by the softmax warps (one-byte caches)
+            const uint32_t qb = bar + 8 * (NARROW ? kBarQConv : kBarQFull);
             if constexpr (NARROW != 0) ok = widen_half(false, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const uint32_t kb = bar + 8 * (kBarKFull + j % kStages), kph = (j / kStages) & 1;
@@ -449,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acc0 = j > 0;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+                    tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV<NARROW>, kk > 0 ? 1u : acc0);
                 tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
             };
             if constexpr (NARROW != 0) ok = widen_half(true, 0);
@@ -491,6 +526,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sm_log2 = a.k_head ? a.sm_base * __ldg(a.k_head + h) : a.sm_log2;
         const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.out_mul;
         bool s_ready = false;  // the next tile's scores were seen complete ahead of time
+        if constexpr (NARROW != 0) {
+            // one-byte caches: the MMAs run on f16 operands, so Q (bf16, landed by TMA) is converted in place, each
+            // query tile by its own four warps; exact for |q| in [2^-14, 65504], larger values raise Q_RANGE
+            bool ok_q = !active || __all_sync(kFull, mbar_spin_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns));
+            if (!ok_q) *abort_flag = 1;
+            if (active && ok_q) {
+                uint8_t* qt = smem + kOffQ + 2 * t * kQHalf;
+                bool in_range = true;
+                for (int i = quad * 32 + lane; i < 2 * kQHalf / 16; i += kSoftmax / 2) {
+                    uint4 w = *reinterpret_cast<const uint4*>(qt + i * 16);
+                    uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f = bf16x2_to_float2(ws[k]);
+                        in_range = in_range && fabsf(f.x) < 65520.f && fabsf(f.y) < 65520.f;
+                        ws[k] = f16x2_rn(f.x, f.y);
+                    }
+                    *reinterpret_cast<uint4*>(qt + i * 16) = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+                }
+                if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
+                fence_proxy_async_smem();  // the S MMAs (async proxy) read what was written
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * kBarQConv);
+        }
         for (int j = 0; active && j < n_tiles; ++j) {
             const int tile0 = j * kKeys, b = j & 1;
             const uint32_t tS = tmem + kColS + 128 * t + 64 * b + trow;
@@ -542,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p1 = (i + 1 < lim) ? p1 : 0.f;
                     }
                     ls2[(i >> 1) & 1] = __fadd2_rn(ls2[(i >> 1) & 1], make_float2(p0, p1));
-                    pk[i / 2] = bf16x2_rn(p0, p1);
+                    if constexpr (NARROW != 0) pk[i / 2] = f16x2_rn(p0, p1);
+                    else pk[i / 2] = bf16x2_rn(p0, p1);
                 }
             };
             if (masked) exp_pack(std::true_type{});

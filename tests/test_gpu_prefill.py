@@ -271,3 +271,24 @@ def test_prefill_chunk_edge_shapes(NQ, q_start, Hq, Hkv, S):
     ref = oracle.paged_prefill_chunk(q, q_start, kc, vc, table, kv_len, scale)
     got = _run(q, kc, vc, table, q_start, kv_len, scale)
     assert_close("bf16", got, ref, f"prefill NQ={NQ} q_start={q_start} G={Hq // Hkv} S={S}")
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "i8"])
+def test_prefill_one_byte_cache_query_out_of_f16_range_is_flagged(kv):
+    """One-byte caches run the tile's products on f16 operands: a query value the f16 range cannot hold raises
+    PKV_DEVERR_Q_RANGE (0x10); the other rows still match the oracle."""
+    q, kc, vc, table, kv_len = _chunk_case(40, 100, 8, 1, 16, seed=13, kv=kv)
+    q = q.copy()
+    q[5, 3, 7] = 0x47C8  # bf16 bits of 102400
+    dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
+    out = torch.empty_like(dq)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.pkv_paged_prefill_chunk(out, dq, 100, dk, dv, B.CacheDesc.for_cache(dk, 0.25, 0.5), to_device(table),
+                                kv_len, 1 / np.sqrt(128), err)
+    torch.cuda.synchronize()
+    assert err.item() & 0x10
+    code = {"e4m3": oracle.E4M3, "i8": oracle.I8}[kv]
+    rows = [0, 1, 20, 39]
+    ref = oracle.paged_prefill_chunk(q, 100, kc, vc, table, kv_len, 1 / np.sqrt(128), rows=rows, cache_dtype=code,
+                                     k_scale=0.25, v_scale=0.5)
+    assert_close(kv, to_host(out)[rows], ref, "rows without the out-of-range query")
