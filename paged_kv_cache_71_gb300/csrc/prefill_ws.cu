@@ -18,9 +18,10 @@
 //     table per copy, one lane per block) into two 4-deep rings; block-table
 //     entries are read 32 at a time, a batch ahead.  For FP8 / INT8 caches
 //     the codes go to a two-slot staging ring per operand and are widened to
-//     f16 into a 3-deep ring, half the rows by the producer and half by the
-//     MMA warp that consumes the operand; the MMAs of those caches run on f16
-//     operands (Q converted in place once, P packed as f16);
+//     f16 into a 3-deep ring: by the producer alone when both query tiles are
+//     live, else half the rows by the producer and half by the MMA warp that
+//     consumes the operand; the MMAs of those caches run on f16 operands (Q
+//     converted in place once, P packed as f16);
 //   * warps 9 and 11 issue the tcgen05 MMAs (each warp runs its loop, one
 //     elected lane issues): warp 9 S_A(j), S_B(j) into the buffers that
 //     P(j-2) was read from, as soon as P(j-2).V has completed; warp 11
@@ -50,7 +51,7 @@ constexpr int kStgSlot = kKeys * 128;          // one key tile of one-byte codes
 constexpr int kOffQ = 0;                       // tile A: 2 halves, tile B: 2 halves
 
 // Shared-memory plan per cache kind (NARROW: 0 bf16, 1 FP8 E4M3 codes, 2 INT8 codes).  One-byte caches
-// land in a two-slot staging ring per operand and are widened to f16 by the producer and MMA warps.
+// land in a two-slot staging ring per operand and are widened to f16 by the producer (and MMA) warps.
 template <int NARROW>
 struct Plan {
     static constexpr int kStages = NARROW ? 3 : 4;                  // bf16 K and V ring depth
@@ -148,7 +149,8 @@ __device__ __forceinline__ uint32_t s8x2_to_f16x2(uint32_t f, int i0) {
 
 }  // namespace
 
-template <int NARROW>
+// ADAPT (one-byte caches, varlen launches): each CTA chooses split widening when only its query tile A is live
+template <int NARROW, bool ADAPT>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -248,14 +250,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int max_key = min(kv_len - 1, q_start + last_q);
     const int n_tiles = max_key / kKeys + 1;
     const int blocks_per_tile = kKeys / a.S;
+    // One-byte caches: with both query tiles live the tensor pipe has work enough to hide the widening and the
+    // producer widens every row, leaving the MMA warps to issue; in a varlen launch a CTA with tile A alone (a
+    // decode token) has the MMA warps also widen half of the rows of the operand they consume.  Single-chunk
+    // launches compile the producer-only form alone.
+    const bool split = NARROW != 0 && ADAPT && !has_b;
 
     if (tid == 0) {
         // the bf16 instance never waits on the staging-free barriers
         for (int i = 0; i < (NARROW ? kNumBars : kBarStgFree); ++i) {
             int count = (i >= kBarPFull && i < kBarPFull + 4) ? kSoftmax / 2 : i == kBarDrain ? 2 : 1;
             if (i == kBarQConv) count = kSoftmax / 32;
-            // one-byte caches: a bf16 K or V stage is complete when both warps widened their halves
-            if (NARROW && ((i >= kBarKFull && i < kBarKFull + kMaxStages) || (i >= kBarVFull && i < kBarVFull + kMaxStages)))
+            // split widening: an f16 K or V stage is complete when both warps widened their halves
+            if (split && ((i >= kBarKFull && i < kBarKFull + kMaxStages) || (i >= kBarVFull && i < kBarVFull + kMaxStages)))
                 count = 2;
             mbar_init(bar + 8 * i, count);
         }
@@ -273,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // One-byte caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into f16 stage st
     // (exact: every E4M3 and INT8 code is an f16 value; the per-tensor or per-head scales go to the scores and the
-    // output).  128 codes per key row, in 128-byte swizzled lines like the bf16 halves.  Each of the two warps
-    // that serve an operand (its producer and its MMA warp) widens one half of the rows.
+    // output).  128 codes per key row, in 128-byte swizzled lines like the 16-bit halves.  With split widening
+    // each of the two warps that serve an operand (its producer and its MMA warp) widens one half of the rows.
     auto widen_rows = [&](bool is_v, int slot, int st, int rr) {
         const uint8_t* src = smem + kOffStg + ((is_v ? 2 : 0) + slot) * kStgSlot;
         uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * 2 * kKvHalf;
@@ -367,8 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = j + 1;
             }
         } else {
-            // one-byte codes: copy tile j+1 into its staging slot (once the MMA warp has widened its half of tile
-            // j-1 from there), then widen the first half of the rows of tile j into the bf16 ring
+            // one-byte codes: copy tile j+1 into its staging slot (once tile j-1 has been widened from there: by this
+            // warp, and with split widening by the MMA warp too), then widen the rows of tile j (split widening: the
+            // first half) into the f16 ring
             const int sbar = kBarStg + (is_v ? 2 : 0), fbar = kBarStgFree + (is_v ? 2 : 0);
             const uint32_t stg0 = sb + kOffStg + (is_v ? 2 : 0) * kStgSlot;
             auto stage = [&](int jj, int row) {
@@ -383,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kStages;
                 if (j + 1 < n_tiles) {
-                    // slot (j+1) & 1 last held tile j-1: this warp widened its half at j-1 (and fenced)
-                    if (j >= 1 && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (fbar + ((j - 1) & 1)),
+                    // slot (j+1) & 1 last held tile j-1: this warp widened its rows at j-1 (and fenced)
+                    if (split && j >= 1 && !__all_sync(kFull, mbar_spin_bounded(bar + 8 * (fbar + ((j - 1) & 1)),
                                                                       ((j - 1) >> 1) & 1, a.timeout_ns))) {
                         if (lane == 0) *abort_flag = 1;
                         break;
@@ -400,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 widened = j + 1;
                 if (__any_sync(kFull, *abort_flag != 0)) break;
                 widen_rows(is_v, j & 1, st, 0);
+                if (!split) widen_rows(is_v, j & 1, st, 1);
                 fence_proxy_async_smem();  // the MMA (async proxy) reads what was written; the next copy overwrites
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar + 8 * (full + st));
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // Q landed (bf16 caches) or converted to f16 by the softmax warps (one-byte caches)
             const uint32_t qb = bar + 8 * (NARROW ? kBarQConv : kBarQFull);
-            if constexpr (NARROW != 0) ok = widen_half(false, 0);
+            if (split) ok = widen_half(false, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const uint32_t kb = bar + 8 * (kBarKFull + j % kStages), kph = (j / kStages) & 1;
                 for (int t = 0; t < (has_b ? 2 : 1); ++t) {
@@ -472,9 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_commit_warp(bar + 8 * (kBarKEmpty + j % kStages));
                 // the next tile's half of K, while the tensor pipe works on S(j)
-                if constexpr (NARROW != 0) {
-                    if (j + 1 < n_tiles) ok = widen_half(false, j + 1);
-                }
+                if (split && j + 1 < n_tiles) ok = widen_half(false, j + 1);
             }
         } else {
             // P(j).V(j) of both query tiles once their softmax is done
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV<NARROW>, kk > 0 ? 1u : acc0);
                 tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
             };
-            if constexpr (NARROW != 0) ok = widen_half(true, 0);
+            if (split) ok = widen_half(true, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j % kStages, b = j & 1;
                 const uint32_t ph = (j >> 1) & 1, vb = bar + 8 * (kBarVFull + st), vph = (j / kStages) & 1;
@@ -502,9 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_commit_warp(bar + 8 * (kBarVEmpty + st));
                 // the next tile's half of V, while the tensor pipe works on P(j).V
-                if constexpr (NARROW != 0) {
-                    if (j + 1 < n_tiles) ok = widen_half(true, j + 1);
-                }
+                if (split && j + 1 < n_tiles) ok = widen_half(true, j + 1);
             }
             // the last P.V follows every S MMA (it needed that tile's softmax), so this covers all MMAs
             if (ok) tc_commit_warp(bar + 8 * kBarFinal);
@@ -704,8 +709,11 @@ template <int NARROW>
 static cudaError_t launch_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const PrefillArgs& a, cudaStream_t stream) {
     const size_t smem = ws_smem_bytes<NARROW>();
-    cudaError_t e = cudaFuncSetAttribute(paged_prefill_ws_kernel<NARROW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    constexpr bool kAdapt = NARROW != 0;
+    const bool adapt = kAdapt && a.cu_q != nullptr;
+    cudaError_t e = cudaFuncSetAttribute(
+        adapt ? paged_prefill_ws_kernel<NARROW, kAdapt> : paged_prefill_ws_kernel<NARROW, false>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // CTAs: one per 2 * 128 / G tokens of each chunk; in the varlen form an upper bound (each chunk adds at
     // most one partial CTA), the CTAs past the chunks' total leave at once
@@ -713,7 +721,10 @@ static cudaError_t launch_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, c
     const int grid_x = a.cu_q == nullptr ? (a.NQ + cta_q - 1) / cta_q : a.NQ / cta_q + a.nseq;
     if (grid_x <= 0) return cudaSuccess;
     dim3 grid(grid_x, a.Hkv);
-    paged_prefill_ws_kernel<NARROW><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+    if (adapt)
+        paged_prefill_ws_kernel<NARROW, kAdapt><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
+    else
+        paged_prefill_ws_kernel<NARROW, false><<<grid, kThreads, smem, stream>>>(qmap, kmap, vmap, a);
     return cudaGetLastError();
 }
 
