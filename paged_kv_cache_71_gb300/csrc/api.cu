@@ -102,6 +102,15 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// L2 fetch size for rows of `row_bytes` contiguous bytes: the row itself, never more.  The row of the next KV head
+// follows in memory, and a wider promotion fetches it from DRAM for a warp that does not need it (at 128-byte rows
+// 256-byte promotion read 1.42x the bytes of an INT8 decode, the neighbour head's rows mostly evicted before use).
+static CUtensorMapL2promotion promotion_for_row(uint64_t row_bytes) {
+    return row_bytes >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+           : row_bytes >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_64B;
+}
+
 // A [NB*S][Hkv][D] view of one cache tensor, box = one (block, head) tile [S][1][D].
 static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv_cache_desc& c) {
     EncodeTiledFn enc = encode_fn();
@@ -117,7 +126,7 @@ static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv
     cuuint32_t box[3] = {static_cast<cuuint32_t>(c.head_dim), 1u, static_cast<cuuint32_t>(c.block_size)};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, promotion_for_row(static_cast<uint64_t>(c.head_dim) * es),
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return PKV_OK;
@@ -134,7 +143,7 @@ static pkv_status tensor_map_sw128(CUtensorMap* map, const void* base, bool fp8,
     cuuint32_t box[3] = {fp8 ? 128u : 64u, b1, b2};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promotion_for_row(d0 * es),
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)", static_cast<int>(r));
     return PKV_OK;

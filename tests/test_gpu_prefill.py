@@ -187,10 +187,13 @@ def test_prefill_varlen_mixed_batch_matches_oracle(Hq, Hkv, S):
     assert np.isnan(got[cu[-1]:]).all(), "rows outside every chunk were written"
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(16, 4), (64, 8)])
 @pytest.mark.parametrize("kv,k_scale,v_scale", [("e4m3", 0.25, 0.5), ("i8", 1 / 32, 1 / 16)])
-def test_prefill_varlen_one_byte_caches(kv, k_scale, v_scale):
-    """The mixed batch over an FP8 or INT8 cache: codes widened on chip, scales on scores and output."""
-    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case(MIXED, 16, 4, 16, seed=29, kv=kv)
+def test_prefill_varlen_one_byte_caches(kv, k_scale, v_scale, Hq, Hkv):
+    """The mixed batch over an FP8 or INT8 cache: codes widened on chip, scales on scores and output.  Single-token
+    chunks and chunk tails that leave query tile B empty run with split widening and a four-slot staging ring (up to
+    32 key tiles here, so the ring wraps many times)."""
+    q, kc, vc, tables, cu, q_starts, kv_lens = _varlen_case(MIXED, Hq, Hkv, 16, seed=29 + Hq, kv=kv)
     scale = 1 / np.sqrt(128)
     out, err = _run_varlen(q, kc, vc, tables, cu, q_starts, kv_lens, scale, k_scale, v_scale)
     assert err == 0, hex(err)
