@@ -99,6 +99,16 @@ def decode_fma_flops(w) -> int:
 DECODE_SOURCES = ("decode.cuh", "pkv_device.cuh", "decode_bf16_s16.cu")
 
 
+def decode_kernel(w) -> tuple[str, tuple]:
+    """The decode kernel a workload runs on, and the sources its profile digest covers: FP8 / INT8 caches with
+    128-dim heads take the tensor-core form, everything else the CUDA-core form."""
+    if w.kv_dtype in ("e4m3", "i8") and w.head_dim == 128:
+        tag = "fp8" if w.kv_dtype == "e4m3" else "i8"
+        return "paged_decode_mma_kernel", ("decode_mma.cuh", "decode.cuh", "pkv_device.cuh",
+                                           f"decode_mma_{tag}_s{w.block_size}.cu")
+    return "paged_decode_kernel", DECODE_SOURCES
+
+
 def kernel_digest(files) -> str:
     import hashlib
     h = hashlib.sha256()
@@ -108,7 +118,7 @@ def kernel_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, sources=DECODE_SOURCES):
     """DRAM bytes per decode launch from the committed ncu summary of this workload, if that summary was
     taken on the kernel sources as they are now (same digest); otherwise None."""
     import re
@@ -119,7 +129,7 @@ def profiled_traffic(workload: str):
         return None
     dig = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
     tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    if not dig or not tr or dig.group(1) != kernel_digest(DECODE_SOURCES):
+    if not dig or not tr or dig.group(1) != kernel_digest(sources):
         return None
     return int(tr.group(1))
 
@@ -374,14 +384,16 @@ def main():
     alg = decode_algorithmic_bytes(w)
     dec_avg = float(np.mean(decode_ms))
     achieved = alg / (dec_avg / 1e3) / 1e9
+    kname, ksrc = decode_kernel(w)
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name), "peak_source": peak_src,
-            "kernel": "paged_decode_kernel", "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
-    # the binding ceiling: reading the K/V at the HBM peak needs (flops per byte) x peak of fp32 FMA work; where
-    # that exceeds the CUDA cores' FMA peak (large G, one-byte caches) the kernel is bound by arithmetic instead
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name, ksrc), "peak_source": peak_src,
+            "kernel": kname, "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
+    # the binding ceiling of the CUDA-core form: reading the K/V at the HBM peak needs (flops per byte) x peak of
+    # fp32 FMA work; where that exceeds the CUDA cores' FMA peak the kernel is bound by arithmetic instead (the
+    # tensor-core form does its contractions on the tensor pipe, far below its peak, and stays HBM-bound)
     flops = decode_fma_flops(w)
     fma_needed = flops / alg * peak * 1e9 / 1e12  # TFLOP/s at the HBM peak
-    if fma_needed > FP32_FMA_TFLOPS:
+    if kname == "paged_decode_kernel" and fma_needed > FP32_FMA_TFLOPS:
         achieved_tf = flops / (dec_avg / 1e3) / 1e12
         roof.update({"bound": "alu", "achieved": round(achieved_tf, 2), "peak": round(FP32_FMA_TFLOPS, 2),
                      "unit": "TFLOP/s", "frac": round(achieved_tf / FP32_FMA_TFLOPS, 4),

@@ -10,6 +10,7 @@
 
 #include "cache_ops.cuh"
 #include "decode.cuh"
+#include "decode_mma.cuh"
 #include "prefill.cuh"
 
 namespace pkv {
@@ -373,6 +374,68 @@ PKV_API pkv_status pkv_block_hashes(const int32_t* token_ids, const int64_t* cu_
     return PKV_OK;
 }
 
+template <class KV>
+static cudaError_t dispatch_mma(int S, int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
+                                int grid, int block, size_t smem, cudaStream_t s) {
+#define PKV_MMA_G(S_)                                                                      \
+    switch (G) {                                                                           \
+        case 1: return launch_paged_decode_mma<1, S_, KV>(km, vm, a, grid, block, smem, s); \
+        case 2: return launch_paged_decode_mma<2, S_, KV>(km, vm, a, grid, block, smem, s); \
+        case 4: return launch_paged_decode_mma<4, S_, KV>(km, vm, a, grid, block, smem, s); \
+        case 8: return launch_paged_decode_mma<8, S_, KV>(km, vm, a, grid, block, smem, s); \
+        default: return cudaErrorInvalidValue;                                             \
+    }
+    switch (S) {
+        case 4: PKV_MMA_G(4)
+        case 8: PKV_MMA_G(8)
+        case 16: PKV_MMA_G(16)
+        case 32: PKV_MMA_G(32)
+        default: return cudaErrorInvalidValue;
+    }
+#undef PKV_MMA_G
+}
+
+// Decode over an FP8 or INT8 cache with 128-dim heads: the tensor-core form of the kernel (decode_mma.cuh).  Its
+// stages hold 128-byte swizzled K and V tiles, each starting on a 1024-byte boundary; `a` arrives with everything but
+// the shared-memory plan filled in.
+static pkv_status decode_one_byte_mma(DecodeArgs a, const pkv_cache_desc& c, int G, int num_seqs, const void* k_cache,
+                                      const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
+    const int S = c.block_size, Hkv = c.num_kv_heads;
+    const uint32_t tile = static_cast<uint32_t>(std::max(S * 128, 1024));
+    a.kv_bytes = static_cast<uint32_t>(S * 128);
+    a.q_bytes = static_cast<uint32_t>(G * 256);
+    a.stage_bytes = 2 * tile + static_cast<uint32_t>(std::max(G * 256, 1024));
+    a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 1023) / 1024 * 1024);
+    const size_t budget = static_cast<size_t>(di.smem_optin) - 256 - 1024;  // static shared memory, alignment slack
+    int nw = policy_warps(G, 128), depth = 0;
+    while (nw >= 1) {
+        const size_t avail = budget > a.prefix_bytes ? budget - a.prefix_bytes : 0;
+        const size_t per_warp_avail = avail / nw;
+        depth = 6;  // the deepest pipeline whose region, rounded to 1024 bytes, fits
+        while (depth >= 2 && (static_cast<size_t>(depth) * a.stage_bytes + 8 * depth + 1023) / 1024 * 1024 > per_warp_avail)
+            --depth;
+        if (depth >= 2) break;
+        nw >>= 1;
+    }
+    if (depth < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for this block size and batch");
+    a.depth = depth;
+    a.warp_bytes = static_cast<uint32_t>((static_cast<size_t>(depth) * a.stage_bytes + 8 * depth + 1023) / 1024 * 1024);
+    const size_t smem = a.prefix_bytes + static_cast<size_t>(nw) * a.warp_bytes + 1024;
+    const uint64_t rows = static_cast<uint64_t>(c.num_blocks) * S;
+    CUtensorMap km, vm;
+    pkv_status st;
+    if ((st = tensor_map_sw128(&km, k_cache, true, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, true, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if (a.tickets) {
+        cudaError_t e = cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(num_seqs) * Hkv * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing split-KV counters");
+    }
+    const cudaError_t e = c.dtype == PKV_FP8_E4M3 ? dispatch_mma<KvE4M3>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
+                                                  : dispatch_mma<KvI8>(S, G, km, vm, a, di.sms, nw * 32, smem, s);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
+    return PKV_OK;
+}
+
 PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32_t num_seqs,
                                                       int32_t num_q_heads, int32_t num_splits, size_t* bytes) {
     g_detail[0] = 0;
@@ -489,6 +552,8 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
     a.timeout_ns = 2000000000ull;
+    if (narrow(cache->dtype) && D == 128)
+        return decode_one_byte_mma(a, *cache, G, num_seqs, k_cache, v_cache, di, static_cast<cudaStream_t>(stream));
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
     int nw = policy_warps(G, D), depth = 0;
     while (nw >= 1) {

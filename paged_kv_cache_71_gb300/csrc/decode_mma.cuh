@@ -1,0 +1,509 @@
+// decode_mma.cuh -- paged decode attention over FP8 (E4M3) or INT8 K/V caches with the per-warp tensor-core MMA.
+//
+// Method: the same online-softmax recurrence over the blocks named by each sequence's block table as the CUDA-core
+// decode kernel (decode.cuh; "从 PagedAttention 到 Chunked Prefill" §2.2, "PagedAttention：块表"), with the same
+// work split, TMA pipeline per warp and split-KV records.  What changes is the arithmetic: with one-byte codes the
+// CUDA cores must do 2·G fp32 multiply-adds per byte streamed, which at G = 4 is two thirds of their peak at the
+// HBM rate and at G = 8 more than all of it.  Here each warp computes, per 16-token tile of one (sequence, KV head),
+//   S = Q · Kᵀ   as 2 × 8 mma.sync.m16n8k16 (rows: the G query heads, padded to 16; columns: 8 tokens; k: 16 dims)
+//   O += P · V  as 16 mma.sync.m16n8k16 (rows: the G heads; columns: 8 head dims; k: the 16 tokens)
+// on f16 operands with fp32 accumulation.  Every E4M3 and INT8 code is exactly an f16 value, Q is converted from
+// bf16 to f16 once per segment (exact for |q| in [2^-14, 65504]; larger values raise PKV_DEVERR_Q_RANGE), and the
+// probabilities are rounded to f16 (relative 2^-11) before P·V.  The per-tensor or per-head scales are applied to
+// the fp32 scores and to the output.
+//
+// Fragment layout (lane = 4 g + t): in S, thread (g, t) holds row g (query head g of the group) and tokens 2t, 2t+1
+// of each 8-token column tile.  The k index of the S MMAs is a permutation of the head dimension chosen so that a
+// thread's K operand is one contiguous 32-byte run of its token's row (dims 32t .. 32t + 31, four per k-step), and
+// Q is permuted the same way; the dot product does not depend on the order of its terms.  In P·V the k index is
+// the token in natural order, so the probabilities of S's output fragment are P's input fragment as they stand, and
+// the column of output tile n held by thread (g, t) is head dim 16 g + n: each thread reads 16 contiguous codes of
+// four token rows and pairs tokens with one byte permute per two dims.  The output thread (g, t) ends with is
+// O[g][32 t .. 32 t + 31].  K and V tiles arrive by TMA with the 128-byte swizzle (128 codes per row), which keeps
+// all these 16-byte shared-memory reads free of bank conflicts.
+#pragma once
+
+#include "decode.cuh"
+
+namespace pkv {
+
+// one m16n8k16 MMA, f16 operands, fp32 accumulate; rows 8-15 of A are zero and their outputs are dropped
+__device__ __forceinline__ void mma_f16_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2, uint32_t b0,
+                                              uint32_t b1) {
+    float d2, d3;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(c0), "+f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    (void)d2;
+    (void)d3;
+}
+
+// two one-byte codes (low byte first in the low 16 bits of w, or the high 16 bits when HI) -> f16x2, exactly
+template <class KV, bool HI>
+__device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w) {
+    if constexpr (KV::code == PKV_INT8) {
+        // signed byte b: (b ^ 0x80) = b + 128 in the low mantissa bits of 1024.0 reads 1024 + b + 128; one packed
+        // subtraction of 1152 leaves b
+        const uint32_t f = w ^ 0x80808080u;
+        const uint32_t h = __byte_perm(f, 0x64646464u, HI ? 0x7362u : 0x5140u);
+        uint32_t r;
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+        return r;
+    } else {
+        uint32_t r;
+        const uint16_t c = static_cast<uint16_t>(HI ? (w >> 16) : (w & 0xffffu));
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+        return r;
+    }
+}
+
+__device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16 bytes at chunk c (16-byte unit, 0..7) of a 128-byte row stored with the 128-byte TMA swizzle; `row_addr` is
+// the row's shared-memory address (128-byte aligned)
+__device__ __forceinline__ uint4 lds_sw128(uint32_t row_addr, int c) {
+    uint4 v;
+    const uint32_t addr = row_addr + ((static_cast<uint32_t>(c) ^ ((row_addr >> 7) & 7u)) << 4);
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// byte b (0..3) of word w, and of word x, interleaved: [w.b, x.b, w.b+1, x.b+1] for even b
+template <int B>
+__device__ __forceinline__ uint32_t pair_bytes(uint32_t w, uint32_t x) {
+    static_assert(B == 0 || B == 2, "even byte");
+    return __byte_perm(w, x, B == 0 ? 0x5140u : 0x7362u);
+}
+
+// Shared-memory plan of one warp stage: K tile, V tile (each S rows of 128 codes, padded to 1024 bytes so that
+// every tile starts on the 128-byte swizzle's 1024-byte period), then the G query rows (bf16).
+template <int G, int S>
+struct MmaStage {
+    static constexpr int kTile = S * 128 < 1024 ? 1024 : S * 128;
+    static constexpr int kQ = G * 256 < 1024 ? 1024 : G * 256;
+    static constexpr int kBytes = 2 * kTile + kQ;
+};
+
+template <int G, int S, class KV>
+__global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                            const DecodeArgs a) {
+    constexpr int D = 128;
+    constexpr int TS = S < 16 ? S : 16;   // tokens of a block per 16-row MMA tile
+    constexpr int NT = S / TS;            // tiles per block
+    constexpr int kTile = MmaStage<G, S>::kTile;
+    static_assert(G <= 8, "query rows of one MMA tile");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int NW = blockDim.x >> 5;
+    const int B = a.B, Hkv = a.Hkv;
+    const int g = lane >> 2, t = lane & 3;  // fragment row (query head) and column pair
+
+    // ---- 1. per-sequence block counts and their prefix sum (P[s] = blocks before s)
+    int* P = reinterpret_cast<int*>(smem);
+    {
+        const int per = (B + blockDim.x - 1) / blockDim.x;
+        const int s0 = tid * per;
+        const int s1 = min(B, s0 + per);
+        int local = 0;
+        for (int s = s0; s < s1; ++s) {
+            int L = a.context_lens[s];
+            if (L < 0 || L > a.MB * S) {
+                if (blockIdx.x == 0) raise_error(a.err, PKV_DEVERR_BAD_LENGTH);
+                L = 0;
+            }
+            local += (L + S - 1) / S;
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        __shared__ int warp_tot[32];
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int wbase = 0;
+        for (int i = 0; i < warp; ++i) wbase += warp_tot[i];
+        int run = wbase + incl - local;
+        for (int s = s0; s < s1; ++s) {
+            P[s] = run;
+            int L = a.context_lens[s];
+            if (L < 0 || L > a.MB * S) L = 0;
+            run += (L + S - 1) / S;
+        }
+        if (tid == blockDim.x - 1) {
+            int tot = 0;
+            for (int i = 0; i < NW; ++i) tot += warp_tot[i];
+            P[B] = tot;
+        }
+        __syncthreads();
+    }
+
+    // ---- 2. empty sequences get zero rows (spread over the CTAs)
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        if (P[s + 1] != P[s]) continue;
+        const int n = a.Hq * D;
+        for (int i = tid; i < n; i += blockDim.x) reinterpret_cast<uint16_t*>(a.out)[static_cast<size_t>(s) * n + i] = 0;
+    }
+
+    // ---- 3. this warp's stages and barriers, and its share of the work stream
+    uint8_t* wreg = smem + a.prefix_bytes + static_cast<size_t>(warp) * a.warp_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wreg + static_cast<size_t>(a.depth) * a.stage_bytes);
+    const uint32_t wreg_u32 = smem_u32(wreg);
+    const uint32_t bars_u32 = smem_u32(bars);
+    if (lane == 0) {
+        for (int i = 0; i < a.depth; ++i) mbar_init(bars_u32 + 8 * i, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int T = Hkv * P[B];
+    if (T == 0) return;
+    const int W = min(static_cast<int>(gridDim.x) * NW, T);
+    const int w = blockIdx.x * NW + warp;
+    const WorkSplit split{P, B, Hkv, T, a.part_blocks, W, T / W, T % W};
+    const int A0 = split.start(w);
+    const int A1 = split.start(w + 1);
+    if (A0 >= A1) return;
+    if (lane == 0) {
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+    }
+    const uint64_t pol = policy_evict_first();
+
+    // Stream position x -> packed metadata (computed by the lane that owns x).
+    auto make_meta = [&](int x) -> Meta {
+        Meta m{0, -1, 0};
+        if (x >= A1) return m;
+        const int s = find_seq(P, B, x / Hkv);
+        const int local = x - Hkv * P[s];
+        const int nb = P[s + 1] - P[s];
+        const int h = local / nb;
+        const int j = local - h * nb;
+        const int L = a.context_lens[s];
+        m.a = s * 1024 + h;
+        m.b = a.block_tables[static_cast<size_t>(s) * a.MB + j];
+        const int valid = min(S, L - j * S);
+        m.c = valid | (j == 0 ? kMetaFirst : 0) | (j == nb - 1 ? kMetaLast : 0) |
+              ((m.b >= 0 && m.b < a.NB) ? kMetaOk : 0);
+        return m;
+    };
+
+    // Issue the copies of stream index k into stage k % depth (by the lane holding the block's metadata).
+    auto issue = [&](int k, const Meta& m) {
+        const int st = static_cast<int>(k % a.depth);
+        const bool seg_start = (m.c & kMetaFirst) || (k == 0);
+        const bool ok = (m.c & kMetaOk) != 0;
+        if (!ok) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
+        const uint32_t tx = (ok ? 2u * a.kv_bytes : 0u) + (seg_start ? a.q_bytes : 0u);
+        const uint32_t bar = bars_u32 + 8 * st;
+        const uint32_t dst = wreg_u32 + st * a.stage_bytes;
+        if (tx) mbar_arrive_expect_tx(bar, tx); else mbar_arrive(bar);
+        const int s = m.a >> 10, h = m.a & 1023;
+        if (ok) {
+            tma_load_3d(dst, &kmap, 0, h, m.b * S, bar, pol);
+            tma_load_3d(dst + kTile, &vmap, 0, h, m.b * S, bar, pol);
+        }
+        if (seg_start) {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) +
+                                 (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G) * D * 2;
+            bulk_load(dst + 2 * kTile, src, a.q_bytes, bar);
+        }
+    };
+
+    const int n_blocks = A1 - A0;
+    int wbase = A0;
+    Meta cur = make_meta(wbase + lane);
+    Meta nxt = make_meta(wbase + 32 + lane);
+    if (lane < a.depth && lane < n_blocks) {
+        fence_proxy_async_smem();
+        issue(lane, cur);
+    }
+
+    // Bounded wait for stage k; on timeout record the error and drain the copies still in flight (bounded).
+    auto wait_stage = [&](int k) -> bool {
+        const int st = static_cast<int>(k % a.depth);
+        if (mbar_wait_bounded(bars_u32 + 8 * st, static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
+            return true;
+        raise_error(a.err, PKV_DEVERR_TIMEOUT);
+        for (int kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
+            mbar_wait_bounded(bars_u32 + 8 * static_cast<int>(kk % a.depth),
+                              static_cast<uint32_t>((kk / a.depth) & 1), a.timeout_ns);
+        return false;
+    };
+
+    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    int k = 0;
+    while (k < n_blocks) {
+        // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
+        const int seg_x0 = A0 + k;
+        uint32_t qa[8][2];  // Q fragments per k-step (row g; dims 32t + 4ks + {0,1} and {2,3}), f16
+        float o[16][2];     // O[g][32t + n] and O[g][32t + 16 + n] for output tile n
+        float m_ref = -INFINITY;  // running max of row g (log2 units), the same in the 4 threads of the row
+        float l_run = 0.f;        // this thread's share of the running sum of row g
+        int ma = 0, mc = 0, seg_first = 0;
+        bool first = true;
+        int x_last;
+        float qm = a.q_mul;
+
+        // One 16-row MMA tile of the block: K rows at kt, V rows at vt (shared addresses of the tile's row 0),
+        // tv valid tokens (M: tv may be below the tile's rows, the rest are stale and masked out).
+        auto tile = [&](auto masked, uint32_t kt, uint32_t vt, int tv) {
+            constexpr bool M = decltype(masked)::value;
+            const int lim = M ? tv : TS;
+            // ---- S = Q Kᵀ: column tile 0 holds tokens 0-7, tile 1 tokens 8-15 (thread: tokens 2t, 2t+1 of each)
+            float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
+            {
+                const uint4 x0 = g < TS ? lds_sw128(kt + g * 128, 2 * t) : zero4;
+                const uint4 x1 = g < TS ? lds_sw128(kt + g * 128, 2 * t + 1) : zero4;
+                const uint32_t kw0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16_rows8(s0a, s0b, qa[ks][0], qa[ks][1], codes2_to_f16x2<KV, false>(kw0[ks]),
+                                  codes2_to_f16x2<KV, true>(kw0[ks]));
+                if constexpr (TS > 8) {
+                    const uint4 y0 = lds_sw128(kt + (8 + g) * 128, 2 * t);
+                    const uint4 y1 = lds_sw128(kt + (8 + g) * 128, 2 * t + 1);
+                    const uint32_t kw1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_f16_rows8(s1a, s1b, qa[ks][0], qa[ks][1], codes2_to_f16x2<KV, false>(kw1[ks]),
+                                      codes2_to_f16x2<KV, true>(kw1[ks]));
+                }
+            }
+            // ---- online softmax of row g over the tile's tokens
+            const int t0 = 2 * t, t2 = 8 + 2 * t;
+            float sc0 = (t0 < lim) ? s0a * qm : -INFINITY;
+            float sc1 = (t0 + 1 < lim) ? s0b * qm : -INFINITY;
+            float sc2 = (t2 < lim) ? s1a * qm : -INFINITY;
+            float sc3 = (t2 + 1 < lim) ? s1b * qm : -INFINITY;
+            float mb = fmaxf(fmaxf(sc0, sc1), fmaxf(sc2, sc3));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+            const bool need = mb > m_ref + kLazyRescale;
+            if (__any_sync(kFull, need)) {
+                const float m_new = need ? mb : m_ref;
+                const float alpha = (m_new == m_ref) ? 1.f : ex2_approx(m_ref - m_new);
+                l_run *= alpha;
+                m_ref = m_new;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= alpha;
+                    o[n][1] *= alpha;
+                }
+            }
+            const float p0 = ex2_approx(sc0 - m_ref), p1 = ex2_approx(sc1 - m_ref);
+            const float p2 = ex2_approx(sc2 - m_ref), p3 = ex2_approx(sc3 - m_ref);
+            l_run += (p0 + p1) + (p2 + p3);
+            const uint32_t pa0 = f16x2_pack(p0, p1), pa2 = f16x2_pack(p2, p3);
+            // ---- O += P V: thread (g, t) supplies V[2t, 2t+1, 2t+8, 2t+9][16g .. 16g+15]; rows past the valid
+            // tokens are zero (stale rows may hold anything, and 0 * NaN would reach O)
+            const uint4 v0 = (t0 < lim) ? lds_sw128(vt + t0 * 128, g) : zero4;
+            const uint4 v1 = (t0 + 1 < lim) ? lds_sw128(vt + (t0 + 1) * 128, g) : zero4;
+            const uint4 v2 = (t2 < lim) ? lds_sw128(vt + t2 * 128, g) : zero4;
+            const uint4 v3 = (t2 + 1 < lim) ? lds_sw128(vt + (t2 + 1) * 128, g) : zero4;
+            const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
+                const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
+                mma_f16_rows8(o[4 * j][0], o[4 * j][1], pa0, pa2, codes2_to_f16x2<KV, false>(lo01),
+                              codes2_to_f16x2<KV, false>(lo23));
+                mma_f16_rows8(o[4 * j + 1][0], o[4 * j + 1][1], pa0, pa2, codes2_to_f16x2<KV, true>(lo01),
+                              codes2_to_f16x2<KV, true>(lo23));
+                mma_f16_rows8(o[4 * j + 2][0], o[4 * j + 2][1], pa0, pa2, codes2_to_f16x2<KV, false>(hi01),
+                              codes2_to_f16x2<KV, false>(hi23));
+                mma_f16_rows8(o[4 * j + 3][0], o[4 * j + 3][1], pa0, pa2, codes2_to_f16x2<KV, true>(hi01),
+                              codes2_to_f16x2<KV, true>(hi23));
+            }
+        };
+
+        while (true) {
+            const int x = A0 + k;
+            if (x - wbase >= 32) {
+                wbase += 32;
+                cur = nxt;
+                nxt = make_meta(wbase + 32 + lane);
+            }
+            const int src = x - wbase;
+            ma = __shfl_sync(kFull, cur.a, src);
+            mc = __shfl_sync(kFull, cur.c, src);
+            if (!wait_stage(k)) return;
+            const uint32_t sp = wreg_u32 + static_cast<uint32_t>(k % a.depth) * a.stage_bytes;
+            if (first) {
+                // Q of this (s, h): row g, dims 32t .. 32t+31 (bf16 -> f16 in the permuted k order)
+                seg_first = mc & kMetaFirst;
+                qm = a.k_head ? a.q_base * __ldg(a.k_head + (ma & 1023)) : a.q_mul;
+                bool in_range = true;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint4 w4 = zero4;
+                    if (g < G) {
+                        const uint32_t qaddr = sp + 2 * kTile + g * 256 + t * 64 + i * 16;
+                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w4.x), "=r"(w4.y), "=r"(w4.z), "=r"(w4.w)
+                                     : "r"(qaddr));
+                    }
+                    const float2 f0 = bf16x2_to_float2(w4.x), f1 = bf16x2_to_float2(w4.y);
+                    const float2 f2 = bf16x2_to_float2(w4.z), f3 = bf16x2_to_float2(w4.w);
+                    in_range = in_range && fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))) < 65520.f &&
+                               fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))) < 65520.f;
+                    qa[2 * i][0] = f16x2_pack(f0.x, f0.y);
+                    qa[2 * i][1] = f16x2_pack(f1.x, f1.y);
+                    qa[2 * i + 1][0] = f16x2_pack(f2.x, f2.y);
+                    qa[2 * i + 1][1] = f16x2_pack(f3.x, f3.y);
+                }
+                if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
+#pragma unroll
+                for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = 0.f;
+                first = false;
+            }
+            if (mc & kMetaOk) {
+                const int valid = mc & 63;
+#pragma unroll
+                for (int ti = 0; ti < NT; ++ti) {
+                    const int tv = valid - ti * TS;
+                    if (tv <= 0) break;
+                    const uint32_t kt = sp + ti * TS * 128, vt = sp + kTile + ti * TS * 128;
+                    if (tv >= TS) tile(std::false_type{}, kt, vt, TS);
+                    else tile(std::true_type{}, kt, vt, tv);
+                }
+            }
+            __syncwarp();
+
+            // ---- refill this stage with stream index k + depth (issued by the lane holding its metadata)
+            const int kn = k + a.depth;
+            if (kn < n_blocks) {
+                const int sn = A0 + kn - wbase;
+                if (lane == (sn & 31)) {
+                    fence_proxy_async_smem();
+                    issue(kn, sn < 32 ? cur : nxt);
+                }
+            }
+            const bool last = (mc & kMetaLast) != 0 || x == A1 - 1;
+            ++k;
+            if (last) {
+                x_last = x;
+                break;
+            }
+        }
+
+        // ------------------------------------------------ end of segment
+        l_run += __shfl_xor_sync(kFull, l_run, 1);
+        l_run += __shfl_xor_sync(kFull, l_run, 2);
+        const int s = ma >> 10, h = ma & 1023;
+        const int nb = P[s + 1] - P[s];
+        const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.o_mul;
+        auto store_row = [&](const float (&v)[32], float inv) {  // out[s][h G + g][32t .. 32t+31], bf16
+            uint32_t wv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wv[i] = static_cast<uint32_t>(float_to_bf16_bits(v[2 * i] * inv)) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(v[2 * i + 1] * inv)) << 16);
+            uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) +
+                                                   ((static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) *
+                                                        D + 32 * t) * 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) orow[i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+        };
+        const bool whole = seg_first && (mc & kMetaLast) && (x_last - seg_x0 + 1 == nb);
+        if (whole) {
+            if (g < G) {
+                float v[32];
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    v[n] = o[n][0];
+                    v[16 + n] = o[n][1];
+                }
+                store_row(v, l_run > 0.f ? out_mul / l_run : 0.f);
+            }
+            continue;
+        }
+        // partial record of this segment: O[G][D], m[G], l[G]
+        const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
+        {
+            const int slot = (seg_x0 == A0) ? 0 : 1;
+            float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
+            if (g < G) {
+                float4* ro = reinterpret_cast<float4*>(rec + g * D + 32 * t);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    ro[i] = make_float4(o[4 * i][0], o[4 * i + 1][0], o[4 * i + 2][0], o[4 * i + 3][0]);
+                    ro[4 + i] = make_float4(o[4 * i][1], o[4 * i + 1][1], o[4 * i + 2][1], o[4 * i + 3][1]);
+                }
+                if (t == 0) {
+                    rec[G * D + g] = m_ref;
+                    rec[G * D + G + g] = l_run;
+                }
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        const int seg_blocks = x_last - seg_x0 + 1;
+        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], seg_blocks);
+        old = __shfl_sync(kFull, old, 0);
+        if (old + seg_blocks != nb) continue;
+
+        // last finisher of pair (s, h): merge its segments in stream order
+        __threadfence();
+        const int U0 = Hkv * P[s] + h * nb;
+        const int U1 = U0 + nb;
+        float Mx = -INFINITY, Ls = 0.f;
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        int wq = w, ys = A0;
+        while (ys > U0 && wq > 0) ys = split.start(--wq);
+        while (ys < U1 && wq < W) {
+            const int ye = split.start(wq + 1);
+            if (ye > ys && g < G) {  // a non-empty share holds one segment of the pair
+                const int sl = (ys >= U0) ? 0 : 1;
+                const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
+                const float mr = __ldcg(r + G * D + g);
+                const float lr = __ldcg(r + G * D + G + g);
+                const float mn = fmaxf(Mx, mr);
+                const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
+                const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
+                Ls = Ls * fo + lr * fr;
+                Mx = mn;
+                const float4* ro = reinterpret_cast<const float4*>(r + g * D + 32 * t);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 ov = __ldcg(ro + i);
+                    acc[4 * i] = acc[4 * i] * fo + ov.x * fr;
+                    acc[4 * i + 1] = acc[4 * i + 1] * fo + ov.y * fr;
+                    acc[4 * i + 2] = acc[4 * i + 2] * fo + ov.z * fr;
+                    acc[4 * i + 3] = acc[4 * i + 3] * fo + ov.w * fr;
+                }
+            }
+            ++wq;
+            ys = ye;
+        }
+        if (g < G) store_row(acc, Ls > 0.f ? out_mul / Ls : 0.f);
+    }
+}
+
+// Host-side launch for one instantiation (defined in decode_mma_*.cu).
+template <int G, int S, class KV>
+cudaError_t launch_paged_decode_mma(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,
+                                    int block, size_t smem, cudaStream_t stream) {
+    auto kern = paged_decode_mma_kernel<G, S, KV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, block, smem, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

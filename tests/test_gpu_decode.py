@@ -76,14 +76,17 @@ def test_decode_shapes(kv, q, G, D):
         assert_close(kv, to_host(st.out), ref, f"G={G} D={D} {kv} splits={ns}")
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "i8"])
 @pytest.mark.parametrize("S", [4, 8, 16, 32])
-def test_decode_block_sizes(S):
-    w = _random_workload([1, S - 1, S, S + 1, 3 * S + 2, 10 * S, 200], 8, 2, 128, S, "bf16", "bf16", seed=S)
+def test_decode_block_sizes(S, kv):
+    """Every block size, ragged last blocks; one-byte caches run on 16-token MMA tiles (S = 32: two per block,
+    S < 16: one partly filled)."""
+    w = _random_workload([1, S - 1, S, S + 1, 3 * S + 2, 10 * S, 200], 8, 2, 128, S, kv, "bf16", seed=S)
     _, _, ref = oracle_step(w)
     for ns in (0, 1, 4):
         st = _run(w, ns)
         assert st.device_error() == 0
-        assert_close("bf16", to_host(st.out), ref, f"S={S} splits={ns}")
+        assert_close(kv, to_host(st.out), ref, f"S={S} {kv} splits={ns}")
 
 
 def test_split_modes_agree_closely():
@@ -108,11 +111,13 @@ def test_empty_sequence_gives_zero_row():
         assert_close("bf16", out, ref, "empty row")
 
 
-@pytest.mark.parametrize("kv", ["f32", "bf16"])
-def test_poisoned_unused_slots_do_not_leak(kv):
-    """NaN in every slot that no sequence owns (tails of last blocks, free blocks) changes nothing."""
+@pytest.mark.parametrize("kv,D,S", [("f32", 64, 8), ("bf16", 64, 8), ("e4m3", 128, 16), ("e4m3", 128, 4),
+                                    ("i8", 128, 8), ("i8", 128, 32)])
+def test_poisoned_unused_slots_do_not_leak(kv, D, S):
+    """NaN (the largest code for INT8) in every slot that no sequence owns (tails of last blocks, free blocks)
+    changes nothing: stale rows of a partly filled tile must not reach the scores or P.V."""
     q = "f32" if kv == "f32" else "bf16"
-    w = _random_workload([13, 2, 40, 77], 8, 2, 64, 8, kv, q, seed=21, extra_blocks=12)
+    w = _random_workload([13, 2, 40, 77], 8, 2, D, S, kv, q, seed=21, extra_blocks=12)
     _, _, ref = oracle_step(w)
     clean = to_host(_run(w, 0).out)
     S = w.block_size
@@ -120,7 +125,7 @@ def test_poisoned_unused_slots_do_not_leak(kv):
     for s in range(w.num_seqs):
         for p in range(int(w.context_lens[s])):
             owned[w.block_tables[s, p // S], p % S] = True
-    nan = np.float32(np.nan) if kv == "f32" else np.uint16(0x7FC0)
+    nan = {"f32": np.float32(np.nan), "bf16": np.uint16(0x7FC0), "e4m3": np.uint8(0x7F), "i8": np.uint8(0x7F)}[kv]
     for cache in (w.k_cache, w.v_cache):
         cache[~owned] = nan
     for ns in (0, 1, 2):
