@@ -396,18 +396,18 @@ static cudaError_t dispatch_mma(int S, int G, const CUtensorMap& km, const CUten
 }
 
 // Decode over an FP8 or INT8 cache with 128-dim heads: the tensor-core form of the kernel (decode_mma.cuh).  Its
-// stages hold 128-byte swizzled K and V tiles, each starting on a 1024-byte boundary; `a` arrives with everything but
-// the shared-memory plan filled in.
+// stages hold 128-byte swizzled K and V tiles only, each starting on a 1024-byte boundary; `a` arrives with everything
+// but the shared-memory plan filled in.
 static pkv_status decode_one_byte_mma(DecodeArgs a, const pkv_cache_desc& c, int G, int num_seqs, const void* k_cache,
                                       const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
     const int S = c.block_size, Hkv = c.num_kv_heads;
     const uint32_t tile = static_cast<uint32_t>(std::max(S * 128, 1024));
     a.kv_bytes = static_cast<uint32_t>(S * 128);
-    a.q_bytes = static_cast<uint32_t>(G * 256);
-    a.stage_bytes = 2 * tile + static_cast<uint32_t>(std::max(G * 256, 1024));
+    a.q_bytes = 0;  // the query rows are read straight into registers
+    a.stage_bytes = 2 * tile;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 1023) / 1024 * 1024);
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256 - 1024;  // static shared memory, alignment slack
-    int nw = policy_warps(G, 128), depth = 0;
+    int nw = kMmaWarps, depth = 0;
     while (nw >= 1) {
         const size_t avail = budget > a.prefix_bytes ? budget - a.prefix_bytes : 0;
         const size_t per_warp_avail = avail / nw;

@@ -27,17 +27,18 @@
 
 namespace pkv {
 
-// one m16n8k16 MMA, f16 operands, fp32 accumulate; rows 8-15 of A are zero and their outputs are dropped
-__device__ __forceinline__ void mma_f16_rows8(float& c0, float& c1, uint32_t a0, uint32_t a2, uint32_t b0,
-                                              uint32_t b1) {
-    float d2, d3;
+// Warps per CTA of the tensor-core decode (at most the CUDA-core policy's count, which sizes the split-KV
+// workspace): few instructions per block leave the pipeline depth, not the warp count, as what hides latency.
+constexpr int kMmaWarps = 8;
+
+// one m16n8k16 MMA, f16 operands, fp32 accumulate in place.  The operands are whole register quads (rows 8-15 of A
+// are zero registers of the quad and rows 8-15 of C accumulate nothing of use), so no copies are needed around it.
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %10, %10};"
-        : "+f"(c0), "+f"(c1), "=f"(d2), "=f"(d3)
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-    (void)d2;
-    (void)d3;
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // two one-byte codes (low byte first in the low 16 bits of w, or the high 16 bits when HI) -> f16x2, exactly
@@ -65,11 +66,14 @@ __device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
     return r;
 }
 
-// 16 bytes at chunk c (16-byte unit, 0..7) of a 128-byte row stored with the 128-byte TMA swizzle; `row_addr` is
-// the row's shared-memory address (128-byte aligned)
-__device__ __forceinline__ uint4 lds_sw128(uint32_t row_addr, int c) {
+// Byte offset of 16-byte chunk c (0..7) of row r in a tile of 128-byte rows stored with the 128-byte TMA swizzle
+// (the tile starts on a 1024-byte boundary, so the chunk is c ^ (r & 7))
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+    return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
-    const uint32_t addr = row_addr + ((static_cast<uint32_t>(c) ^ ((row_addr >> 7) & 7u)) << 4);
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
@@ -82,22 +86,22 @@ __device__ __forceinline__ uint32_t pair_bytes(uint32_t w, uint32_t x) {
 }
 
 // Shared-memory plan of one warp stage: K tile, V tile (each S rows of 128 codes, padded to 1024 bytes so that
-// every tile starts on the 128-byte swizzle's 1024-byte period), then the G query rows (bf16).
-template <int G, int S>
+// every tile starts on the 128-byte swizzle's 1024-byte period).  The query rows do not pass through the stages:
+// each thread loads its 64 bytes of Q into registers once per segment, so every stage byte carries K or V.
+template <int S>
 struct MmaStage {
     static constexpr int kTile = S * 128 < 1024 ? 1024 : S * 128;
-    static constexpr int kQ = G * 256 < 1024 ? 1024 : G * 256;
-    static constexpr int kBytes = 2 * kTile + kQ;
+    static constexpr int kBytes = 2 * kTile;
 };
 
 template <int G, int S, class KV>
-__global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
+__global__ void __launch_bounds__(32 * kMmaWarps, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const DecodeArgs a) {
     constexpr int D = 128;
     constexpr int TS = S < 16 ? S : 16;   // tokens of a block per 16-row MMA tile
     constexpr int NT = S / TS;            // tiles per block
-    constexpr int kTile = MmaStage<G, S>::kTile;
+    constexpr int kTile = MmaStage<S>::kTile;
     static_assert(G <= 8, "query rows of one MMA tile");
 
     extern __shared__ uint8_t smem_raw[];
@@ -107,6 +111,14 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
     const int NW = blockDim.x >> 5;
     const int B = a.B, Hkv = a.Hkv;
     const int g = lane >> 2, t = lane & 3;  // fragment row (query head) and column pair
+    // this thread's operand offsets inside a K or V tile: K rows g and 8 + g, chunks 2t and 2t + 1 (head dims
+    // 32t .. 32t + 31); V rows 2t, 2t + 1, 2t + 8, 2t + 9, chunk g (head dims 16g .. 16g + 15)
+    const uint32_t ko0 = sw128_offset(g, 2 * t), ko1 = sw128_offset(g, 2 * t + 1);
+    const uint32_t ko2 = sw128_offset(8 + g, 2 * t), ko3 = sw128_offset(8 + g, 2 * t + 1);
+    const uint32_t vo0 = sw128_offset(2 * t, g), vo1 = sw128_offset(2 * t + 1, g);
+    const uint32_t vo2 = sw128_offset(2 * t + 8, g), vo3 = sw128_offset(2 * t + 9, g);
+    uint32_t zr;  // a zero the compiler cannot fold: it fills rows 8-15 of the A quads in place
+    asm volatile("mov.b32 %0, 0;" : "=r"(zr));
 
     // ---- 1. per-sequence block counts and their prefix sum (P[s] = blocks before s)
     int* P = reinterpret_cast<int*>(smem);
@@ -199,25 +211,19 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
         return m;
     };
 
-    // Issue the copies of stream index k into stage k % depth (by the lane holding the block's metadata).
-    auto issue = [&](int k, const Meta& m) {
-        const int st = static_cast<int>(k % a.depth);
-        const bool seg_start = (m.c & kMetaFirst) || (k == 0);
+    // Issue the copies of a stream index into stage st (by the lane holding the block's metadata).
+    auto issue = [&](int st, const Meta& m) {
         const bool ok = (m.c & kMetaOk) != 0;
         if (!ok) raise_error(a.err, PKV_DEVERR_BAD_BLOCK);
-        const uint32_t tx = (ok ? 2u * a.kv_bytes : 0u) + (seg_start ? a.q_bytes : 0u);
         const uint32_t bar = bars_u32 + 8 * st;
         const uint32_t dst = wreg_u32 + st * a.stage_bytes;
-        if (tx) mbar_arrive_expect_tx(bar, tx); else mbar_arrive(bar);
-        const int s = m.a >> 10, h = m.a & 1023;
         if (ok) {
+            mbar_arrive_expect_tx(bar, 2u * a.kv_bytes);
+            const int h = m.a & 1023;
             tma_load_3d(dst, &kmap, 0, h, m.b * S, bar, pol);
             tma_load_3d(dst + kTile, &vmap, 0, h, m.b * S, bar, pol);
-        }
-        if (seg_start) {
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q) +
-                                 (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G) * D * 2;
-            bulk_load(dst + 2 * kTile, src, a.q_bytes, bar);
+        } else {
+            mbar_arrive(bar);
         }
     };
 
@@ -230,11 +236,10 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
         issue(lane, cur);
     }
 
-    // Bounded wait for stage k; on timeout record the error and drain the copies still in flight (bounded).
-    auto wait_stage = [&](int k) -> bool {
-        const int st = static_cast<int>(k % a.depth);
-        if (mbar_wait_bounded(bars_u32 + 8 * st, static_cast<uint32_t>((k / a.depth) & 1), a.timeout_ns))
-            return true;
+    // Bounded wait for stream index k in stage st (phase parity ph); on timeout record the error and drain the
+    // copies still in flight (bounded).
+    auto wait_stage = [&](int k, int st, uint32_t ph) -> bool {
+        if (mbar_wait_bounded(bars_u32 + 8 * st, ph, a.timeout_ns)) return true;
         raise_error(a.err, PKV_DEVERR_TIMEOUT);
         for (int kk = k + 1; kk < k + a.depth && kk < n_blocks; ++kk)
             mbar_wait_bounded(bars_u32 + 8 * static_cast<int>(kk % a.depth),
@@ -244,11 +249,13 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
 
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
     int k = 0;
+    int st = 0;       // stage of stream index k (k % depth)
+    uint32_t ph = 0;  // its phase parity ((k / depth) & 1)
     while (k < n_blocks) {
         // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
         const int seg_x0 = A0 + k;
-        uint32_t qa[8][2];  // Q fragments per k-step (row g; dims 32t + 4ks + {0,1} and {2,3}), f16
-        float o[16][2];     // O[g][32t + n] and O[g][32t + 16 + n] for output tile n
+        uint32_t qa[8][4];  // Q fragment quads per k-step: row g, dims 32t + 4ks + {0,1} and {2,3} (f16); zero rows
+        float o[16][4];     // O[g][32t + n] and O[g][32t + 16 + n] for output tile n (and rows 8-15, unused)
         float m_ref = -INFINITY;  // running max of row g (log2 units), the same in the 4 threads of the row
         float l_run = 0.f;        // this thread's share of the running sum of row g
         int ma = 0, mc = 0, seg_first = 0;
@@ -262,31 +269,41 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
             constexpr bool M = decltype(masked)::value;
             const int lim = M ? tv : TS;
             // ---- S = Q Kᵀ: column tile 0 holds tokens 0-7, tile 1 tokens 8-15 (thread: tokens 2t, 2t+1 of each)
-            float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             {
-                const uint4 x0 = g < TS ? lds_sw128(kt + g * 128, 2 * t) : zero4;
-                const uint4 x1 = g < TS ? lds_sw128(kt + g * 128, 2 * t + 1) : zero4;
+                const uint4 x0 = g < TS ? lds128(kt + ko0) : zero4;
+                const uint4 x1 = g < TS ? lds128(kt + ko1) : zero4;
                 const uint32_t kw0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float e0[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-steps: a second accumulation chain
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_f16_rows8(s0a, s0b, qa[ks][0], qa[ks][1], codes2_to_f16x2<KV, false>(kw0[ks]),
-                                  codes2_to_f16x2<KV, true>(kw0[ks]));
+                for (int ks = 0; ks < 8; ks += 2) {
+                    mma_16816(s0, qa[ks], codes2_to_f16x2<KV, false>(kw0[ks]), codes2_to_f16x2<KV, true>(kw0[ks]));
+                    mma_16816(e0, qa[ks + 1], codes2_to_f16x2<KV, false>(kw0[ks + 1]),
+                              codes2_to_f16x2<KV, true>(kw0[ks + 1]));
+                }
+                s0[0] += e0[0];
+                s0[1] += e0[1];
                 if constexpr (TS > 8) {
-                    const uint4 y0 = lds_sw128(kt + (8 + g) * 128, 2 * t);
-                    const uint4 y1 = lds_sw128(kt + (8 + g) * 128, 2 * t + 1);
+                    const uint4 y0 = lds128(kt + ko2);
+                    const uint4 y1 = lds128(kt + ko3);
                     const uint32_t kw1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+                    float e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_f16_rows8(s1a, s1b, qa[ks][0], qa[ks][1], codes2_to_f16x2<KV, false>(kw1[ks]),
-                                      codes2_to_f16x2<KV, true>(kw1[ks]));
+                    for (int ks = 0; ks < 8; ks += 2) {
+                        mma_16816(s1, qa[ks], codes2_to_f16x2<KV, false>(kw1[ks]), codes2_to_f16x2<KV, true>(kw1[ks]));
+                        mma_16816(e1, qa[ks + 1], codes2_to_f16x2<KV, false>(kw1[ks + 1]),
+                                  codes2_to_f16x2<KV, true>(kw1[ks + 1]));
+                    }
+                    s1[0] += e1[0];
+                    s1[1] += e1[1];
                 }
             }
             // ---- online softmax of row g over the tile's tokens
             const int t0 = 2 * t, t2 = 8 + 2 * t;
-            float sc0 = (t0 < lim) ? s0a * qm : -INFINITY;
-            float sc1 = (t0 + 1 < lim) ? s0b * qm : -INFINITY;
-            float sc2 = (t2 < lim) ? s1a * qm : -INFINITY;
-            float sc3 = (t2 + 1 < lim) ? s1b * qm : -INFINITY;
+            float sc0 = (t0 < lim) ? s0[0] * qm : -INFINITY;
+            float sc1 = (t0 + 1 < lim) ? s0[1] * qm : -INFINITY;
+            float sc2 = (t2 < lim) ? s1[0] * qm : -INFINITY;
+            float sc3 = (t2 + 1 < lim) ? s1[1] * qm : -INFINITY;
             float mb = fmaxf(fmaxf(sc0, sc1), fmaxf(sc2, sc3));
             mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
             mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
@@ -299,33 +316,29 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
                     o[n][0] *= alpha;
-                    o[n][1] *= alpha;
+                    o[n][1] *= alpha;  // rows 8-15 (elements 2, 3) carry nothing of use
                 }
             }
             const float p0 = ex2_approx(sc0 - m_ref), p1 = ex2_approx(sc1 - m_ref);
             const float p2 = ex2_approx(sc2 - m_ref), p3 = ex2_approx(sc3 - m_ref);
             l_run += (p0 + p1) + (p2 + p3);
-            const uint32_t pa0 = f16x2_pack(p0, p1), pa2 = f16x2_pack(p2, p3);
+            const uint32_t pa[4] = {f16x2_pack(p0, p1), zr, f16x2_pack(p2, p3), zr};
             // ---- O += P V: thread (g, t) supplies V[2t, 2t+1, 2t+8, 2t+9][16g .. 16g+15]; rows past the valid
             // tokens are zero (stale rows may hold anything, and 0 * NaN would reach O)
-            const uint4 v0 = (t0 < lim) ? lds_sw128(vt + t0 * 128, g) : zero4;
-            const uint4 v1 = (t0 + 1 < lim) ? lds_sw128(vt + (t0 + 1) * 128, g) : zero4;
-            const uint4 v2 = (t2 < lim) ? lds_sw128(vt + t2 * 128, g) : zero4;
-            const uint4 v3 = (t2 + 1 < lim) ? lds_sw128(vt + (t2 + 1) * 128, g) : zero4;
+            const uint4 v0 = (t0 < lim) ? lds128(vt + vo0) : zero4;
+            const uint4 v1 = (t0 + 1 < lim) ? lds128(vt + vo1) : zero4;
+            const uint4 v2 = (t2 < lim) ? lds128(vt + vo2) : zero4;
+            const uint4 v3 = (t2 + 1 < lim) ? lds128(vt + vo3) : zero4;
             const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
             const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
                 const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
-                mma_f16_rows8(o[4 * j][0], o[4 * j][1], pa0, pa2, codes2_to_f16x2<KV, false>(lo01),
-                              codes2_to_f16x2<KV, false>(lo23));
-                mma_f16_rows8(o[4 * j + 1][0], o[4 * j + 1][1], pa0, pa2, codes2_to_f16x2<KV, true>(lo01),
-                              codes2_to_f16x2<KV, true>(lo23));
-                mma_f16_rows8(o[4 * j + 2][0], o[4 * j + 2][1], pa0, pa2, codes2_to_f16x2<KV, false>(hi01),
-                              codes2_to_f16x2<KV, false>(hi23));
-                mma_f16_rows8(o[4 * j + 3][0], o[4 * j + 3][1], pa0, pa2, codes2_to_f16x2<KV, true>(hi01),
-                              codes2_to_f16x2<KV, true>(hi23));
+                mma_16816(o[4 * j], pa, codes2_to_f16x2<KV, false>(lo01), codes2_to_f16x2<KV, false>(lo23));
+                mma_16816(o[4 * j + 1], pa, codes2_to_f16x2<KV, true>(lo01), codes2_to_f16x2<KV, true>(lo23));
+                mma_16816(o[4 * j + 2], pa, codes2_to_f16x2<KV, false>(hi01), codes2_to_f16x2<KV, false>(hi23));
+                mma_16816(o[4 * j + 3], pa, codes2_to_f16x2<KV, true>(hi01), codes2_to_f16x2<KV, true>(hi23));
             }
         };
 
@@ -339,34 +352,32 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
             const int src = x - wbase;
             ma = __shfl_sync(kFull, cur.a, src);
             mc = __shfl_sync(kFull, cur.c, src);
-            if (!wait_stage(k)) return;
-            const uint32_t sp = wreg_u32 + static_cast<uint32_t>(k % a.depth) * a.stage_bytes;
+            if (!wait_stage(k, st, ph)) return;
+            const uint32_t sp = wreg_u32 + static_cast<uint32_t>(st) * a.stage_bytes;
             if (first) {
-                // Q of this (s, h): row g, dims 32t .. 32t+31 (bf16 -> f16 in the permuted k order)
+                // Q of this (s, h): row g, dims 32t .. 32t+31, from global memory (bf16 -> f16 in the permuted k order)
                 seg_first = mc & kMetaFirst;
                 qm = a.k_head ? a.q_base * __ldg(a.k_head + (ma & 1023)) : a.q_mul;
+                const uint4* qrow = reinterpret_cast<const uint4*>(
+                    reinterpret_cast<const uint8_t*>(a.q) +
+                    ((static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(ma & 1023) * G + g) * D + 32 * t) * 2);
                 bool in_range = true;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    uint4 w4 = zero4;
-                    if (g < G) {
-                        const uint32_t qaddr = sp + 2 * kTile + g * 256 + t * 64 + i * 16;
-                        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(w4.x), "=r"(w4.y), "=r"(w4.z), "=r"(w4.w)
-                                     : "r"(qaddr));
-                    }
+                    const uint4 w4 = g < G ? __ldg(qrow + i) : zero4;
                     const float2 f0 = bf16x2_to_float2(w4.x), f1 = bf16x2_to_float2(w4.y);
                     const float2 f2 = bf16x2_to_float2(w4.z), f3 = bf16x2_to_float2(w4.w);
                     in_range = in_range && fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))) < 65520.f &&
                                fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))) < 65520.f;
                     qa[2 * i][0] = f16x2_pack(f0.x, f0.y);
-                    qa[2 * i][1] = f16x2_pack(f1.x, f1.y);
+                    qa[2 * i][2] = f16x2_pack(f1.x, f1.y);
                     qa[2 * i + 1][0] = f16x2_pack(f2.x, f2.y);
-                    qa[2 * i + 1][1] = f16x2_pack(f3.x, f3.y);
+                    qa[2 * i + 1][2] = f16x2_pack(f3.x, f3.y);
+                    qa[2 * i][1] = qa[2 * i][3] = qa[2 * i + 1][1] = qa[2 * i + 1][3] = zr;
                 }
                 if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
 #pragma unroll
-                for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = 0.f;
+                for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
                 first = false;
             }
             if (mc & kMetaOk) {
@@ -388,11 +399,15 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, 128>::warps, 1)
                 const int sn = A0 + kn - wbase;
                 if (lane == (sn & 31)) {
                     fence_proxy_async_smem();
-                    issue(kn, sn < 32 ? cur : nxt);
+                    issue(st, sn < 32 ? cur : nxt);
                 }
             }
             const bool last = (mc & kMetaLast) != 0 || x == A1 - 1;
             ++k;
+            if (++st == a.depth) {
+                st = 0;
+                ph ^= 1u;
+            }
             if (last) {
                 x_last = x;
                 break;
