@@ -101,9 +101,11 @@ DECODE_SOURCES = ("decode.cuh", "pkv_device.cuh", "decode_bf16_s16.cu")
 
 def decode_kernel(w) -> tuple[str, tuple]:
     """The decode kernel a workload runs on, and the sources its profile digest covers: FP8 / INT8 caches with
-    128-dim heads take the tensor-core form, everything else the CUDA-core form."""
-    if w.kv_dtype in ("e4m3", "i8") and w.head_dim == 128:
-        tag = "fp8" if w.kv_dtype == "e4m3" else "i8"
+    128-dim heads, and bf16 caches of 128-dim heads in GQA groups of 8, take the tensor-core form, everything else
+    the CUDA-core form."""
+    G = w.num_q_heads // w.num_kv_heads
+    if w.head_dim == 128 and (w.kv_dtype in ("e4m3", "i8") or (w.kv_dtype == "bf16" and G >= 8)):
+        tag = {"e4m3": "fp8", "i8": "i8", "bf16": "bf16"}[w.kv_dtype]
         return "paged_decode_mma_kernel", ("decode_mma.cuh", "decode.cuh", "pkv_device.cuh",
                                            f"decode_mma_{tag}_s{w.block_size}.cu")
     return "paged_decode_kernel", DECODE_SOURCES

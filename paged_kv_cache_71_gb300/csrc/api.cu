@@ -395,14 +395,21 @@ static cudaError_t dispatch_mma(int S, int G, const CUtensorMap& km, const CUten
 #undef PKV_MMA_G
 }
 
-// Decode over an FP8 or INT8 cache with 128-dim heads: the tensor-core form of the kernel (decode_mma.cuh).  Its
-// stages hold 128-byte swizzled K and V tiles only, each starting on a 1024-byte boundary; `a` arrives with everything
-// but the shared-memory plan filled in.
-static pkv_status decode_one_byte_mma(DecodeArgs a, const pkv_cache_desc& c, int G, int num_seqs, const void* k_cache,
-                                      const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
+// Smallest GQA group that a bf16 cache decodes on the tensor-core form; below it the CUDA cores keep up with HBM
+// (measured on GB300), at and above it their fp32 FMA issue is the limit.
+#ifndef PKV_BF16_MMA_MIN_G
+#define PKV_BF16_MMA_MIN_G 8
+#endif
+
+// Decode on the tensor-core form of the kernel (decode_mma.cuh): FP8 / INT8 caches, and bf16 caches from
+// PKV_BF16_MMA_MIN_G up, 128-dim heads.  Its stages hold 128-byte swizzled K and V tiles only (two 64-dim halves per
+// bf16 row), each half starting on a 1024-byte boundary; `a` arrives with everything but the shared-memory plan.
+static pkv_status decode_tensor_core(DecodeArgs a, const pkv_cache_desc& c, int G, int num_seqs, const void* k_cache,
+                                     const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
     const int S = c.block_size, Hkv = c.num_kv_heads;
-    const uint32_t tile = static_cast<uint32_t>(std::max(S * 128, 1024));
-    a.kv_bytes = static_cast<uint32_t>(S * 128);
+    const bool b16 = c.dtype == PKV_BF16;
+    const uint32_t tile = static_cast<uint32_t>((b16 ? 2 : 1) * std::max(S * 128, 1024));
+    a.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));
     a.q_bytes = 0;  // the query rows are read straight into registers
     a.stage_bytes = 2 * tile;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 1023) / 1024 * 1024);
@@ -424,14 +431,15 @@ static pkv_status decode_one_byte_mma(DecodeArgs a, const pkv_cache_desc& c, int
     const uint64_t rows = static_cast<uint64_t>(c.num_blocks) * S;
     CUtensorMap km, vm;
     pkv_status st;
-    if ((st = tensor_map_sw128(&km, k_cache, true, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
-    if ((st = tensor_map_sw128(&vm, v_cache, true, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&km, k_cache, !b16, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, !b16, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
     if (a.tickets) {
         cudaError_t e = cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(num_seqs) * Hkv * 4, s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing split-KV counters");
     }
-    const cudaError_t e = c.dtype == PKV_FP8_E4M3 ? dispatch_mma<KvE4M3>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
-                                                  : dispatch_mma<KvI8>(S, G, km, vm, a, di.sms, nw * 32, smem, s);
+    const cudaError_t e = b16                       ? dispatch_mma<KvBF16>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
+                          : c.dtype == PKV_FP8_E4M3 ? dispatch_mma<KvE4M3>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
+                                                    : dispatch_mma<KvI8>(S, G, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
     return PKV_OK;
 }
@@ -552,8 +560,8 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
     a.timeout_ns = 2000000000ull;
-    if (narrow(cache->dtype) && D == 128)
-        return decode_one_byte_mma(a, *cache, G, num_seqs, k_cache, v_cache, di, static_cast<cudaStream_t>(stream));
+    if (D == 128 && (narrow(cache->dtype) || (cache->dtype == PKV_BF16 && G >= PKV_BF16_MMA_MIN_G)))
+        return decode_tensor_core(a, *cache, G, num_seqs, k_cache, v_cache, di, static_cast<cudaStream_t>(stream));
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
     int nw = policy_warps(G, D), depth = 0;
     while (nw >= 1) {

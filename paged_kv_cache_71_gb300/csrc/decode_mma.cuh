@@ -31,14 +31,23 @@ namespace pkv {
 // workspace): few instructions per block leave the pipeline depth, not the warp count, as what hides latency.
 constexpr int kMmaWarps = 8;
 
-// one m16n8k16 MMA, f16 operands, fp32 accumulate in place.  The operands are whole register quads (rows 8-15 of A
-// are zero registers of the quad and rows 8-15 of C accumulate nothing of use), so no copies are needed around it.
+// one m16n8k16 MMA, f16 (or bf16: B16) operands, fp32 accumulate in place.  The operands are whole register quads
+// (rows 8-15 of A are zero registers of the quad and rows 8-15 of C accumulate nothing of use), so no copies are
+// needed around it.
+template <bool B16>
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    if constexpr (B16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // two one-byte codes (low byte first in the low 16 bits of w, or the high 16 bits when HI) -> f16x2, exactly
@@ -60,9 +69,13 @@ __device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t w) {
     }
 }
 
-__device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
+template <bool B16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    if constexpr (B16)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
@@ -85,12 +98,14 @@ __device__ __forceinline__ uint32_t pair_bytes(uint32_t w, uint32_t x) {
     return __byte_perm(w, x, B == 0 ? 0x5140u : 0x7362u);
 }
 
-// Shared-memory plan of one warp stage: K tile, V tile (each S rows of 128 codes, padded to 1024 bytes so that
-// every tile starts on the 128-byte swizzle's 1024-byte period).  The query rows do not pass through the stages:
-// each thread loads its 64 bytes of Q into registers once per segment, so every stage byte carries K or V.
-template <int S>
+// Shared-memory plan of one warp stage: K tile, V tile.  A tile is one half (one-byte codes: S rows of 128 codes)
+// or two halves (bf16: head dims 0-63, then 64-127, S rows of 128 bytes each), every half padded to 1024 bytes so
+// that it starts on the 128-byte swizzle's 1024-byte period.  The query rows do not pass through the stages: each
+// thread loads its 64 bytes of Q into registers once per segment, so every stage byte carries K or V.
+template <int S, int ES>
 struct MmaStage {
-    static constexpr int kTile = S * 128 < 1024 ? 1024 : S * 128;
+    static constexpr int kHalf = S * 128 < 1024 ? 1024 : S * 128;
+    static constexpr int kTile = (ES == 2 ? 2 : 1) * kHalf;
     static constexpr int kBytes = 2 * kTile;
 };
 
@@ -101,8 +116,10 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     constexpr int D = 128;
     constexpr int TS = S < 16 ? S : 16;   // tokens of a block per 16-row MMA tile
     constexpr int NT = S / TS;            // tiles per block
-    constexpr int kTile = MmaStage<S>::kTile;
+    constexpr bool B16 = KV::es == 2;  // bf16 cache: bf16 MMAs on the cached values as they are
+    constexpr int kHalf = MmaStage<S, KV::es>::kHalf, kTile = MmaStage<S, KV::es>::kTile;
     static_assert(G <= 8, "query rows of one MMA tile");
+    static_assert(KV::es <= 2, "one-byte or bf16 caches");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -111,12 +128,12 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     const int NW = blockDim.x >> 5;
     const int B = a.B, Hkv = a.Hkv;
     const int g = lane >> 2, t = lane & 3;  // fragment row (query head) and column pair
-    // this thread's operand offsets inside a K or V tile: K rows g and 8 + g, chunks 2t and 2t + 1 (head dims
-    // 32t .. 32t + 31); V rows 2t, 2t + 1, 2t + 8, 2t + 9, chunk g (head dims 16g .. 16g + 15)
-    const uint32_t ko0 = sw128_offset(g, 2 * t), ko1 = sw128_offset(g, 2 * t + 1);
-    const uint32_t ko2 = sw128_offset(8 + g, 2 * t), ko3 = sw128_offset(8 + g, 2 * t + 1);
-    const uint32_t vo0 = sw128_offset(2 * t, g), vo1 = sw128_offset(2 * t + 1, g);
-    const uint32_t vo2 = sw128_offset(2 * t + 8, g), vo3 = sw128_offset(2 * t + 9, g);
+    // this thread's operand offsets inside a K or V half: K rows g and 8 + g (1024 bytes further, same swizzle),
+    // chunks 2t and 2t + 1; V rows 2t, 2t + 1 and 2t + 8, 2t + 9 (1024 bytes further), chunk g.  One-byte codes:
+    // the K chunks are head dims 32t .. 32t + 31, the V chunk dims 16g .. 16g + 15.  bf16: the same chunks of both
+    // halves, K dims 16t .. 16t + 15 and 64 + 16t .. 64 + 16t + 15, V dims 8g .. 8g + 7 and 64 + 8g .. 64 + 8g + 7.
+    const uint32_t kb0 = sw128_offset(g, 2 * t), kb1 = sw128_offset(g, 2 * t + 1);
+    const uint32_t vb0 = sw128_offset(2 * t, g), vb1 = sw128_offset(2 * t + 1, g);
     uint32_t zr;  // a zero the compiler cannot fold: it fills rows 8-15 of the A quads in place
     asm volatile("mov.b32 %0, 0;" : "=r"(zr));
 
@@ -220,8 +237,11 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         if (ok) {
             mbar_arrive_expect_tx(bar, 2u * a.kv_bytes);
             const int h = m.a & 1023;
-            tma_load_3d(dst, &kmap, 0, h, m.b * S, bar, pol);
-            tma_load_3d(dst + kTile, &vmap, 0, h, m.b * S, bar, pol);
+#pragma unroll
+            for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
+                tma_load_3d(dst + hf * kHalf, &kmap, hf * 64, h, m.b * S, bar, pol);
+                tma_load_3d(dst + kTile + hf * kHalf, &vmap, hf * 64, h, m.b * S, bar, pol);
+            }
         } else {
             mbar_arrive(bar);
         }
@@ -268,31 +288,51 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         auto tile = [&](auto masked, uint32_t kt, uint32_t vt, int tv) {
             constexpr bool M = decltype(masked)::value;
             const int lim = M ? tv : TS;
+            // K operand of one token row (at byte offset ro in each half of the tile): registers b0, b1 per k-step
+            auto k_frags = [&](uint32_t ro, bool present, uint32_t (&kf)[8][2]) {
+                if constexpr (B16) {
+                    const uint4 x0 = present ? lds128(kt + ro + kb0) : zero4;
+                    const uint4 x1 = present ? lds128(kt + ro + kb1) : zero4;
+                    const uint4 x2 = present ? lds128(kt + kHalf + ro + kb0) : zero4;
+                    const uint4 x3 = present ? lds128(kt + kHalf + ro + kb1) : zero4;
+                    const uint32_t w[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                            x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        kf[ks][0] = w[2 * ks];
+                        kf[ks][1] = w[2 * ks + 1];
+                    }
+                } else {
+                    const uint4 x0 = present ? lds128(kt + ro + kb0) : zero4;
+                    const uint4 x1 = present ? lds128(kt + ro + kb1) : zero4;
+                    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        kf[ks][0] = codes2_to_f16x2<KV, false>(w[ks]);
+                        kf[ks][1] = codes2_to_f16x2<KV, true>(w[ks]);
+                    }
+                }
+            };
             // ---- S = Q Kᵀ: column tile 0 holds tokens 0-7, tile 1 tokens 8-15 (thread: tokens 2t, 2t+1 of each)
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
             {
-                const uint4 x0 = g < TS ? lds128(kt + ko0) : zero4;
-                const uint4 x1 = g < TS ? lds128(kt + ko1) : zero4;
-                const uint32_t kw0[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                uint32_t kf[8][2];
+                k_frags(0u, g < TS, kf);
                 float e0[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-steps: a second accumulation chain
 #pragma unroll
                 for (int ks = 0; ks < 8; ks += 2) {
-                    mma_16816(s0, qa[ks], codes2_to_f16x2<KV, false>(kw0[ks]), codes2_to_f16x2<KV, true>(kw0[ks]));
-                    mma_16816(e0, qa[ks + 1], codes2_to_f16x2<KV, false>(kw0[ks + 1]),
-                              codes2_to_f16x2<KV, true>(kw0[ks + 1]));
+                    mma_16816<B16>(s0, qa[ks], kf[ks][0], kf[ks][1]);
+                    mma_16816<B16>(e0, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
                 }
                 s0[0] += e0[0];
                 s0[1] += e0[1];
                 if constexpr (TS > 8) {
-                    const uint4 y0 = lds128(kt + ko2);
-                    const uint4 y1 = lds128(kt + ko3);
-                    const uint32_t kw1[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+                    k_frags(1024u, true, kf);
                     float e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int ks = 0; ks < 8; ks += 2) {
-                        mma_16816(s1, qa[ks], codes2_to_f16x2<KV, false>(kw1[ks]), codes2_to_f16x2<KV, true>(kw1[ks]));
-                        mma_16816(e1, qa[ks + 1], codes2_to_f16x2<KV, false>(kw1[ks + 1]),
-                                  codes2_to_f16x2<KV, true>(kw1[ks + 1]));
+                        mma_16816<B16>(s1, qa[ks], kf[ks][0], kf[ks][1]);
+                        mma_16816<B16>(e1, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
                     }
                     s1[0] += e1[0];
                     s1[1] += e1[1];
@@ -322,23 +362,36 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
             const float p0 = ex2_approx(sc0 - m_ref), p1 = ex2_approx(sc1 - m_ref);
             const float p2 = ex2_approx(sc2 - m_ref), p3 = ex2_approx(sc3 - m_ref);
             l_run += (p0 + p1) + (p2 + p3);
-            const uint32_t pa[4] = {f16x2_pack(p0, p1), zr, f16x2_pack(p2, p3), zr};
-            // ---- O += P V: thread (g, t) supplies V[2t, 2t+1, 2t+8, 2t+9][16g .. 16g+15]; rows past the valid
+            const uint32_t pa[4] = {pack2<B16>(p0, p1), zr, pack2<B16>(p2, p3), zr};
+            // ---- O += P V: thread (g, t) supplies V rows 2t, 2t+1, 2t+8, 2t+9 of its chunk(s); rows past the valid
             // tokens are zero (stale rows may hold anything, and 0 * NaN would reach O)
-            const uint4 v0 = (t0 < lim) ? lds128(vt + vo0) : zero4;
-            const uint4 v1 = (t0 + 1 < lim) ? lds128(vt + vo1) : zero4;
-            const uint4 v2 = (t2 < lim) ? lds128(vt + vo2) : zero4;
-            const uint4 v3 = (t2 + 1 < lim) ? lds128(vt + vo3) : zero4;
-            const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
-            const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
-                const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
-                mma_16816(o[4 * j], pa, codes2_to_f16x2<KV, false>(lo01), codes2_to_f16x2<KV, false>(lo23));
-                mma_16816(o[4 * j + 1], pa, codes2_to_f16x2<KV, true>(lo01), codes2_to_f16x2<KV, true>(lo23));
-                mma_16816(o[4 * j + 2], pa, codes2_to_f16x2<KV, false>(hi01), codes2_to_f16x2<KV, false>(hi23));
-                mma_16816(o[4 * j + 3], pa, codes2_to_f16x2<KV, true>(hi01), codes2_to_f16x2<KV, true>(hi23));
+            for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
+                const uint32_t vh = vt + hf * kHalf;
+                const uint4 v0 = (t0 < lim) ? lds128(vh + vb0) : zero4;
+                const uint4 v1 = (t0 + 1 < lim) ? lds128(vh + vb1) : zero4;
+                const uint4 v2 = (t2 < lim) ? lds128(vh + 1024 + vb0) : zero4;
+                const uint4 v3 = (t2 + 1 < lim) ? lds128(vh + 1024 + vb1) : zero4;
+                const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+                const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if constexpr (B16) {
+                        // word j holds dims 2j, 2j+1 of the chunk: output tiles 8 hf + 2j and 8 hf + 2j + 1
+                        mma_16816<true>(o[8 * hf + 2 * j], pa, __byte_perm(va[j], vb[j], 0x5410u),
+                                        __byte_perm(vc[j], vd[j], 0x5410u));
+                        mma_16816<true>(o[8 * hf + 2 * j + 1], pa, __byte_perm(va[j], vb[j], 0x7632u),
+                                        __byte_perm(vc[j], vd[j], 0x7632u));
+                    } else {
+                        // word j holds dims 4j .. 4j+3 of the chunk: output tiles 4j .. 4j+3
+                        const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
+                        const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
+                        mma_16816<false>(o[4 * j], pa, codes2_to_f16x2<KV, false>(lo01), codes2_to_f16x2<KV, false>(lo23));
+                        mma_16816<false>(o[4 * j + 1], pa, codes2_to_f16x2<KV, true>(lo01), codes2_to_f16x2<KV, true>(lo23));
+                        mma_16816<false>(o[4 * j + 2], pa, codes2_to_f16x2<KV, false>(hi01), codes2_to_f16x2<KV, false>(hi23));
+                        mma_16816<false>(o[4 * j + 3], pa, codes2_to_f16x2<KV, true>(hi01), codes2_to_f16x2<KV, true>(hi23));
+                    }
+                }
             }
         };
 
@@ -355,24 +408,35 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
             if (!wait_stage(k, st, ph)) return;
             const uint32_t sp = wreg_u32 + static_cast<uint32_t>(st) * a.stage_bytes;
             if (first) {
-                // Q of this (s, h): row g, dims 32t .. 32t+31, from global memory (bf16 -> f16 in the permuted k order)
+                // Q of this (s, h) from global memory: row g, the head dims this thread's K operand holds, in the
+                // same permuted k order (one-byte caches: dims 32t .. 32t+31, bf16 -> f16; bf16 caches: dims
+                // 16t .. 16t+15 and 64+16t .. 64+16t+15 as they are)
                 seg_first = mc & kMetaFirst;
                 qm = a.k_head ? a.q_base * __ldg(a.k_head + (ma & 1023)) : a.q_mul;
                 const uint4* qrow = reinterpret_cast<const uint4*>(
                     reinterpret_cast<const uint8_t*>(a.q) +
-                    ((static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(ma & 1023) * G + g) * D + 32 * t) * 2);
+                    (static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(ma & 1023) * G + g) * D * 2);
                 bool in_range = true;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 w4 = g < G ? __ldg(qrow + i) : zero4;
+                    const int qi = B16 ? (i < 2 ? 2 * t + i : 8 + 2 * t + i - 2) : 4 * t + i;  // 16-byte units
+                    const uint4 w4 = g < G ? __ldg(qrow + qi) : zero4;
+                    if constexpr (B16) {
+                        qa[2 * i][0] = w4.x;
+                        qa[2 * i][2] = w4.y;
+                        qa[2 * i + 1][0] = w4.z;
+                        qa[2 * i + 1][2] = w4.w;
+                        qa[2 * i][1] = qa[2 * i][3] = qa[2 * i + 1][1] = qa[2 * i + 1][3] = zr;
+                        continue;
+                    }
                     const float2 f0 = bf16x2_to_float2(w4.x), f1 = bf16x2_to_float2(w4.y);
                     const float2 f2 = bf16x2_to_float2(w4.z), f3 = bf16x2_to_float2(w4.w);
                     in_range = in_range && fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))) < 65520.f &&
                                fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))) < 65520.f;
-                    qa[2 * i][0] = f16x2_pack(f0.x, f0.y);
-                    qa[2 * i][2] = f16x2_pack(f1.x, f1.y);
-                    qa[2 * i + 1][0] = f16x2_pack(f2.x, f2.y);
-                    qa[2 * i + 1][2] = f16x2_pack(f3.x, f3.y);
+                    qa[2 * i][0] = pack2<false>(f0.x, f0.y);
+                    qa[2 * i][2] = pack2<false>(f1.x, f1.y);
+                    qa[2 * i + 1][0] = pack2<false>(f2.x, f2.y);
+                    qa[2 * i + 1][2] = pack2<false>(f3.x, f3.y);
                     qa[2 * i][1] = qa[2 * i][3] = qa[2 * i + 1][1] = qa[2 * i + 1][3] = zr;
                 }
                 if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
@@ -420,42 +484,59 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         const int s = ma >> 10, h = ma & 1023;
         const int nb = P[s + 1] - P[s];
         const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.o_mul;
-        auto store_row = [&](const float (&v)[32], float inv) {  // out[s][h G + g][32t .. 32t+31], bf16
+        // the 32 output dims of thread (g, t), in runs of 16 contiguous dims: one-byte caches 32t .. 32t+31; bf16
+        // caches 16t .. 16t+15 and 64+16t .. 64+16t+15 (output tile n, column 2t / 2t+1 is dim 8 (2t) + n / 8 (2t+1)
+        // + n for n < 8, and 64 + the same for tile 8 + n)
+        auto dim_of = [&](int i) { return B16 ? (i < 16 ? 16 * t + i : 64 + 16 * t + i - 16) : 32 * t + i; };
+        float v[32];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            if constexpr (B16) {
+                v[n] = o[n][0];
+                v[8 + n] = o[n][1];
+                v[16 + n] = o[8 + n][0];
+                v[24 + n] = o[8 + n][1];
+            } else {
+                v[n] = o[n][0];
+                v[8 + n] = o[8 + n][0];
+                v[16 + n] = o[n][1];
+                v[24 + n] = o[8 + n][1];
+            }
+        }
+        auto store_row = [&](const float (&x)[32], float inv) {  // out[s][h G + g][dim_of(i)], bf16
             uint32_t wv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                wv[i] = static_cast<uint32_t>(float_to_bf16_bits(v[2 * i] * inv)) |
-                        (static_cast<uint32_t>(float_to_bf16_bits(v[2 * i + 1] * inv)) << 16);
-            uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) +
-                                                   ((static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) *
-                                                        D + 32 * t) * 2);
+                wv[i] = static_cast<uint32_t>(float_to_bf16_bits(x[2 * i] * inv)) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(x[2 * i + 1] * inv)) << 16);
+            uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                            (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * 2;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) orow[i] = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(orow + dim_of(8 * i) * 2) =
+                    make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
         };
         const bool whole = seg_first && (mc & kMetaLast) && (x_last - seg_x0 + 1 == nb);
         if (whole) {
-            if (g < G) {
-                float v[32];
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    v[n] = o[n][0];
-                    v[16 + n] = o[n][1];
-                }
-                store_row(v, l_run > 0.f ? out_mul / l_run : 0.f);
-            }
+            if (g < G) store_row(v, l_run > 0.f ? out_mul / l_run : 0.f);
             continue;
         }
-        // partial record of this segment: O[G][D], m[G], l[G]
+        // partial record of this segment: O[G][D], m[G], l[G].  A record is G * (D + 2) floats, so records are
+        // 16-byte aligned for even G and only 8-byte aligned for G = 1: the O runs move as float4 or float2 pairs.
         const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
         {
             const int slot = (seg_x0 == A0) ? 0 : 1;
             float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
             if (g < G) {
-                float4* ro = reinterpret_cast<float4*>(rec + g * D + 32 * t);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    ro[i] = make_float4(o[4 * i][0], o[4 * i + 1][0], o[4 * i + 2][0], o[4 * i + 3][0]);
-                    ro[4 + i] = make_float4(o[4 * i][1], o[4 * i + 1][1], o[4 * i + 2][1], o[4 * i + 3][1]);
+                for (int i = 0; i < 8; ++i) {
+                    float* dst = rec + g * D + dim_of(4 * i);
+                    if constexpr (G % 2 == 0) {
+                        *reinterpret_cast<float4*>(dst) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else {
+                        reinterpret_cast<float2*>(dst)[0] = make_float2(v[4 * i], v[4 * i + 1]);
+                        reinterpret_cast<float2*>(dst)[1] = make_float2(v[4 * i + 2], v[4 * i + 3]);
+                    }
                 }
                 if (t == 0) {
                     rec[G * D + g] = m_ref;
@@ -493,10 +574,16 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                 const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
                 Ls = Ls * fo + lr * fr;
                 Mx = mn;
-                const float4* ro = reinterpret_cast<const float4*>(r + g * D + 32 * t);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const float4 ov = __ldcg(ro + i);
+                    float4 ov;
+                    if constexpr (G % 2 == 0) {
+                        ov = __ldcg(reinterpret_cast<const float4*>(r + g * D + dim_of(4 * i)));
+                    } else {
+                        const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + g * D + dim_of(4 * i)));
+                        const float2 o23 = __ldcg(reinterpret_cast<const float2*>(r + g * D + dim_of(4 * i)) + 1);
+                        ov = make_float4(o01.x, o01.y, o23.x, o23.y);
+                    }
                     acc[4 * i] = acc[4 * i] * fo + ov.x * fr;
                     acc[4 * i + 1] = acc[4 * i + 1] * fo + ov.y * fr;
                     acc[4 * i + 2] = acc[4 * i + 2] * fo + ov.z * fr;

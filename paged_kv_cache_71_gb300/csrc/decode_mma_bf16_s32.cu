@@ -1,0 +1,16 @@
+// decode_mma_bf16_s32.cu -- tensor-core decode instantiations for a bf16 K/V cache (128-dim heads, bf16 queries),
+// block size 32.  (One file per cache dtype and block size, so that the instantiations compile in parallel.)
+#include "decode_mma.cuh"
+
+namespace pkv {
+
+#define PKV_INST(G_)                                                                                        \
+    template cudaError_t launch_paged_decode_mma<G_, 32, KvBF16>(const CUtensorMap&, const CUtensorMap&,    \
+                                                              const DecodeArgs&, int, int, size_t, cudaStream_t);
+PKV_INST(1)
+PKV_INST(2)
+PKV_INST(4)
+PKV_INST(8)
+#undef PKV_INST
+
+}  // namespace pkv

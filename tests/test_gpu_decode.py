@@ -76,17 +76,29 @@ def test_decode_shapes(kv, q, G, D):
         assert_close(kv, to_host(st.out), ref, f"G={G} D={D} {kv} splits={ns}")
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3", "i8"])
+@pytest.mark.parametrize("kv,G", [("bf16", 4), ("bf16", 8), ("e4m3", 4), ("i8", 8)])
 @pytest.mark.parametrize("S", [4, 8, 16, 32])
-def test_decode_block_sizes(S, kv):
-    """Every block size, ragged last blocks; one-byte caches run on 16-token MMA tiles (S = 32: two per block,
-    S < 16: one partly filled)."""
-    w = _random_workload([1, S - 1, S, S + 1, 3 * S + 2, 10 * S, 200], 8, 2, 128, S, kv, "bf16", seed=S)
+def test_decode_block_sizes(S, kv, G):
+    """Every block size, ragged last blocks; the tensor-core form (one-byte caches, bf16 at G = 8) runs on 16-token
+    MMA tiles (S = 32: two per block, S < 16: one partly filled)."""
+    w = _random_workload([1, S - 1, S, S + 1, 3 * S + 2, 10 * S, 200], 2 * G, 2, 128, S, kv, "bf16", seed=S + G)
     _, _, ref = oracle_step(w)
     for ns in (0, 1, 4):
         st = _run(w, ns)
         assert st.device_error() == 0
         assert_close(kv, to_host(st.out), ref, f"S={S} {kv} splits={ns}")
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "i8", "bf16"])
+def test_group_of_one_with_split_sequences(kv):
+    """G = 1 over long sequences cut between workers: a worker's second segment writes its split-KV record to the odd
+    slot, whose start is only 8-byte aligned when a record is G * (D + 2) floats with G = 1."""
+    w = _random_workload([3000, 5000, 1000, 7000, 17], 4, 4, 128, 16, kv, "bf16", seed=101)
+    _, _, ref = oracle_step(w)
+    for ns in (0, 2, 5):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        assert_close(kv, to_host(st.out), ref, f"G=1 {kv} splits={ns}")
 
 
 def test_split_modes_agree_closely():
@@ -111,13 +123,13 @@ def test_empty_sequence_gives_zero_row():
         assert_close("bf16", out, ref, "empty row")
 
 
-@pytest.mark.parametrize("kv,D,S", [("f32", 64, 8), ("bf16", 64, 8), ("e4m3", 128, 16), ("e4m3", 128, 4),
-                                    ("i8", 128, 8), ("i8", 128, 32)])
-def test_poisoned_unused_slots_do_not_leak(kv, D, S):
+@pytest.mark.parametrize("kv,D,S,G", [("f32", 64, 8, 4), ("bf16", 64, 8, 4), ("bf16", 128, 16, 8), ("bf16", 128, 4, 8),
+                                      ("e4m3", 128, 16, 4), ("e4m3", 128, 4, 4), ("i8", 128, 8, 4), ("i8", 128, 32, 8)])
+def test_poisoned_unused_slots_do_not_leak(kv, D, S, G):
     """NaN (the largest code for INT8) in every slot that no sequence owns (tails of last blocks, free blocks)
     changes nothing: stale rows of a partly filled tile must not reach the scores or P.V."""
     q = "f32" if kv == "f32" else "bf16"
-    w = _random_workload([13, 2, 40, 77], 8, 2, D, S, kv, q, seed=21, extra_blocks=12)
+    w = _random_workload([13, 2, 40, 77], 2 * G, 2, D, S, kv, q, seed=21, extra_blocks=12)
     _, _, ref = oracle_step(w)
     clean = to_host(_run(w, 0).out)
     S = w.block_size
