@@ -133,9 +133,10 @@ static pkv_status cache_tensor_map(CUtensorMap* map, const void* base, const pkv
     return PKV_OK;
 }
 
-// A 3-D tiled map with 128-byte swizzle; the inner box is 128 bytes (64 bf16 or 128 FP8 codes).
+// A 3-D tiled map with 128-byte swizzle; the inner box is 128 bytes (64 bf16 or 128 FP8 codes).  fetch_bytes: the L2
+// promotion size (0: the inner row itself).
 static pkv_status tensor_map_sw128(CUtensorMap* map, const void* base, bool fp8, uint64_t d0, uint64_t d1, uint64_t d2,
-                                   uint32_t b1, uint32_t b2) {
+                                   uint32_t b1, uint32_t b2, uint64_t fetch_bytes = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {d0, d1, d2};
@@ -144,7 +145,8 @@ static pkv_status tensor_map_sw128(CUtensorMap* map, const void* base, bool fp8,
     cuuint32_t box[3] = {fp8 ? 128u : 64u, b1, b2};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promotion_for_row(d0 * es),
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     promotion_for_row(fetch_bytes ? fetch_bytes : d0 * es),
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (swizzled) failed (%d)", static_cast<int>(r));
     return PKV_OK;
@@ -192,12 +194,31 @@ static int policy_warps(int G, int D) {
     }
 }
 
-// Split-KV scratch: one completion counter per (sequence, KV head), then two
-// partial (O[G][D], m[G], l[G]) records per worker warp.
-static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D) {
+// Smallest GQA group that a bf16 cache decodes on the tensor-core form; below it the CUDA cores keep up with HBM
+// (measured on GB300), at and above it their fp32 FMA issue is the limit.
+#ifndef PKV_BF16_MMA_MIN_G
+#define PKV_BF16_MMA_MIN_G 8
+#endif
+// Largest GQA group for which the tensor-core form takes two KV heads per work unit (when the head count is even).
+#ifndef PKV_MMA_PAIR_MAX_G
+#define PKV_MMA_PAIR_MAX_G 4
+#endif
+
+// Which decode form runs: the tensor-core form for FP8 / INT8 caches and bf16 caches from PKV_BF16_MMA_MIN_G up
+// (128-dim heads), the CUDA-core form otherwise.
+static bool uses_tensor_core(int dtype, int G, int D) {
+    return D == 128 && (narrow(dtype) || (dtype == PKV_BF16 && G >= PKV_BF16_MMA_MIN_G));
+}
+static int mma_heads_per_unit(int G, int Hkv) { return (G <= PKV_MMA_PAIR_MAX_G && Hkv % 2 == 0) ? 2 : 1; }
+
+// Split-KV scratch: one completion counter per (sequence, KV head), then two partial (O, m, l) records per worker
+// warp, each over the query heads of one work unit (G, or 2G when the tensor-core form pairs KV heads).
+static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D, int dtype) {
     const size_t tickets = ((static_cast<size_t>(B) * Hkv * 4 + 255) / 256) * 256;
-    const size_t W = static_cast<size_t>(sms) * policy_warps(G, D);
-    return tickets + W * 2 * static_cast<size_t>(G) * (D + 2) * 4;
+    const bool tc = uses_tensor_core(dtype, G, D);
+    const size_t W = static_cast<size_t>(sms) * (tc ? kMmaWarps : policy_warps(G, D));
+    const size_t rows = static_cast<size_t>(G) * (tc ? mma_heads_per_unit(G, Hkv) : 1);
+    return tickets + W * 2 * rows * (D + 2) * 4;
 }
 
 template <int D, int S, class KV, class QT>
@@ -375,15 +396,19 @@ PKV_API pkv_status pkv_block_hashes(const int32_t* token_ids, const int64_t* cu_
 }
 
 template <class KV>
-static cudaError_t dispatch_mma(int S, int G, const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                                int grid, int block, size_t smem, cudaStream_t s) {
-#define PKV_MMA_G(S_)                                                                      \
-    switch (G) {                                                                           \
-        case 1: return launch_paged_decode_mma<1, S_, KV>(km, vm, a, grid, block, smem, s); \
-        case 2: return launch_paged_decode_mma<2, S_, KV>(km, vm, a, grid, block, smem, s); \
-        case 4: return launch_paged_decode_mma<4, S_, KV>(km, vm, a, grid, block, smem, s); \
-        case 8: return launch_paged_decode_mma<8, S_, KV>(km, vm, a, grid, block, smem, s); \
-        default: return cudaErrorInvalidValue;                                             \
+static cudaError_t dispatch_mma(int S, int G, int HP, const CUtensorMap& km, const CUtensorMap& vm,
+                                const DecodeArgs& a, int grid, int block, size_t smem, cudaStream_t s) {
+#define PKV_MMA_G(S_)                                                                                         \
+    switch (G * 10 + HP) {                                                                                    \
+        case 11: return launch_paged_decode_mma<1, S_, KV, 1>(km, vm, a, grid, block, smem, s);               \
+        case 21: return launch_paged_decode_mma<2, S_, KV, 1>(km, vm, a, grid, block, smem, s);               \
+        case 41: return launch_paged_decode_mma<4, S_, KV, 1>(km, vm, a, grid, block, smem, s);               \
+        case 81: return launch_paged_decode_mma<8, S_, KV, 1>(km, vm, a, grid, block, smem, s);               \
+        case 12: return launch_paged_decode_mma<1, S_, KV, 2>(km, vm, a, grid, block, smem, s);               \
+        case 22: return launch_paged_decode_mma<2, S_, KV, 2>(km, vm, a, grid, block, smem, s);               \
+        case 42: return launch_paged_decode_mma<4, S_, KV, 2>(km, vm, a, grid, block, smem, s);               \
+        case 82: return launch_paged_decode_mma<8, S_, KV, 2>(km, vm, a, grid, block, smem, s);               \
+        default: return cudaErrorInvalidValue;                                                                \
     }
     switch (S) {
         case 4: PKV_MMA_G(4)
@@ -395,12 +420,6 @@ static cudaError_t dispatch_mma(int S, int G, const CUtensorMap& km, const CUten
 #undef PKV_MMA_G
 }
 
-// Smallest GQA group that a bf16 cache decodes on the tensor-core form; below it the CUDA cores keep up with HBM
-// (measured on GB300), at and above it their fp32 FMA issue is the limit.
-#ifndef PKV_BF16_MMA_MIN_G
-#define PKV_BF16_MMA_MIN_G 8
-#endif
-
 // Decode on the tensor-core form of the kernel (decode_mma.cuh): FP8 / INT8 caches, and bf16 caches from
 // PKV_BF16_MMA_MIN_G up, 128-dim heads.  Its stages hold 128-byte swizzled K and V tiles only (two 64-dim halves per
 // bf16 row), each half starting on a 1024-byte boundary; `a` arrives with everything but the shared-memory plan.
@@ -408,10 +427,11 @@ static pkv_status decode_tensor_core(DecodeArgs a, const pkv_cache_desc& c, int 
                                      const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
     const int S = c.block_size, Hkv = c.num_kv_heads;
     const bool b16 = c.dtype == PKV_BF16;
+    const int HP = mma_heads_per_unit(G, Hkv);  // KV heads per work unit
     const uint32_t tile = static_cast<uint32_t>((b16 ? 2 : 1) * std::max(S * 128, 1024));
-    a.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));
+    a.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));  // one K (or V) tile of one head
     a.q_bytes = 0;  // the query rows are read straight into registers
-    a.stage_bytes = 2 * tile;
+    a.stage_bytes = 2 * HP * tile;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 1023) / 1024 * 1024);
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256 - 1024;  // static shared memory, alignment slack
     int nw = kMmaWarps, depth = 0;
@@ -431,15 +451,18 @@ static pkv_status decode_tensor_core(DecodeArgs a, const pkv_cache_desc& c, int 
     const uint64_t rows = static_cast<uint64_t>(c.num_blocks) * S;
     CUtensorMap km, vm;
     pkv_status st;
-    if ((st = tensor_map_sw128(&km, k_cache, !b16, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
-    if ((st = tensor_map_sw128(&vm, v_cache, !b16, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    // a unit's HP heads are read together, so a one-byte row pair (256 contiguous bytes) is fetched as one
+    const uint64_t fetch = static_cast<uint64_t>(b16 ? 256 : 128 * HP);
+    if ((st = tensor_map_sw128(&km, k_cache, !b16, 128, Hkv, rows, 1, S, fetch)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, !b16, 128, Hkv, rows, 1, S, fetch)) != PKV_OK) return st;
     if (a.tickets) {
         cudaError_t e = cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(num_seqs) * Hkv * 4, s);
         if (e != cudaSuccess) return cuda_fail(e, "clearing split-KV counters");
     }
-    const cudaError_t e = b16                       ? dispatch_mma<KvBF16>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
-                          : c.dtype == PKV_FP8_E4M3 ? dispatch_mma<KvE4M3>(S, G, km, vm, a, di.sms, nw * 32, smem, s)
-                                                    : dispatch_mma<KvI8>(S, G, km, vm, a, di.sms, nw * 32, smem, s);
+    const cudaError_t e =
+        b16                       ? dispatch_mma<KvBF16>(S, G, HP, km, vm, a, di.sms, nw * 32, smem, s)
+        : c.dtype == PKV_FP8_E4M3 ? dispatch_mma<KvE4M3>(S, G, HP, km, vm, a, di.sms, nw * 32, smem, s)
+                                  : dispatch_mma<KvI8>(S, G, HP, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
     return PKV_OK;
 }
@@ -463,7 +486,7 @@ PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cach
     DeviceInfo di;
     if ((st = device_info(&di)) != PKV_OK) return st;
     *bytes = workspace_bytes_for(di.sms, num_seqs, cache->num_kv_heads, num_q_heads / cache->num_kv_heads,
-                                 cache->head_dim);
+                                 cache->head_dim, cache->dtype);
     return PKV_OK;
 }
 
@@ -522,7 +545,7 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     int32_t* tickets = nullptr;
     float* partials = nullptr;
     if (num_splits != 1) {
-        const size_t need = workspace_bytes_for(di.sms, num_seqs, Hkv, G, D);
+        const size_t need = workspace_bytes_for(di.sms, num_seqs, Hkv, G, D, cache->dtype);
         if (!workspace || workspace_bytes < need)
             return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                         workspace ? workspace_bytes : static_cast<size_t>(0));
@@ -560,7 +583,7 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
     a.timeout_ns = 2000000000ull;
-    if (D == 128 && (narrow(cache->dtype) || (cache->dtype == PKV_BF16 && G >= PKV_BF16_MMA_MIN_G)))
+    if (uses_tensor_core(cache->dtype, G, D))
         return decode_tensor_core(a, *cache, G, num_seqs, k_cache, v_cache, di, static_cast<cudaStream_t>(stream));
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
     int nw = policy_warps(G, D), depth = 0;

@@ -98,18 +98,24 @@ __device__ __forceinline__ uint32_t pair_bytes(uint32_t w, uint32_t x) {
     return __byte_perm(w, x, B == 0 ? 0x5140u : 0x7362u);
 }
 
-// Shared-memory plan of one warp stage: K tile, V tile.  A tile is one half (one-byte codes: S rows of 128 codes)
-// or two halves (bf16: head dims 0-63, then 64-127, S rows of 128 bytes each), every half padded to 1024 bytes so
-// that it starts on the 128-byte swizzle's 1024-byte period.  The query rows do not pass through the stages: each
-// thread loads its 64 bytes of Q into registers once per segment, so every stage byte carries K or V.
-template <int S, int ES>
+// Shared-memory plan of one warp stage: the K tiles of its HP KV heads, then their V tiles.  A tile is one half
+// (one-byte codes: S rows of 128 codes) or two halves (bf16: head dims 0-63, then 64-127, S rows of 128 bytes each),
+// every half padded to 1024 bytes so that it starts on the 128-byte swizzle's 1024-byte period.  The query rows do
+// not pass through the stages: each thread loads its Q into registers once per segment, so every stage byte
+// carries K or V.
+template <int S, int ES, int HP>
 struct MmaStage {
     static constexpr int kHalf = S * 128 < 1024 ? 1024 : S * 128;
     static constexpr int kTile = (ES == 2 ? 2 : 1) * kHalf;
-    static constexpr int kBytes = 2 * kTile;
+    static constexpr int kBytes = 2 * HP * kTile;
 };
 
-template <int G, int S, class KV>
+// HP: KV heads per work unit.  With HP = 2 (GQA groups up to 8) a warp takes two neighbouring KV heads of the same
+// blocks together: the second head's query rows are rows 8-15 of the MMAs (zero padding otherwise), its scores the
+// second half of each S quad and its output the second half of each O quad.  The MMA count per byte is the same,
+// the per-block work of the pipeline (waits, refills, metadata, softmax reductions) is shared by two heads, and the
+// two heads' rows of a token, adjacent in the cache, are fetched together.
+template <int G, int S, class KV, int HP>
 __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const DecodeArgs a) {
@@ -117,8 +123,9 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     constexpr int TS = S < 16 ? S : 16;   // tokens of a block per 16-row MMA tile
     constexpr int NT = S / TS;            // tiles per block
     constexpr bool B16 = KV::es == 2;  // bf16 cache: bf16 MMAs on the cached values as they are
-    constexpr int kHalf = MmaStage<S, KV::es>::kHalf, kTile = MmaStage<S, KV::es>::kTile;
-    static_assert(G <= 8, "query rows of one MMA tile");
+    constexpr int kHalf = MmaStage<S, KV::es, HP>::kHalf, kTile = MmaStage<S, KV::es, HP>::kTile;
+    constexpr int GU = HP * G;  // query heads of a work unit (rows of its split-KV records)
+    static_assert(G <= 8 && (HP == 1 || HP == 2), "query rows of one MMA tile");
     static_assert(KV::es <= 2, "one-byte or bf16 caches");
 
     extern __shared__ uint8_t smem_raw[];
@@ -196,11 +203,12 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     }
     __syncwarp();
 
-    const int T = Hkv * P[B];
+    const int Hu = Hkv / HP;  // work units per block: KV heads taken HP at a time
+    const int T = Hu * P[B];
     if (T == 0) return;
     const int W = min(static_cast<int>(gridDim.x) * NW, T);
     const int w = blockIdx.x * NW + warp;
-    const WorkSplit split{P, B, Hkv, T, a.part_blocks, W, T / W, T % W};
+    const WorkSplit split{P, B, Hu, T, a.part_blocks, W, T / W, T % W};
     const int A0 = split.start(w);
     const int A1 = split.start(w + 1);
     if (A0 >= A1) return;
@@ -214,13 +222,13 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     auto make_meta = [&](int x) -> Meta {
         Meta m{0, -1, 0};
         if (x >= A1) return m;
-        const int s = find_seq(P, B, x / Hkv);
-        const int local = x - Hkv * P[s];
+        const int s = find_seq(P, B, x / Hu);
+        const int local = x - Hu * P[s];
         const int nb = P[s + 1] - P[s];
-        const int h = local / nb;
-        const int j = local - h * nb;
+        const int u = local / nb;
+        const int j = local - u * nb;
         const int L = a.context_lens[s];
-        m.a = s * 1024 + h;
+        m.a = s * 1024 + u;
         m.b = a.block_tables[static_cast<size_t>(s) * a.MB + j];
         const int valid = min(S, L - j * S);
         m.c = valid | (j == 0 ? kMetaFirst : 0) | (j == nb - 1 ? kMetaLast : 0) |
@@ -235,13 +243,15 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         const uint32_t bar = bars_u32 + 8 * st;
         const uint32_t dst = wreg_u32 + st * a.stage_bytes;
         if (ok) {
-            mbar_arrive_expect_tx(bar, 2u * a.kv_bytes);
-            const int h = m.a & 1023;
+            mbar_arrive_expect_tx(bar, 2u * HP * a.kv_bytes);
+            const int h0 = (m.a & 1023) * HP;
 #pragma unroll
-            for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
-                tma_load_3d(dst + hf * kHalf, &kmap, hf * 64, h, m.b * S, bar, pol);
-                tma_load_3d(dst + kTile + hf * kHalf, &vmap, hf * 64, h, m.b * S, bar, pol);
-            }
+            for (int hh = 0; hh < HP; ++hh)
+#pragma unroll
+                for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
+                    tma_load_3d(dst + hh * kTile + hf * kHalf, &kmap, hf * 64, h0 + hh, m.b * S, bar, pol);
+                    tma_load_3d(dst + (HP + hh) * kTile + hf * kHalf, &vmap, hf * 64, h0 + hh, m.b * S, bar, pol);
+                }
         } else {
             mbar_arrive(bar);
         }
@@ -272,29 +282,33 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     int st = 0;       // stage of stream index k (k % depth)
     uint32_t ph = 0;  // its phase parity ((k / depth) & 1)
     while (k < n_blocks) {
-        // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
+        // ------------------------------------------------ one segment: consecutive blocks of one (s, unit) pair
         const int seg_x0 = A0 + k;
-        uint32_t qa[8][4];  // Q fragment quads per k-step: row g, dims 32t + 4ks + {0,1} and {2,3} (f16); zero rows
-        float o[16][4];     // O[g][32t + n] and O[g][32t + 16 + n] for output tile n (and rows 8-15, unused)
-        float m_ref = -INFINITY;  // running max of row g (log2 units), the same in the 4 threads of the row
-        float l_run = 0.f;        // this thread's share of the running sum of row g
+        // Q fragment quads per k-step: rows g (head 0 of the unit) and g + 8 (head 1, or zero), dims as this
+        // thread's K operand holds them
+        uint32_t qa[8][4];
+        // O[g][dim] of head 0 in elements 0, 1 and of head 1 in elements 2, 3 of output tile n (dims: dim_of below)
+        float o[16][4];
+        float m_ref[HP], l_run[HP], qm[HP];  // per head: running max of row g (log2 units), this thread's share of
+                                             // the running sum, score scale
         int ma = 0, mc = 0, seg_first = 0;
         bool first = true;
         int x_last;
-        float qm = a.q_mul;
 
-        // One 16-row MMA tile of the block: K rows at kt, V rows at vt (shared addresses of the tile's row 0),
-        // tv valid tokens (M: tv may be below the tile's rows, the rest are stale and masked out).
+        // One 16-row MMA tile of the block for every head of the unit: head hh's K rows at kt + hh kTile, V rows
+        // at vt + hh kTile (shared addresses of the tile's row 0), tv valid tokens (M: tv may be below the tile's
+        // rows, the rest are stale and masked out).
         auto tile = [&](auto masked, uint32_t kt, uint32_t vt, int tv) {
             constexpr bool M = decltype(masked)::value;
             const int lim = M ? tv : TS;
-            // K operand of one token row (at byte offset ro in each half of the tile): registers b0, b1 per k-step
-            auto k_frags = [&](uint32_t ro, bool present, uint32_t (&kf)[8][2]) {
+            // K operand of one token row (at byte offset ro in each half of a K tile at kb): registers b0, b1 per
+            // k-step
+            auto k_frags = [&](uint32_t kb, uint32_t ro, bool present, uint32_t (&kf)[8][2]) {
                 if constexpr (B16) {
-                    const uint4 x0 = present ? lds128(kt + ro + kb0) : zero4;
-                    const uint4 x1 = present ? lds128(kt + ro + kb1) : zero4;
-                    const uint4 x2 = present ? lds128(kt + kHalf + ro + kb0) : zero4;
-                    const uint4 x3 = present ? lds128(kt + kHalf + ro + kb1) : zero4;
+                    const uint4 x0 = present ? lds128(kb + ro + kb0) : zero4;
+                    const uint4 x1 = present ? lds128(kb + ro + kb1) : zero4;
+                    const uint4 x2 = present ? lds128(kb + kHalf + ro + kb0) : zero4;
+                    const uint4 x3 = present ? lds128(kb + kHalf + ro + kb1) : zero4;
                     const uint32_t w[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
                                             x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
@@ -303,8 +317,8 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                         kf[ks][1] = w[2 * ks + 1];
                     }
                 } else {
-                    const uint4 x0 = present ? lds128(kt + ro + kb0) : zero4;
-                    const uint4 x1 = present ? lds128(kt + ro + kb1) : zero4;
+                    const uint4 x0 = present ? lds128(kb + ro + kb0) : zero4;
+                    const uint4 x1 = present ? lds128(kb + ro + kb1) : zero4;
                     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
@@ -313,86 +327,101 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                     }
                 }
             };
-            // ---- S = Q Kᵀ: column tile 0 holds tokens 0-7, tile 1 tokens 8-15 (thread: tokens 2t, 2t+1 of each)
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-            {
-                uint32_t kf[8][2];
-                k_frags(0u, g < TS, kf);
-                float e0[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-steps: a second accumulation chain
+            const int t0 = 2 * t, t2 = 8 + 2 * t;
+            uint32_t pq[HP][4];  // P quads: head 0 in rows 0-7, head 1 in rows 8-15
 #pragma unroll
-                for (int ks = 0; ks < 8; ks += 2) {
-                    mma_16816<B16>(s0, qa[ks], kf[ks][0], kf[ks][1]);
-                    mma_16816<B16>(e0, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
-                }
-                s0[0] += e0[0];
-                s0[1] += e0[1];
-                if constexpr (TS > 8) {
-                    k_frags(1024u, true, kf);
-                    float e1[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int hh = 0; hh < HP; ++hh) {
+                // ---- S = Q Kᵀ against head hh's keys: column tile 0 holds tokens 0-7, tile 1 tokens 8-15
+                // (thread: tokens 2t, 2t+1 of each); head hh's scores are elements 2 hh, 2 hh + 1 of the quads
+                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    uint32_t kf[8][2];
+                    k_frags(kt + hh * kTile, 0u, g < TS, kf);
+                    float e0[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-steps: a second accumulation chain
 #pragma unroll
                     for (int ks = 0; ks < 8; ks += 2) {
-                        mma_16816<B16>(s1, qa[ks], kf[ks][0], kf[ks][1]);
-                        mma_16816<B16>(e1, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
+                        mma_16816<B16>(s0, qa[ks], kf[ks][0], kf[ks][1]);
+                        mma_16816<B16>(e0, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
                     }
-                    s1[0] += e1[0];
-                    s1[1] += e1[1];
-                }
-            }
-            // ---- online softmax of row g over the tile's tokens
-            const int t0 = 2 * t, t2 = 8 + 2 * t;
-            float sc0 = (t0 < lim) ? s0[0] * qm : -INFINITY;
-            float sc1 = (t0 + 1 < lim) ? s0[1] * qm : -INFINITY;
-            float sc2 = (t2 < lim) ? s1[0] * qm : -INFINITY;
-            float sc3 = (t2 + 1 < lim) ? s1[1] * qm : -INFINITY;
-            float mb = fmaxf(fmaxf(sc0, sc1), fmaxf(sc2, sc3));
-            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
-            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
-            const bool need = mb > m_ref + kLazyRescale;
-            if (__any_sync(kFull, need)) {
-                const float m_new = need ? mb : m_ref;
-                const float alpha = (m_new == m_ref) ? 1.f : ex2_approx(m_ref - m_new);
-                l_run *= alpha;
-                m_ref = m_new;
+                    s0[2 * hh] += e0[2 * hh];
+                    s0[2 * hh + 1] += e0[2 * hh + 1];
+                    if constexpr (TS > 8) {
+                        k_frags(kt + hh * kTile, 1024u, true, kf);
+                        float e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= alpha;
-                    o[n][1] *= alpha;  // rows 8-15 (elements 2, 3) carry nothing of use
-                }
-            }
-            const float p0 = ex2_approx(sc0 - m_ref), p1 = ex2_approx(sc1 - m_ref);
-            const float p2 = ex2_approx(sc2 - m_ref), p3 = ex2_approx(sc3 - m_ref);
-            l_run += (p0 + p1) + (p2 + p3);
-            const uint32_t pa[4] = {pack2<B16>(p0, p1), zr, pack2<B16>(p2, p3), zr};
-            // ---- O += P V: thread (g, t) supplies V rows 2t, 2t+1, 2t+8, 2t+9 of its chunk(s); rows past the valid
-            // tokens are zero (stale rows may hold anything, and 0 * NaN would reach O)
-#pragma unroll
-            for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
-                const uint32_t vh = vt + hf * kHalf;
-                const uint4 v0 = (t0 < lim) ? lds128(vh + vb0) : zero4;
-                const uint4 v1 = (t0 + 1 < lim) ? lds128(vh + vb1) : zero4;
-                const uint4 v2 = (t2 < lim) ? lds128(vh + 1024 + vb0) : zero4;
-                const uint4 v3 = (t2 + 1 < lim) ? lds128(vh + 1024 + vb1) : zero4;
-                const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
-                const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if constexpr (B16) {
-                        // word j holds dims 2j, 2j+1 of the chunk: output tiles 8 hf + 2j and 8 hf + 2j + 1
-                        mma_16816<true>(o[8 * hf + 2 * j], pa, __byte_perm(va[j], vb[j], 0x5410u),
-                                        __byte_perm(vc[j], vd[j], 0x5410u));
-                        mma_16816<true>(o[8 * hf + 2 * j + 1], pa, __byte_perm(va[j], vb[j], 0x7632u),
-                                        __byte_perm(vc[j], vd[j], 0x7632u));
-                    } else {
-                        // word j holds dims 4j .. 4j+3 of the chunk: output tiles 4j .. 4j+3
-                        const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
-                        const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
-                        mma_16816<false>(o[4 * j], pa, codes2_to_f16x2<KV, false>(lo01), codes2_to_f16x2<KV, false>(lo23));
-                        mma_16816<false>(o[4 * j + 1], pa, codes2_to_f16x2<KV, true>(lo01), codes2_to_f16x2<KV, true>(lo23));
-                        mma_16816<false>(o[4 * j + 2], pa, codes2_to_f16x2<KV, false>(hi01), codes2_to_f16x2<KV, false>(hi23));
-                        mma_16816<false>(o[4 * j + 3], pa, codes2_to_f16x2<KV, true>(hi01), codes2_to_f16x2<KV, true>(hi23));
+                        for (int ks = 0; ks < 8; ks += 2) {
+                            mma_16816<B16>(s1, qa[ks], kf[ks][0], kf[ks][1]);
+                            mma_16816<B16>(e1, qa[ks + 1], kf[ks + 1][0], kf[ks + 1][1]);
+                        }
+                        s1[2 * hh] += e1[2 * hh];
+                        s1[2 * hh + 1] += e1[2 * hh + 1];
                     }
                 }
+                // ---- online softmax of head hh's row g over the tile's tokens
+                const float sc0 = (t0 < lim) ? s0[2 * hh] * qm[hh] : -INFINITY;
+                const float sc1 = (t0 + 1 < lim) ? s0[2 * hh + 1] * qm[hh] : -INFINITY;
+                const float sc2 = (t2 < lim) ? s1[2 * hh] * qm[hh] : -INFINITY;
+                const float sc3 = (t2 + 1 < lim) ? s1[2 * hh + 1] * qm[hh] : -INFINITY;
+                float mb = fmaxf(fmaxf(sc0, sc1), fmaxf(sc2, sc3));
+                mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+                mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+                const bool need = mb > m_ref[hh] + kLazyRescale;
+                if (__any_sync(kFull, need)) {
+                    const float m_new = need ? mb : m_ref[hh];
+                    const float alpha = (m_new == m_ref[hh]) ? 1.f : ex2_approx(m_ref[hh] - m_new);
+                    l_run[hh] *= alpha;
+                    m_ref[hh] = m_new;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        o[n][2 * hh] *= alpha;
+                        o[n][2 * hh + 1] *= alpha;
+                    }
+                }
+                const float p0 = ex2_approx(sc0 - m_ref[hh]), p1 = ex2_approx(sc1 - m_ref[hh]);
+                const float p2 = ex2_approx(sc2 - m_ref[hh]), p3 = ex2_approx(sc3 - m_ref[hh]);
+                l_run[hh] += (p0 + p1) + (p2 + p3);
+                const uint32_t plo = pack2<B16>(p0, p1), phi = pack2<B16>(p2, p3);
+                pq[hh][0] = hh == 0 ? plo : zr;
+                pq[hh][1] = hh == 0 ? zr : plo;
+                pq[hh][2] = hh == 0 ? phi : zr;
+                pq[hh][3] = hh == 0 ? zr : phi;
             }
+            // ---- O += P V per head: thread (g, t) supplies V rows 2t, 2t+1, 2t+8, 2t+9 of its chunk(s); rows
+            // past the valid tokens are zero (stale rows may hold anything, and 0 * NaN would reach O)
+#pragma unroll
+            for (int hh = 0; hh < HP; ++hh)
+#pragma unroll
+                for (int hf = 0; hf < (B16 ? 2 : 1); ++hf) {
+                    const uint32_t vh = vt + hh * kTile + hf * kHalf;
+                    const uint4 v0 = (t0 < lim) ? lds128(vh + vb0) : zero4;
+                    const uint4 v1 = (t0 + 1 < lim) ? lds128(vh + vb1) : zero4;
+                    const uint4 v2 = (t2 < lim) ? lds128(vh + 1024 + vb0) : zero4;
+                    const uint4 v3 = (t2 + 1 < lim) ? lds128(vh + 1024 + vb1) : zero4;
+                    const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+                    const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if constexpr (B16) {
+                            // word j holds dims 2j, 2j+1 of the chunk: output tiles 8 hf + 2j and 8 hf + 2j + 1
+                            mma_16816<true>(o[8 * hf + 2 * j], pq[hh], __byte_perm(va[j], vb[j], 0x5410u),
+                                            __byte_perm(vc[j], vd[j], 0x5410u));
+                            mma_16816<true>(o[8 * hf + 2 * j + 1], pq[hh], __byte_perm(va[j], vb[j], 0x7632u),
+                                            __byte_perm(vc[j], vd[j], 0x7632u));
+                        } else {
+                            // word j holds dims 4j .. 4j+3 of the chunk: output tiles 4j .. 4j+3
+                            const uint32_t lo01 = pair_bytes<0>(va[j], vb[j]), lo23 = pair_bytes<0>(vc[j], vd[j]);
+                            const uint32_t hi01 = pair_bytes<2>(va[j], vb[j]), hi23 = pair_bytes<2>(vc[j], vd[j]);
+                            mma_16816<false>(o[4 * j], pq[hh], codes2_to_f16x2<KV, false>(lo01),
+                                             codes2_to_f16x2<KV, false>(lo23));
+                            mma_16816<false>(o[4 * j + 1], pq[hh], codes2_to_f16x2<KV, true>(lo01),
+                                             codes2_to_f16x2<KV, true>(lo23));
+                            mma_16816<false>(o[4 * j + 2], pq[hh], codes2_to_f16x2<KV, false>(hi01),
+                                             codes2_to_f16x2<KV, false>(hi23));
+                            mma_16816<false>(o[4 * j + 3], pq[hh], codes2_to_f16x2<KV, true>(hi01),
+                                             codes2_to_f16x2<KV, true>(hi23));
+                        }
+                    }
+                }
         };
 
         while (true) {
@@ -408,36 +437,50 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
             if (!wait_stage(k, st, ph)) return;
             const uint32_t sp = wreg_u32 + static_cast<uint32_t>(st) * a.stage_bytes;
             if (first) {
-                // Q of this (s, h) from global memory: row g, the head dims this thread's K operand holds, in the
-                // same permuted k order (one-byte caches: dims 32t .. 32t+31, bf16 -> f16; bf16 caches: dims
-                // 16t .. 16t+15 and 64+16t .. 64+16t+15 as they are)
+                // Q of this (s, unit) from global memory: for each head hh of the unit, row g, the head dims this
+                // thread's K operand holds, in the same permuted k order (one-byte caches: dims 32t .. 32t+31,
+                // bf16 -> f16; bf16 caches: dims 16t .. 16t+15 and 64+16t .. 64+16t+15 as they are)
                 seg_first = mc & kMetaFirst;
-                qm = a.k_head ? a.q_base * __ldg(a.k_head + (ma & 1023)) : a.q_mul;
-                const uint4* qrow = reinterpret_cast<const uint4*>(
-                    reinterpret_cast<const uint8_t*>(a.q) +
-                    (static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(ma & 1023) * G + g) * D * 2);
                 bool in_range = true;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int qi = B16 ? (i < 2 ? 2 * t + i : 8 + 2 * t + i - 2) : 4 * t + i;  // 16-byte units
-                    const uint4 w4 = g < G ? __ldg(qrow + qi) : zero4;
-                    if constexpr (B16) {
-                        qa[2 * i][0] = w4.x;
-                        qa[2 * i][2] = w4.y;
-                        qa[2 * i + 1][0] = w4.z;
-                        qa[2 * i + 1][2] = w4.w;
-                        qa[2 * i][1] = qa[2 * i][3] = qa[2 * i + 1][1] = qa[2 * i + 1][3] = zr;
-                        continue;
+                for (int ks = 0; ks < 8; ++ks) qa[ks][1] = qa[ks][3] = zr;
+#pragma unroll
+                for (int hh = 0; hh < HP; ++hh) {
+                    const int hk = (ma & 1023) * HP + hh;  // the KV head
+                    qm[hh] = a.k_head ? a.q_base * __ldg(a.k_head + hk) : a.q_mul;
+                    m_ref[hh] = -INFINITY;
+                    l_run[hh] = 0.f;
+                    const uint4* qrow = reinterpret_cast<const uint4*>(
+                        reinterpret_cast<const uint8_t*>(a.q) +
+                        (static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(hk) * G + g) * D * 2);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int qi = B16 ? (i < 2 ? 2 * t + i : 8 + 2 * t + i - 2) : 4 * t + i;  // 16-byte units
+                        const uint4 w4 = g < G ? __ldg(qrow + qi) : zero4;
+                        uint32_t f[4];
+                        if constexpr (B16) {
+                            f[0] = w4.x;
+                            f[1] = w4.y;
+                            f[2] = w4.z;
+                            f[3] = w4.w;
+                        } else {
+                            const float2 f0 = bf16x2_to_float2(w4.x), f1 = bf16x2_to_float2(w4.y);
+                            const float2 f2 = bf16x2_to_float2(w4.z), f3 = bf16x2_to_float2(w4.w);
+                            in_range = in_range &&
+                                       fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))) < 65520.f &&
+                                       fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))) < 65520.f;
+                            f[0] = pack2<false>(f0.x, f0.y);
+                            f[1] = pack2<false>(f1.x, f1.y);
+                            f[2] = pack2<false>(f2.x, f2.y);
+                            f[3] = pack2<false>(f3.x, f3.y);
+                        }
+                        // dims d, d+1 go to the k 2t register of the quad, d+2, d+3 to the k 2t+8 register; head 0
+                        // in rows g (elements 0, 2), head 1 in rows g + 8 (elements 1, 3)
+                        qa[2 * i][hh] = f[0];
+                        qa[2 * i][2 + hh] = f[1];
+                        qa[2 * i + 1][hh] = f[2];
+                        qa[2 * i + 1][2 + hh] = f[3];
                     }
-                    const float2 f0 = bf16x2_to_float2(w4.x), f1 = bf16x2_to_float2(w4.y);
-                    const float2 f2 = bf16x2_to_float2(w4.z), f3 = bf16x2_to_float2(w4.w);
-                    in_range = in_range && fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))) < 65520.f &&
-                               fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))) < 65520.f;
-                    qa[2 * i][0] = pack2<false>(f0.x, f0.y);
-                    qa[2 * i][2] = pack2<false>(f1.x, f1.y);
-                    qa[2 * i + 1][0] = pack2<false>(f2.x, f2.y);
-                    qa[2 * i + 1][2] = pack2<false>(f3.x, f3.y);
-                    qa[2 * i][1] = qa[2 * i][3] = qa[2 * i + 1][1] = qa[2 * i + 1][3] = zr;
                 }
                 if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
 #pragma unroll
@@ -450,7 +493,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                 for (int ti = 0; ti < NT; ++ti) {
                     const int tv = valid - ti * TS;
                     if (tv <= 0) break;
-                    const uint32_t kt = sp + ti * TS * 128, vt = sp + kTile + ti * TS * 128;
+                    const uint32_t kt = sp + ti * TS * 128, vt = sp + HP * kTile + ti * TS * 128;
                     if (tv >= TS) tile(std::false_type{}, kt, vt, TS);
                     else tile(std::true_type{}, kt, vt, tv);
                 }
@@ -479,68 +522,89 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         }
 
         // ------------------------------------------------ end of segment
-        l_run += __shfl_xor_sync(kFull, l_run, 1);
-        l_run += __shfl_xor_sync(kFull, l_run, 2);
-        const int s = ma >> 10, h = ma & 1023;
+        const int s = ma >> 10, u = ma & 1023;
         const int nb = P[s + 1] - P[s];
-        const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.o_mul;
         // the 32 output dims of thread (g, t), in runs of 16 contiguous dims: one-byte caches 32t .. 32t+31; bf16
         // caches 16t .. 16t+15 and 64+16t .. 64+16t+15 (output tile n, column 2t / 2t+1 is dim 8 (2t) + n / 8 (2t+1)
         // + n for n < 8, and 64 + the same for tile 8 + n)
         auto dim_of = [&](int i) { return B16 ? (i < 16 ? 16 * t + i : 64 + 16 * t + i - 16) : 32 * t + i; };
-        float v[32];
+        // head hh's O in dim_of order
+        auto o_row = [&](int hh, float (&v)[32]) {
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            if constexpr (B16) {
-                v[n] = o[n][0];
-                v[8 + n] = o[n][1];
-                v[16 + n] = o[8 + n][0];
-                v[24 + n] = o[8 + n][1];
-            } else {
-                v[n] = o[n][0];
-                v[8 + n] = o[8 + n][0];
-                v[16 + n] = o[n][1];
-                v[24 + n] = o[8 + n][1];
+            for (int n = 0; n < 8; ++n) {
+                if constexpr (B16) {
+                    v[n] = o[n][2 * hh];
+                    v[8 + n] = o[n][2 * hh + 1];
+                    v[16 + n] = o[8 + n][2 * hh];
+                    v[24 + n] = o[8 + n][2 * hh + 1];
+                } else {
+                    v[n] = o[n][2 * hh];
+                    v[8 + n] = o[8 + n][2 * hh];
+                    v[16 + n] = o[n][2 * hh + 1];
+                    v[24 + n] = o[8 + n][2 * hh + 1];
+                }
             }
-        }
-        auto store_row = [&](const float (&x)[32], float inv) {  // out[s][h G + g][dim_of(i)], bf16
+        };
+        // out[s][query head (u HP + hh) G + g][dim_of(i)], bf16
+        auto store_row = [&](int hh, const float (&x)[32], float inv) {
             uint32_t wv[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 wv[i] = static_cast<uint32_t>(float_to_bf16_bits(x[2 * i] * inv)) |
                         (static_cast<uint32_t>(float_to_bf16_bits(x[2 * i + 1] * inv)) << 16);
             uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
-                            (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * 2;
+                            (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(u * HP + hh) * G + g) * D * 2;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(orow + dim_of(8 * i) * 2) =
                     make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
         };
+        auto out_mul = [&](int hh) { return a.v_head ? __ldg(a.v_head + u * HP + hh) : a.o_mul; };
+#pragma unroll
+        for (int hh = 0; hh < HP; ++hh) {
+            l_run[hh] += __shfl_xor_sync(kFull, l_run[hh], 1);
+            l_run[hh] += __shfl_xor_sync(kFull, l_run[hh], 2);
+        }
         const bool whole = seg_first && (mc & kMetaLast) && (x_last - seg_x0 + 1 == nb);
         if (whole) {
-            if (g < G) store_row(v, l_run > 0.f ? out_mul / l_run : 0.f);
+            if (g < G) {
+#pragma unroll
+                for (int hh = 0; hh < HP; ++hh) {
+                    float v[32];
+                    o_row(hh, v);
+                    store_row(hh, v, l_run[hh] > 0.f ? out_mul(hh) / l_run[hh] : 0.f);
+                }
+            }
             continue;
         }
-        // partial record of this segment: O[G][D], m[G], l[G].  A record is G * (D + 2) floats, so records are
-        // 16-byte aligned for even G and only 8-byte aligned for G = 1: the O runs move as float4 or float2 pairs.
-        const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
+        // partial record of this segment: O[GU][D], m[GU], l[GU] (row hh G + g for head hh).  A record is
+        // GU * (D + 2) floats, so records are 16-byte aligned for even GU and only 8-byte aligned for GU = 1: the O
+        // runs move as float4 or as float2 pairs.
+        const size_t rec_floats = static_cast<size_t>(GU) * (D + 2);
         {
             const int slot = (seg_x0 == A0) ? 0 : 1;
             float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
             if (g < G) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float* dst = rec + g * D + dim_of(4 * i);
-                    if constexpr (G % 2 == 0) {
-                        *reinterpret_cast<float4*>(dst) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    } else {
-                        reinterpret_cast<float2*>(dst)[0] = make_float2(v[4 * i], v[4 * i + 1]);
-                        reinterpret_cast<float2*>(dst)[1] = make_float2(v[4 * i + 2], v[4 * i + 3]);
+                for (int hh = 0; hh < HP; ++hh) {
+                    float v[32];
+                    o_row(hh, v);
+                    const int row = hh * G + g;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float* dst = rec + row * D + dim_of(4 * i);
+                        if constexpr (GU % 2 == 0) {
+                            *reinterpret_cast<float4*>(dst) =
+                                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        } else {
+                            reinterpret_cast<float2*>(dst)[0] = make_float2(v[4 * i], v[4 * i + 1]);
+                            reinterpret_cast<float2*>(dst)[1] = make_float2(v[4 * i + 2], v[4 * i + 3]);
+                        }
                     }
-                }
-                if (t == 0) {
-                    rec[G * D + g] = m_ref;
-                    rec[G * D + G + g] = l_run;
+                    if (t == 0) {
+                        rec[GU * D + row] = m_ref[hh];
+                        rec[GU * D + GU + row] = l_run[hh];
+                    }
                 }
             }
         }
@@ -548,60 +612,64 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         __syncwarp();
         int old = 0;
         const int seg_blocks = x_last - seg_x0 + 1;
-        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], seg_blocks);
+        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hu + u], seg_blocks);
         old = __shfl_sync(kFull, old, 0);
         if (old + seg_blocks != nb) continue;
 
-        // last finisher of pair (s, h): merge its segments in stream order
+        // last finisher of pair (s, unit): merge its segments in stream order
         __threadfence();
-        const int U0 = Hkv * P[s] + h * nb;
+        const int U0 = Hu * P[s] + u * nb;
         const int U1 = U0 + nb;
-        float Mx = -INFINITY, Ls = 0.f;
-        float acc[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-        int wq = w, ys = A0;
-        while (ys > U0 && wq > 0) ys = split.start(--wq);
-        while (ys < U1 && wq < W) {
-            const int ye = split.start(wq + 1);
-            if (ye > ys && g < G) {  // a non-empty share holds one segment of the pair
-                const int sl = (ys >= U0) ? 0 : 1;
-                const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
-                const float mr = __ldcg(r + G * D + g);
-                const float lr = __ldcg(r + G * D + G + g);
-                const float mn = fmaxf(Mx, mr);
-                const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
-                const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
-                Ls = Ls * fo + lr * fr;
-                Mx = mn;
+        for (int hh = 0; hh < HP; ++hh) {
+            const int row = hh * G + g;
+            float Mx = -INFINITY, Ls = 0.f;
+            float acc[32];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float4 ov;
-                    if constexpr (G % 2 == 0) {
-                        ov = __ldcg(reinterpret_cast<const float4*>(r + g * D + dim_of(4 * i)));
-                    } else {
-                        const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + g * D + dim_of(4 * i)));
-                        const float2 o23 = __ldcg(reinterpret_cast<const float2*>(r + g * D + dim_of(4 * i)) + 1);
-                        ov = make_float4(o01.x, o01.y, o23.x, o23.y);
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            int wq = w, ys = A0;
+            while (ys > U0 && wq > 0) ys = split.start(--wq);
+            while (ys < U1 && wq < W) {
+                const int ye = split.start(wq + 1);
+                if (ye > ys && g < G) {  // a non-empty share holds one segment of the pair
+                    const int sl = (ys >= U0) ? 0 : 1;
+                    const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
+                    const float mr = __ldcg(r + GU * D + row);
+                    const float lr = __ldcg(r + GU * D + GU + row);
+                    const float mn = fmaxf(Mx, mr);
+                    const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
+                    const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
+                    Ls = Ls * fo + lr * fr;
+                    Mx = mn;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 ov;
+                        if constexpr (GU % 2 == 0) {
+                            ov = __ldcg(reinterpret_cast<const float4*>(r + row * D + dim_of(4 * i)));
+                        } else {
+                            const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)));
+                            const float2 o23 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)) + 1);
+                            ov = make_float4(o01.x, o01.y, o23.x, o23.y);
+                        }
+                        acc[4 * i] = acc[4 * i] * fo + ov.x * fr;
+                        acc[4 * i + 1] = acc[4 * i + 1] * fo + ov.y * fr;
+                        acc[4 * i + 2] = acc[4 * i + 2] * fo + ov.z * fr;
+                        acc[4 * i + 3] = acc[4 * i + 3] * fo + ov.w * fr;
                     }
-                    acc[4 * i] = acc[4 * i] * fo + ov.x * fr;
-                    acc[4 * i + 1] = acc[4 * i + 1] * fo + ov.y * fr;
-                    acc[4 * i + 2] = acc[4 * i + 2] * fo + ov.z * fr;
-                    acc[4 * i + 3] = acc[4 * i + 3] * fo + ov.w * fr;
                 }
+                ++wq;
+                ys = ye;
             }
-            ++wq;
-            ys = ye;
+            if (g < G) store_row(hh, acc, Ls > 0.f ? out_mul(hh) / Ls : 0.f);
         }
-        if (g < G) store_row(acc, Ls > 0.f ? out_mul / Ls : 0.f);
     }
 }
 
 // Host-side launch for one instantiation (defined in decode_mma_*.cu).
-template <int G, int S, class KV>
+template <int G, int S, class KV, int HP>
 cudaError_t launch_paged_decode_mma(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,
                                     int block, size_t smem, cudaStream_t stream) {
-    auto kern = paged_decode_mma_kernel<G, S, KV>;
+    auto kern = paged_decode_mma_kernel<G, S, KV, HP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     kern<<<grid, block, smem, stream>>>(kmap, vmap, a);

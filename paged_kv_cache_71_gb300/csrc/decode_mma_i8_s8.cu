@@ -4,13 +4,17 @@
 
 namespace pkv {
 
-#define PKV_INST(G_)                                                                                        \
-    template cudaError_t launch_paged_decode_mma<G_, 8, KvI8>(const CUtensorMap&, const CUtensorMap&,    \
-                                                              const DecodeArgs&, int, int, size_t, cudaStream_t);
-PKV_INST(1)
-PKV_INST(2)
-PKV_INST(4)
-PKV_INST(8)
+#define PKV_INST(G_, HP_)                                                                                   \
+    template cudaError_t launch_paged_decode_mma<G_, 8, KvI8, HP_>(const CUtensorMap&, const CUtensorMap&,     \
+                                                                  const DecodeArgs&, int, int, size_t, cudaStream_t);
+PKV_INST(1, 1)
+PKV_INST(2, 1)
+PKV_INST(4, 1)
+PKV_INST(8, 1)
+PKV_INST(1, 2)
+PKV_INST(2, 2)
+PKV_INST(4, 2)
+PKV_INST(8, 2)
 #undef PKV_INST
 
 }  // namespace pkv

@@ -101,6 +101,18 @@ def test_group_of_one_with_split_sequences(kv):
         assert_close(kv, to_host(st.out), ref, f"G=1 {kv} splits={ns}")
 
 
+@pytest.mark.parametrize("kv,G", [("e4m3", 1), ("i8", 4), ("e4m3", 8), ("bf16", 8)])
+def test_odd_kv_head_count(kv, G):
+    """Three KV heads: the tensor-core form takes KV heads in pairs only when their count is even, so this runs one
+    head per work unit; ragged lengths, every split mode."""
+    w = _random_workload([1, 15, 16, 17, 300, 2100], 3 * G, 3, 128, 16, kv, "bf16", seed=70 + G)
+    _, _, ref = oracle_step(w)
+    for ns in (0, 1, 3):
+        st = _run(w, ns)
+        assert st.device_error() == 0
+        assert_close(kv, to_host(st.out), ref, f"Hkv=3 G={G} {kv} splits={ns}")
+
+
 def test_split_modes_agree_closely():
     """Any split gives the same attention up to fp32 rounding order."""
     w = _random_workload([700, 1, 2048, 333, 5000], 16, 4, 64, 16, "f32", "f32", seed=77)
