@@ -66,8 +66,8 @@ typedef enum {
 #define PKV_DEVERR_BAD_BLOCK 0x2    /* block id < 0 or >= num_blocks where one must be read */
 #define PKV_DEVERR_BAD_LENGTH 0x4   /* context_len < 0 or > max_blocks_per_seq * block_size */
 #define PKV_DEVERR_TIMEOUT 0x8      /* a bounded wait on an async copy gave up */
-#define PKV_DEVERR_Q_RANGE 0x10     /* a query value beyond the f16 range (|q| >= 65520) in a prefill over an
-                                       FP8 or INT8 cache, whose tensor-core products run on f16 operands */
+#define PKV_DEVERR_Q_RANGE 0x10     /* a query value beyond the f16 range (|q| >= 65520) in a prefill or decode
+                                       over an FP8 or INT8 cache, whose tensor-core products run on f16 operands */
 
 /* Description of one layer's K and V cache pools. */
 typedef struct {
@@ -140,6 +140,13 @@ pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cache, int32
  *   num_splits == P : cut only on boundaries of partitions of
  *                     ceil(ceil(max_context_len / S) / P) blocks
  * Any choice gives the same result up to fp32 rounding order.
+ *
+ * Arithmetic: fp32 accumulation throughout.  FP8 / INT8 caches with 128-dim
+ * heads, and bf16 caches of 128-dim heads in groups of G = 8, run q.K and P.V
+ * on the tensor cores: cached codes and bf16 values enter exactly, q is taken
+ * to f16 for one-byte caches (|q| >= 65520 sets PKV_DEVERR_Q_RANGE) and the
+ * probabilities are rounded to f16 (bf16 for a bf16 cache) before P.V.  The
+ * other cases compute on fp32 values throughout.
  *
  *   q:   [num_seqs][num_q_heads][head_dim], q_dtype f32 (with an f32 cache)
  *        or bf16 (with a bf16, FP8 or INT8 cache); out has q's dtype and shape.

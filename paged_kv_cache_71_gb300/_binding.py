@@ -23,6 +23,7 @@ PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_OUT_OF_RANGE",
                 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
 DEVERR_BAD_SLOT, DEVERR_BAD_BLOCK, DEVERR_BAD_LENGTH, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEVERR_Q_RANGE = 0x10
 
 _DTYPE_CODE = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.uint8: PKV_FP8_E4M3,
                torch.float8_e4m3fn: PKV_FP8_E4M3, torch.int8: PKV_INT8}

@@ -17,6 +17,20 @@ def test_library_exports_every_declared_entry_point():
         assert hasattr(L, n), n
 
 
+def test_binding_constants_match_the_header():
+    """The device error bits and dtype codes the binding uses are the ones include/pkv.h defines."""
+    import os
+    import re
+    text = open(os.path.join(os.path.dirname(__file__), "..", "include", "pkv.h")).read()
+    defs = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"#define (PKV_DEVERR_\w+) (0x[0-9a-fA-F]+|\d+)", text)}
+    assert defs == {"PKV_DEVERR_BAD_SLOT": B.DEVERR_BAD_SLOT, "PKV_DEVERR_BAD_BLOCK": B.DEVERR_BAD_BLOCK,
+                    "PKV_DEVERR_BAD_LENGTH": B.DEVERR_BAD_LENGTH, "PKV_DEVERR_TIMEOUT": B.DEVERR_TIMEOUT,
+                    "PKV_DEVERR_Q_RANGE": B.DEVERR_Q_RANGE}
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"(PKV_(?:F32|BF16|FP8_E4M3|INT8))\s*=\s*(\d+)", text)}
+    assert enums == {"PKV_F32": B.PKV_F32, "PKV_BF16": B.PKV_BF16, "PKV_FP8_E4M3": B.PKV_FP8_E4M3,
+                     "PKV_INT8": B.PKV_INT8}
+
+
 def test_status_strings_and_version():
     assert pkv.pkv_abi_version() == 2  # the cache descriptor carries optional per-head scales
     for code, name in B.STATUS_NAMES.items():

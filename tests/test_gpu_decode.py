@@ -113,6 +113,20 @@ def test_odd_kv_head_count(kv, G):
         assert_close(kv, to_host(st.out), ref, f"Hkv=3 G={G} {kv} splits={ns}")
 
 
+@pytest.mark.parametrize("kv", ["e4m3", "i8"])
+def test_one_byte_decode_query_out_of_f16_range_is_flagged(kv):
+    """Decode over a one-byte cache takes q to f16 for the tensor-core products: a query value of 2^17 (a bf16 value
+    beyond f16) must set PKV_DEVERR_Q_RANGE in the device error word; in-range queries leave it clear."""
+    w = _random_workload([40, 7, 300], 8, 2, 128, 16, kv, "bf16", seed=91)
+    st = _run(w, 0)
+    assert st.device_error() == 0
+    q = w.q.copy()
+    q[1, 3, 17] = np.uint16(0x4800)  # bf16 bits of 2^17 = 131072
+    w.q = q
+    st = _run(w, 0)
+    assert st.device_error() & B.DEVERR_Q_RANGE
+
+
 def test_split_modes_agree_closely():
     """Any split gives the same attention up to fp32 rounding order."""
     w = _random_workload([700, 1, 2048, 333, 5000], 16, 4, 64, 16, "f32", "f32", seed=77)
