@@ -295,3 +295,25 @@ def test_prefill_one_byte_cache_query_out_of_f16_range_is_flagged(kv):
     ref = oracle.paged_prefill_chunk(q, 100, kc, vc, table, kv_len, 1 / np.sqrt(128), rows=rows, cache_dtype=code,
                                      k_scale=0.25, v_scale=0.5)
     assert_close(kv, to_host(out)[rows], ref, "rows without the out-of-range query")
+
+
+def test_fp8_prefill_query_rows_of_wide_range():
+    """Query rows mixing values from 2^-12 to 2^6 (and exact zeros) over an FP8 cache: the tile takes q to f16,
+    which holds every one of them exactly, so the chunk matches the oracle."""
+    q, kc, vc, table, kv_len = _chunk_case(70, 250, 16, 2, 16, seed=17, kv="e4m3")
+    rng = np.random.default_rng(5)
+    mag = np.exp2(rng.integers(-12, 7, size=q.shape)).astype(np.float32)
+    sign = np.where(rng.random(q.shape) < 0.5, -1.0, 1.0).astype(np.float32)
+    vals = (mag * sign).astype(np.float32)
+    vals[rng.random(q.shape) < 0.05] = 0.0
+    q = (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16 (powers of two)
+    dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
+    out = torch.empty_like(dq)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv.pkv_paged_prefill_chunk(out, dq, 250, dk, dv, B.CacheDesc.for_cache(dk, 0.25, 0.5), to_device(table),
+                                kv_len, 1 / np.sqrt(128), err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref = oracle.paged_prefill_chunk(q, 250, kc, vc, table, kv_len, 1 / np.sqrt(128), cache_dtype=oracle.E4M3,
+                                     k_scale=0.25, v_scale=0.5)
+    assert_close("e4m3", to_host(out), ref, "wide-range query rows")
