@@ -1,26 +1,29 @@
-// decode_mma.cuh -- paged decode attention over FP8 (E4M3) or INT8 K/V caches with the per-warp tensor-core MMA.
+// decode_mma.cuh -- paged decode attention with the per-warp tensor-core MMA: FP8 (E4M3) and INT8 K/V caches, and
+// bf16 caches in GQA groups of 8 (128-dim heads, bf16 queries).
 //
 // Method: the same online-softmax recurrence over the blocks named by each sequence's block table as the CUDA-core
 // decode kernel (decode.cuh; "从 PagedAttention 到 Chunked Prefill" §2.2, "PagedAttention：块表"), with the same
-// work split, TMA pipeline per warp and split-KV records.  What changes is the arithmetic: with one-byte codes the
-// CUDA cores must do 2·G fp32 multiply-adds per byte streamed, which at G = 4 is two thirds of their peak at the
-// HBM rate and at G = 8 more than all of it.  Here each warp computes, per 16-token tile of one (sequence, KV head),
+// work split, TMA pipeline per warp and split-KV records.  What changes is the arithmetic: on the CUDA cores these
+// cases need 2·G fp32 multiply-adds per cached element, which at the HBM rate is two thirds of the fp32 peak (INT8
+// at G = 4, bf16 at G = 8) or more than all of it (FP8 at G = 8).  Here each warp computes, per 16-token tile of one
+// (sequence, KV head),
 //   S = Q · Kᵀ   as 2 × 8 mma.sync.m16n8k16 (rows: the G query heads, padded to 16; columns: 8 tokens; k: 16 dims)
 //   O += P · V  as 16 mma.sync.m16n8k16 (rows: the G heads; columns: 8 head dims; k: the 16 tokens)
-// on f16 operands with fp32 accumulation.  Every E4M3 and INT8 code is exactly an f16 value, Q is converted from
-// bf16 to f16 once per segment (exact for |q| in [2^-14, 65504]; larger values raise PKV_DEVERR_Q_RANGE), and the
-// probabilities are rounded to f16 (relative 2^-11) before P·V.  The per-tensor or per-head scales are applied to
-// the fp32 scores and to the output.
+// with fp32 accumulation.  One-byte caches run f16 operands: every E4M3 and INT8 code is exactly an f16 value, Q is
+// converted from bf16 to f16 once per segment (exact for |q| in [2^-14, 65504]; larger values raise
+// PKV_DEVERR_Q_RANGE), and the probabilities are rounded to f16 (relative 2^-11) before P·V.  bf16 caches run bf16
+// operands on the cached values as they are, with the probabilities rounded to bf16.  The per-tensor or per-head
+// scales are applied to the fp32 scores and to the output.  For groups up to 4 a warp takes two neighbouring KV heads
+// together (HP = 2): the second head's query rows are MMA rows 8-15.
 //
-// Fragment layout (lane = 4 g + t): in S, thread (g, t) holds row g (query head g of the group) and tokens 2t, 2t+1
-// of each 8-token column tile.  The k index of the S MMAs is a permutation of the head dimension chosen so that a
-// thread's K operand is one contiguous 32-byte run of its token's row (dims 32t .. 32t + 31, four per k-step), and
-// Q is permuted the same way; the dot product does not depend on the order of its terms.  In P·V the k index is
-// the token in natural order, so the probabilities of S's output fragment are P's input fragment as they stand, and
-// the column of output tile n held by thread (g, t) is head dim 16 g + n: each thread reads 16 contiguous codes of
-// four token rows and pairs tokens with one byte permute per two dims.  The output thread (g, t) ends with is
-// O[g][32 t .. 32 t + 31].  K and V tiles arrive by TMA with the 128-byte swizzle (128 codes per row), which keeps
-// all these 16-byte shared-memory reads free of bank conflicts.
+// Fragment layout (lane = 4 g + t): in S, thread (g, t) holds row g (query head g of the group; row g + 8 for the
+// second head of a unit) and tokens 2t, 2t+1 of each 8-token column tile.  The k index of the S MMAs is a
+// permutation of the head dimension chosen so that a thread's K operand is one contiguous run of its token's row
+// (one-byte codes: dims 32t .. 32t + 31, four per k-step; bf16: dims 16t .. 16t + 15 of each 64-dim half), and Q is
+// permuted the same way; the dot product does not depend on the order of its terms.  In P·V the k index is the token
+// in natural order, so the probabilities of S's output fragment are P's input fragment as they stand, and each
+// thread reads 16-byte runs of four token rows and pairs tokens with byte permutes.  K and V tiles arrive by TMA with
+// the 128-byte swizzle (128-byte rows), which keeps all these 16-byte shared-memory reads free of bank conflicts.
 #pragma once
 
 #include "decode.cuh"
