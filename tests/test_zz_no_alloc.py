@@ -31,7 +31,7 @@ def _random(lens, Hq, Hkv, D, S, kv, q, seed):
     for s, L in enumerate(lens):
         alloc.add_seq(s, L - 1)
         slots.append(alloc.append_token(s))
-    sc = wl.FP8_SCALE if kv == "e4m3" else 1.0
+    sc = {"e4m3": wl.FP8_SCALE, "i8": wl.INT8_SCALE}.get(kv, 1.0)
     return wl.Workload("random", seed, Hq, Hkv, D, S, kv, q, sc, sc,
                        wl.random_values(rng, (len(lens), Hq, D), q),
                        wl.random_values(rng, (NB, S, Hkv, D), kv), wl.random_values(rng, (NB, S, Hkv, D), kv),
@@ -44,6 +44,8 @@ CASES = [
     ("tiny", lambda: wl.tiny()),
     ("bf16_gqa4", lambda: _random([1, 17, 300, 2048, 999, 64], 32, 8, 128, 16, "bf16", "bf16", 5)),
     ("fp8_gqa8", lambda: _random([4096, 12, 777], 64, 8, 128, 16, "e4m3", "bf16", 6)),
+    # tensor-core form with two KV heads per work unit: split-KV records over 8 query heads
+    ("int8_gqa4_pairs", lambda: _random([3000, 5, 640, 17, 1500], 32, 8, 128, 16, "i8", "bf16", 7)),
 ]
 
 
