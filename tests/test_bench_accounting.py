@@ -60,3 +60,25 @@ def test_decode_ceiling_switches_to_fma_where_arithmetic_binds():
         need = bench.decode_fma_flops(w) / bench.decode_algorithmic_bytes(w) * hbm / 1e12
         assert (need > bench.FP32_FMA_TFLOPS) == alu
     assert abs(bench.FP32_FMA_TFLOPS - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
+
+
+def test_decode_kernel_attribution_follows_the_library_policy():
+    """The benchmark names the decode kernel a workload runs on as the library dispatches it: the tensor-core form
+    for FP8 / INT8 caches with 128-dim heads and for bf16 caches of 128-dim heads in GQA groups of 8, the CUDA-core
+    form otherwise; only the CUDA-core form is ever reported against the fp32 FMA ceiling."""
+    import bench
+    from paged_kv_cache_71_gb300 import workload as wl
+    expect = {"tiny": "paged_decode_kernel", "llama2_7b": "paged_decode_kernel",
+              "llama3_8b_gqa": "paged_decode_kernel", "prefix_shared": "paged_decode_kernel",
+              "llama3_8b_gqa_int8": "paged_decode_mma_kernel", "llama70b_mixed_bf16": "paged_decode_mma_kernel",
+              "llama70b_mixed_fp8": "paged_decode_mma_kernel"}
+    for name, kernel in expect.items():
+        w = wl.make(name, batch=8) if name in ("llama3_8b_gqa", "llama70b_mixed_bf16", "llama70b_mixed_fp8") \
+            else wl.make(name)
+        got, sources = bench.decode_kernel(w)
+        assert got == kernel, name
+        for f in sources:  # every source the profile digest covers exists
+            assert os.path.exists(os.path.join(bench.ROOT, "paged_kv_cache_71_gb300", "csrc", f)), (name, f)
+    # the policy constants the attribution mirrors
+    api = open(os.path.join(bench.ROOT, "paged_kv_cache_71_gb300", "csrc", "api.cu")).read()
+    assert "#define PKV_BF16_MMA_MIN_G 8" in api
