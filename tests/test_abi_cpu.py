@@ -93,3 +93,21 @@ def test_reshape_and_copy_host_checks():
     assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 16, 0, None, None) == 0
     assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 12, 3, None, None) == 1
     assert L.pkv_copy_blocks(None, 16, ctypes.byref(d), 16, 3, None, None) == 1
+
+
+def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No CPU fallback: with libpkv.so absent every call raises instead of computing anything."""
+    import torch
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libpkv.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()
+    desc = B.CacheDesc(num_blocks=4, block_size=16, num_kv_heads=2, head_dim=128, dtype=B.PKV_BF16,
+                       k_scale=1.0, v_scale=1.0)
+    with pytest.raises(RuntimeError, match="not built"):
+        pkv.pkv_paged_attention_workspace_size(desc, 2, 4, 0)
+    q = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(RuntimeError, match="not built"):
+        pkv.pkv_paged_attention_decode(q.clone(), q, torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16),
+                                       torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16), desc,
+                                       torch.zeros(2, 1, dtype=torch.int32), torch.ones(2, dtype=torch.int32), 0.1)
