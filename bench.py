@@ -442,6 +442,7 @@ def run_prefill_only(args, local):
     import torch
     from paged_kv_cache_71_gb300 import _binding as B
     from paged_kv_cache_71_gb300 import workload as wl
+    from paged_kv_cache_71_gb300.block_manager import SequenceTables
     from paged_kv_cache_71_gb300.runner import to_device
     torch.cuda.set_device(local)
     kv = "e4m3" if args.config.endswith("fp8") else "bf16"
@@ -449,9 +450,9 @@ def run_prefill_only(args, local):
     rng = np.random.default_rng(wl.CONFIG_SEEDS["llama70b_mixed_bf16"])
     kv_len = q_start + NQ
     NB = -(-kv_len // S) + 16
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
-    alloc.add_seq("chunk", kv_len)
-    table = to_device(np.array(alloc.tables["chunk"], np.int32))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
+    alloc.prefill("chunk", kv_len)
+    table = to_device(np.array(alloc.table("chunk"), np.int32))
     dk = to_device(wl.random_values(rng, (NB, S, Hkv, D), kv))
     dv = to_device(wl.random_values(rng, (NB, S, Hkv, D), kv))
     dq = to_device(wl.random_values(rng, (NQ, Hq, D), "bf16"))

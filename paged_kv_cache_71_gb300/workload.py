@@ -1,4 +1,4 @@
-"""Seeded synthetic workloads for paged decode attention, and the host block allocator.
+"""Seeded synthetic workloads for paged decode attention.
 
 This module builds inputs only.  It holds none of the attention arithmetic:
 it draws lengths and values from seeded generators, hands out physical
@@ -6,14 +6,9 @@ blocks the way a serving engine's block manager does, and records where
 each new token must be written.  Both the CUDA path and the CPU oracle
 consume what it produces; neither is imported here.
 
-Block manager semantics follow the allocator simulation in "3.3 批处理与
-内存管理" (Batching and Memory Management, llm-learning-path), section
-"代码": a free list popped from its tail, one reference count per physical
-block, prefill allocates ceil(n / S) blocks, a decode append allocates a
-new block when the last one is full, and a write into a shared (refcount >
-1) partial block first moves the sequence onto a private copy
-("共享与写时复制", copy-on-write).  The copy of the data itself is the
-``copy_blocks`` kernel's job; the allocator records the (src, dst) pair.
+Physical blocks are handed out by ``block_manager.SequenceTables`` (free-id
+stack, reference counts, copy-on-write of shared partial blocks), seeded
+with a random permutation of the pool so that tables are scattered.
 
 Value distributions (all seeded with ``numpy.random.default_rng``):
 Q, K, V ~ N(0, 1) drawn in float32 and rounded once to the storage dtype;
@@ -31,81 +26,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-# ---------------------------------------------------------------- block manager
-
-
-class BlockAllocator:
-    """Host-side paged-KV block manager (free list + refcounts + copy-on-write)."""
-
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
-        self.block_size = int(block_size)
-        self.num_blocks = int(num_blocks)
-        self.free = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
-        assert sorted(self.free) == list(range(num_blocks))
-        self.ref = [0] * num_blocks
-        self.tables: dict = {}
-        self.lens: dict = {}
-        self.pending_copies: list[tuple[int, int]] = []
-
-    def _take(self) -> int:
-        if not self.free:
-            raise MemoryError("KV pool exhausted: the scheduler must preempt (swap out or recompute)")
-        b = self.free.pop()
-        self.ref[b] = 1
-        return b
-
-    def blocks_needed(self, n_tokens: int) -> int:
-        return -(-int(n_tokens) // self.block_size)
-
-    def add_seq(self, sid, n_tokens: int) -> None:
-        """Prefill: allocate ceil(n / S) blocks for n tokens."""
-        self.tables[sid] = [self._take() for _ in range(self.blocks_needed(n_tokens))]
-        self.lens[sid] = int(n_tokens)
-
-    def append_token(self, sid) -> int:
-        """Decode append: returns the slot (block * S + offset) of the new token."""
-        table, n = self.tables[sid], self.lens[sid]
-        if n % self.block_size == 0:
-            table.append(self._take())
-        elif self.ref[table[-1]] > 1:
-            src = table[-1]
-            self.ref[src] -= 1
-            table[-1] = self._take()
-            self.pending_copies.append((src, table[-1]))
-        self.lens[sid] = n + 1
-        return self.slot_of(sid, n)
-
-    def fork(self, parent, child) -> None:
-        """Parallel sampling / beam fork: the child shares every block of the parent."""
-        self.tables[child] = list(self.tables[parent])
-        self.lens[child] = self.lens[parent]
-        for b in self.tables[child]:
-            self.ref[b] += 1
-
-    def free_seq(self, sid) -> None:
-        for b in self.tables.pop(sid):
-            self.ref[b] -= 1
-            if self.ref[b] == 0:
-                self.free.append(b)
-        del self.lens[sid]
-
-    def slot_of(self, sid, pos: int) -> int:
-        """Flattened cache slot of logical position ``pos``: block * S + offset."""
-        S = self.block_size
-        return self.tables[sid][pos // S] * S + pos % S
-
-    def take_copies(self) -> list[tuple[int, int]]:
-        out, self.pending_copies = self.pending_copies, []
-        return out
-
-    def padded_tables(self, sids, width: int | None = None) -> np.ndarray:
-        width = width or max(len(self.tables[s]) for s in sids)
-        bt = np.full((len(sids), width), -1, dtype=np.int32)
-        for i, s in enumerate(sids):
-            t = self.tables[s]
-            bt[i, : len(t)] = t
-        return bt
-
+from .block_manager import SequenceTables
 
 # ---------------------------------------------------------------- value generation
 
@@ -236,18 +157,18 @@ def _decode_batch(name, lens, Hq, Hkv, D, S, kv_dtype, q_dtype, seed, exact_pool
     lens = np.asarray(lens, dtype=np.int64)
     need = int(sum(-(-int(L) // S) for L in lens))
     NB = exact_pool or _pool_size(need)
-    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    tabs = SequenceTables(NB, S, free_order=rng.permutation(NB))
     slots = []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, int(L) - 1)
-        slots.append(alloc.append_token(s))
+        tabs.prefill(s, int(L) - 1)
+        slots.append(tabs.next_slot(s))
     sids = list(range(len(lens)))
     k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, len(lens), Hq, kv_dtype, q_dtype)
     k_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
     v_new = random_values(rng, (len(lens), Hkv, D), q_dtype)
     scale = {"e4m3": FP8_SCALE, "i8": INT8_SCALE}.get(kv_dtype, 1.0)
     return Workload(name, seed, Hq, Hkv, D, S, kv_dtype, q_dtype, scale, scale, q, k_cache, v_cache,
-                    alloc.padded_tables(sids), lens.astype(np.int32), k_new, v_new,
+                    tabs.block_tables(sids), lens.astype(np.int32), k_new, v_new,
                     np.array(slots, dtype=np.int64), np.zeros((0, 2), dtype=np.int64),
                     notes={"pool_blocks": NB, "used_blocks": need})
 
@@ -291,37 +212,37 @@ def prefix_shared(seed: int = CONFIG_SEEDS["prefix_shared"], batch: int = 128, p
     need = (prefix // S) + batch * (-(-(prefix + private) // S) - prefix // S) \
         + (-(-cow_parent_len // S)) + batch
     NB = _pool_size(need)
-    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
-    alloc.add_seq("prefix", prefix)
+    tabs = SequenceTables(NB, S, free_order=rng.permutation(NB))
+    tabs.prefill("prefix", prefix)
     for s in range(batch):
-        alloc.fork("prefix", s)
-    alloc.free_seq("prefix")
+        tabs.fork("prefix", s)
+    tabs.drop("prefix")
     slots = []
     for s in range(batch):
         for _ in range(private - 1):
-            alloc.append_token(s)
-        slots.append(alloc.append_token(s))
-    alloc.add_seq("cow_parent", cow_parent_len)
+            tabs.next_slot(s)
+        slots.append(tabs.next_slot(s))
+    tabs.prefill("cow_parent", cow_parent_len)
     cow_children = [("cow", c) for c in range(batch)]
     for c in cow_children:
-        alloc.fork("cow_parent", c)
+        tabs.fork("cow_parent", c)
     for c in cow_children:
-        slots.append(alloc.append_token(c))
-    pairs = np.array(alloc.take_copies(), dtype=np.int64).reshape(-1, 2)
+        slots.append(tabs.next_slot(c))
+    pairs = np.array(tabs.drain_copies(), dtype=np.int64).reshape(-1, 2)
     sids = list(range(batch))
     k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, batch, Hq, "bf16", "bf16")
     T = len(slots)
     k_new = random_values(rng, (T, Hkv, D), "bf16")
     v_new = random_values(rng, (T, Hkv, D), "bf16")
-    lens = np.array([alloc.lens[s] for s in sids], dtype=np.int32)
-    shared = alloc.tables[0][: prefix // S]
+    lens = np.array([tabs.length(s) for s in sids], dtype=np.int32)
+    shared = tabs.table(0)[: prefix // S]
     return Workload("prefix_shared", seed, Hq, Hkv, D, S, "bf16", "bf16", 1.0, 1.0, q, k_cache, v_cache,
-                    alloc.padded_tables(sids), lens, k_new, v_new, np.array(slots, dtype=np.int64), pairs,
+                    tabs.block_tables(sids), lens, k_new, v_new, np.array(slots, dtype=np.int64), pairs,
                     notes={"pool_blocks": NB, "shared_blocks": list(map(int, shared)),
-                           "shared_refcount": alloc.ref[shared[0]],
-                           "cow_parent_table": list(map(int, alloc.tables["cow_parent"])),
-                           "cow_child_tables": [list(map(int, alloc.tables[c])) for c in cow_children],
-                           "cow_child_len": alloc.lens[cow_children[0]],
+                           "shared_refcount": int(tabs.pool.refcount[shared[0]]),
+                           "cow_parent_table": list(map(int, tabs.table("cow_parent"))),
+                           "cow_child_tables": [list(map(int, tabs.table(c))) for c in cow_children],
+                           "cow_child_len": tabs.length(cow_children[0]),
                            "num_decode_tokens": batch})
 
 
@@ -336,25 +257,25 @@ def llama70b_mixed(kv_dtype: str = "bf16", seed: int = CONFIG_SEEDS["llama70b_mi
     lens = rng.integers(4096, 32769, size=batch)
     need = int(sum(-(-int(L) // S) for L in lens)) + (-(-(prefix + chunk) // S))
     NB = _pool_size(need)
-    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    tabs = SequenceTables(NB, S, free_order=rng.permutation(NB))
     slots = []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, int(L) - 1)
-        slots.append(alloc.append_token(s))
-    alloc.add_seq("chunked", prefix)
+        tabs.prefill(s, int(L) - 1)
+        slots.append(tabs.next_slot(s))
+    tabs.prefill("chunked", prefix)
     for _ in range(chunk):
-        slots.append(alloc.append_token("chunked"))
+        slots.append(tabs.next_slot("chunked"))
     sids = list(range(batch))
     k_cache, v_cache, q = _cache_and_q(rng, NB, S, Hkv, D, batch, Hq, kv_dtype, "bf16")
     T = len(slots)
     k_new = random_values(rng, (T, Hkv, D), "bf16")
     v_new = random_values(rng, (T, Hkv, D), "bf16")
     q_chunk = random_values(rng, (chunk, Hq, D), "bf16")
-    pf = PrefillChunk(q_chunk, prefix, prefix + chunk, np.array(alloc.tables["chunked"], dtype=np.int32))
+    pf = PrefillChunk(q_chunk, prefix, prefix + chunk, np.array(tabs.table("chunked"), dtype=np.int32))
     scale = FP8_SCALE if kv_dtype == "e4m3" else 1.0
     name = "llama70b_mixed_" + ("fp8" if kv_dtype == "e4m3" else "bf16")
     return Workload(name, seed, Hq, Hkv, D, S, kv_dtype, "bf16", scale, scale, q, k_cache, v_cache,
-                    alloc.padded_tables(sids), lens.astype(np.int32), k_new, v_new,
+                    tabs.block_tables(sids), lens.astype(np.int32), k_new, v_new,
                     np.array(slots, dtype=np.int64), np.zeros((0, 2), dtype=np.int64), prefill=pf,
                     notes={"pool_blocks": NB, "num_decode_tokens": batch})
 

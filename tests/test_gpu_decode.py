@@ -14,6 +14,7 @@ import oracle
 import paged_kv_cache_71_gb300 as pkv
 from paged_kv_cache_71_gb300 import _binding as B
 from paged_kv_cache_71_gb300 import workload as wl
+from paged_kv_cache_71_gb300.block_manager import SequenceTables
 from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
 
 from parity import assert_close, host_bits, oracle_step, to_host
@@ -33,11 +34,11 @@ def _random_workload(lens, Hq, Hkv, D, S, kv, q, seed, extra_blocks=7):
     lens = np.asarray(lens, np.int64)
     need = int(sum(-(-int(L) // S) for L in lens))
     NB = need + extra_blocks
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
     slots = []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, int(L) - 1)
-        slots.append(alloc.append_token(s))
+        alloc.prefill(s, int(L) - 1)
+        slots.append(alloc.next_slot(s))
     k_cache = wl.random_values(rng, (NB, S, Hkv, D), kv)
     v_cache = wl.random_values(rng, (NB, S, Hkv, D), kv)
     qa = wl.random_values(rng, (len(lens), Hq, D), q)
@@ -45,7 +46,7 @@ def _random_workload(lens, Hq, Hkv, D, S, kv, q, seed, extra_blocks=7):
     vn = wl.random_values(rng, (len(lens), Hkv, D), q)
     sc = {"e4m3": wl.FP8_SCALE, "i8": wl.INT8_SCALE}.get(kv, 1.0)
     return wl.Workload("random", seed, Hq, Hkv, D, S, kv, q, sc, sc, qa, k_cache, v_cache,
-                       alloc.padded_tables(list(range(len(lens)))), lens.astype(np.int32), kn, vn,
+                       alloc.block_tables(list(range(len(lens)))), lens.astype(np.int32), kn, vn,
                        np.array(slots, np.int64), np.zeros((0, 2), np.int64))
 
 

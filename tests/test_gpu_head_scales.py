@@ -9,6 +9,7 @@ import oracle
 import paged_kv_cache_71_gb300 as pkv
 from paged_kv_cache_71_gb300 import _binding as B
 from paged_kv_cache_71_gb300 import workload as wl
+from paged_kv_cache_71_gb300.block_manager import SequenceTables
 from paged_kv_cache_71_gb300.runner import to_device
 
 from parity import assert_close, host_bits, to_host
@@ -28,11 +29,11 @@ def _problem(rng, kv, lens, Hq=32, Hkv=8, D=128, S=16):
     """A paged pool written through the cache write with per-head scales (oracle image and device copy)."""
     need = sum(-(-L // S) for L in lens)
     NB = need + 5
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
     slots = []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, L)
-        slots += [alloc.slot_of(s, p) for p in range(L)]
+        alloc.prefill(s, L)
+        slots += [alloc.slot(s, p) for p in range(L)]
     slots = np.array(slots, np.int64)
     T = slots.shape[0]
     ks, vs = _HEAD_SCALES[kv]
@@ -44,7 +45,7 @@ def _problem(rng, kv, lens, Hq=32, Hkv=8, D=128, S=16):
     oracle.reshape_and_cache(kn, vn, slots, kc, vc, cache_dtype=_CODE[kv], k_scale=1.0, v_scale=1.0,
                              k_head_scales=ks, v_head_scales=vs)
     q = wl.random_values(rng, (len(lens), Hq, D), "bf16")
-    return q, kn, vn, slots, kc, vc, alloc.padded_tables(list(range(len(lens)))), np.array(lens, np.int32)
+    return q, kn, vn, slots, kc, vc, alloc.block_tables(list(range(len(lens)))), np.array(lens, np.int32)
 
 
 @pytest.mark.parametrize("kv", ["i8", "e4m3"])

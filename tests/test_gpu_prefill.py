@@ -11,6 +11,7 @@ import oracle
 import paged_kv_cache_71_gb300 as pkv
 from paged_kv_cache_71_gb300 import _binding as B
 from paged_kv_cache_71_gb300 import workload as wl
+from paged_kv_cache_71_gb300.block_manager import SequenceTables
 from paged_kv_cache_71_gb300.runner import to_device
 
 from parity import assert_close, to_host
@@ -25,9 +26,9 @@ def _chunk_case(NQ, q_start, Hq, Hkv, S, seed, extra_blocks=5, poison=False, kv=
     kv_len = q_start + NQ
     nb = -(-kv_len // S)
     NB = nb + extra_blocks
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
-    alloc.add_seq("s", kv_len)
-    table = np.array(alloc.tables["s"], np.int32)
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
+    alloc.prefill("s", kv_len)
+    table = np.array(alloc.table("s"), np.int32)
     kc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     vc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     if poison:  # NaN in every slot that is not one of the sequence's tokens
@@ -143,10 +144,10 @@ def _varlen_case(chunks, Hq, Hkv, S, seed, tail_rows=3, kv="bf16"):
     kv_lens = np.array([qs + nq for qs, nq in chunks], np.int32)
     need = sum(-(-int(L) // S) for L in kv_lens)
     NB = need + 7
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
     for s, L in enumerate(kv_lens):
-        alloc.add_seq(s, int(L))
-    tables = alloc.padded_tables(list(range(len(chunks))))
+        alloc.prefill(s, int(L))
+    tables = alloc.block_tables(list(range(len(chunks))))
     kc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     vc = wl.random_values(rng, (NB, S, Hkv, D), kv)
     cu = np.zeros(len(chunks) + 1, np.int32)

@@ -15,7 +15,8 @@ import pytest
 import torch
 
 import oracle
-from paged_kv_cache_71_gb300.workload import BlockAllocator, random_values
+from paged_kv_cache_71_gb300.block_manager import SequenceTables
+from paged_kv_cache_71_gb300.workload import random_values
 
 
 def _load(golden_dir, name):
@@ -58,9 +59,8 @@ def test_worked_example_gather_via_cache_write(golden_dir):
     vc = kc.copy()
     for name, seqd in g["sequences"].items():
         n = seqd["num_tokens"]
-        alloc = BlockAllocator(NB, S)
-        alloc.tables["x"] = list(seqd["block_table"])
-        slots = np.array([alloc.slot_of("x", p) for p in range(n)], np.int64)
+        table = np.array(seqd["block_table"], np.int32)
+        slots = np.array([(lambda bo: bo[0] * S + bo[1])(oracle.lookup(table, p, S)) for p in range(n)], np.int64)
         tag = 100.0 if name == "A" else 200.0
         kn = (tag + np.arange(n, dtype=np.float32))[:, None, None] * np.ones((1, Hkv, D), np.float32)
         oracle.reshape_and_cache(kn, -kn, slots, kc, vc)
@@ -77,37 +77,37 @@ def test_worked_example_gather_via_cache_write(golden_dir):
 
 def test_allocator_simulation(golden_dir):
     g = _load(golden_dir, "allocator_simulation.json")
-    a = BlockAllocator(g["num_blocks"], g["block_size"])
-    a.add_seq("p", 6)
+    a = SequenceTables(g["num_blocks"], g["block_size"])
+    a.prefill("p", 6)
     a.fork("p", "s1")
     a.fork("p", "s2")
     for s in ("s1", "s2"):
-        a.append_token(s)
-    assert {s: a.tables[s] for s in ("p", "s1", "s2")} == g["after_appends"]["tables"]
-    assert len(a.free) == g["after_appends"]["free"]
-    assert [list(p) for p in a.take_copies()] == g["cow_pairs"]
-    a.free_seq("p")
-    assert a.ref == g["after_free_p"]["ref"]
-    assert len(a.free) == g["after_free_p"]["free"]
+        a.next_slot(s)
+    assert {s: a.table(s) for s in ("p", "s1", "s2")} == g["after_appends"]["tables"]
+    assert a.pool.num_free == g["after_appends"]["free"]
+    assert [list(p) for p in a.drain_copies()] == g["cow_pairs"]
+    a.drop("p")
+    assert a.pool.refcount.tolist() == g["after_free_p"]["ref"]
+    assert a.pool.num_free == g["after_free_p"]["free"]
 
 
 def test_allocator_exhaustion_raises():
-    a = BlockAllocator(2, 4)
-    a.add_seq("x", 8)
+    a = SequenceTables(2, 4)
+    a.prefill("x", 8)
     with pytest.raises(MemoryError):
-        a.append_token("x")
+        a.next_slot("x")
 
 
 def test_block_count_self_test(golden_dir):
     g = _load(golden_dir, "block_count_self_test.json")
-    a = BlockAllocator(100, g["block_size"])
-    a.add_seq("r", g["num_tokens"])
-    assert len(a.tables["r"]) == g["blocks"]
-    assert len(a.tables["r"]) * g["block_size"] == g["slots"]
+    a = SequenceTables(100, g["block_size"])
+    a.prefill("r", g["num_tokens"])
+    assert len(a.table("r")) == g["blocks"]
+    assert len(a.table("r")) * g["block_size"] == g["slots"]
     assert g["slots"] - g["num_tokens"] == g["wasted"] < g["block_size"]
     # the last token sits in the last table entry, at offset (n-1) % S
-    blk, off = oracle.lookup(np.array(a.tables["r"], np.int32), g["num_tokens"] - 1, g["block_size"])
-    assert blk == a.tables["r"][-1] and off == (g["num_tokens"] - 1) % g["block_size"]
+    blk, off = oracle.lookup(np.array(a.table("r"), np.int32), g["num_tokens"] - 1, g["block_size"])
+    assert blk == a.table("r")[-1] and off == (g["num_tokens"] - 1) % g["block_size"]
 
 
 # ------------------------------------------------------------------ element formats
@@ -165,19 +165,19 @@ def _scatter_problem(rng, lens, Hq, Hkv, D, S, extra_blocks=3, dtype=np.float64)
     """Random contiguous K/V per sequence, placed into a paged pool by a shuffled allocator."""
     need = sum(-(-L // S) for L in lens)
     NB = need + extra_blocks
-    alloc = BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
     kc = rng.standard_normal((NB, S, Hkv, D)).astype(np.float32)
     vc = rng.standard_normal((NB, S, Hkv, D)).astype(np.float32)
     Ks, Vs = [], []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, L)
+        alloc.prefill(s, L)
         K = rng.standard_normal((L, Hkv, D)).astype(np.float32)
         V = rng.standard_normal((L, Hkv, D)).astype(np.float32)
-        slots = np.array([alloc.slot_of(s, p) for p in range(L)], np.int64)
+        slots = np.array([alloc.slot(s, p) for p in range(L)], np.int64)
         oracle.reshape_and_cache(K, V, slots, kc, vc)
         Ks.append(K)
         Vs.append(V)
-    bt = alloc.padded_tables(list(range(len(lens))))
+    bt = alloc.block_tables(list(range(len(lens))))
     q = rng.standard_normal((len(lens), Hq, D)).astype(np.float32)
     return q, kc, vc, bt, np.array(lens, np.int32), Ks, Vs, alloc
 
@@ -243,7 +243,7 @@ def test_decode_dominant_logit_selects_its_value():
     q, kc, vc, bt, cl, Ks, Vs, alloc = _scatter_problem(rng, [30], 1, 1, 8, 4)
     kc[:] = 0.0
     q[:] = 1.0
-    slot = alloc.slot_of(0, 17)
+    slot = alloc.slot(0, 17)
     kc[slot // 4, slot % 4, 0, :] = 100.0
     out = oracle.paged_attention_decode(q, kc, vc, bt, cl, 1.0)
     np.testing.assert_allclose(out[0, 0], Vs[0][17, 0], rtol=0, atol=1e-12)
@@ -264,21 +264,21 @@ def test_decode_block_permutation_invariance():
 def test_decode_shared_blocks_equal_private_copies():
     rng = np.random.default_rng(8)
     S, Hkv, D = 4, 2, 16
-    a = BlockAllocator(20, S, free_order=rng.permutation(20))
-    a.add_seq("p", 10)
+    a = SequenceTables(20, S, free_order=rng.permutation(20))
+    a.prefill("p", 10)
     a.fork("p", "c")
-    a.append_token("c")  # CoW of the partial block
-    a.append_token("p")
+    a.next_slot("c")  # CoW of the partial block
+    a.next_slot("p")
     kc = rng.standard_normal((20, S, Hkv, D)).astype(np.float32)
     vc = rng.standard_normal((20, S, Hkv, D)).astype(np.float32)
-    for src, dst in a.take_copies():
+    for src, dst in a.drain_copies():
         kc[dst], vc[dst] = kc[src], vc[src]
     # make the two new tokens equal so both sequences hold the same logical data
     for sid in ("p", "c"):
-        sl = a.slot_of(sid, 10)
+        sl = a.slot(sid, 10)
         kc[sl // S, sl % S] = 0.25
         vc[sl // S, sl % S] = -0.5
-    bt = a.padded_tables(["p", "c"])
+    bt = a.block_tables(["p", "c"])
     assert bt[0, 0] == bt[1, 0] and bt[0, 2] != bt[1, 2]
     q = np.repeat(rng.standard_normal((1, 4, D)).astype(np.float32), 2, axis=0)
     out = oracle.paged_attention_decode(q, kc, vc, bt, np.array([11, 11], np.int32), 0.3)

@@ -62,3 +62,28 @@ def test_fp8_codes_have_no_nan():
     rng = np.random.default_rng(0)
     v = wl.random_values(rng, (1000,), "e4m3")
     assert not np.isnan(oracle.e4m3_to_f64(v)).any()
+
+
+def test_block_manager_cow_on_empty_pool_changes_nothing():
+    """A copy-on-write that finds no free block raises before touching the tables or the counts."""
+    from paged_kv_cache_71_gb300.block_manager import SequenceTables
+    import pytest
+    t = SequenceTables(2, 4)
+    t.prefill("p", 6)                 # blocks 1, 0: the pool is now empty
+    t.fork("p", "c")
+    before = (list(t.table("c")), t.pool.refcount.tolist(), t.length("c"))
+    with pytest.raises(MemoryError):
+        t.next_slot("c")              # block 0 is shared and partly filled: needs a copy
+    assert (list(t.table("c")), t.pool.refcount.tolist(), t.length("c")) == before
+    assert t.drain_copies() == []
+
+
+def test_block_manager_released_blocks_come_back_first():
+    from paged_kv_cache_71_gb300.block_manager import SequenceTables
+    t = SequenceTables(6, 4)
+    t.prefill("a", 8)                 # blocks 5, 4
+    t.prefill("b", 4)                 # block 3
+    t.drop("a")                       # 5 then 4 go back on the stack: 4 is on top
+    t.prefill("c", 12)
+    assert t.table("c") == [4, 5, 2]
+    assert t.pool.num_free == 6 - 4

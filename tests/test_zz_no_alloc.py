@@ -15,6 +15,7 @@ import torch
 import paged_kv_cache_71_gb300 as pkv
 from paged_kv_cache_71_gb300 import _binding as B
 from paged_kv_cache_71_gb300 import workload as wl
+from paged_kv_cache_71_gb300.block_manager import SequenceTables
 from paged_kv_cache_71_gb300.runner import DeviceStep
 
 from parity import TOL
@@ -26,16 +27,16 @@ def _random(lens, Hq, Hkv, D, S, kv, q, seed):
     rng = np.random.default_rng(seed)
     need = int(sum(-(-L // S) for L in lens))
     NB = need + 3
-    alloc = wl.BlockAllocator(NB, S, free_order=rng.permutation(NB))
+    alloc = SequenceTables(NB, S, free_order=rng.permutation(NB))
     slots = []
     for s, L in enumerate(lens):
-        alloc.add_seq(s, L - 1)
-        slots.append(alloc.append_token(s))
+        alloc.prefill(s, L - 1)
+        slots.append(alloc.next_slot(s))
     sc = {"e4m3": wl.FP8_SCALE, "i8": wl.INT8_SCALE}.get(kv, 1.0)
     return wl.Workload("random", seed, Hq, Hkv, D, S, kv, q, sc, sc,
                        wl.random_values(rng, (len(lens), Hq, D), q),
                        wl.random_values(rng, (NB, S, Hkv, D), kv), wl.random_values(rng, (NB, S, Hkv, D), kv),
-                       alloc.padded_tables(list(range(len(lens)))), np.array(lens, np.int32),
+                       alloc.block_tables(list(range(len(lens)))), np.array(lens, np.int32),
                        wl.random_values(rng, (len(lens), Hkv, D), q), wl.random_values(rng, (len(lens), Hkv, D), q),
                        np.array(slots, np.int64), np.zeros((0, 2), np.int64))
 
