@@ -235,7 +235,7 @@ pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, i
  *   block_mapping: int64 [num_pairs][2] = (src, dst), device memory.
  * A dst may not appear as a src in the same call (the copies run
  * concurrently); ids outside [0, num_blocks) set PKV_DEVERR_BAD_BLOCK and
- * that pair is skipped.
+ * that pair is skipped.  num_pairs < 2^30 (PKV_ERR_OUT_OF_RANGE otherwise).
  */
 pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* cache,
                            const int64_t* block_mapping, int32_t num_pairs,
@@ -258,7 +258,10 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* c
  *     GPU that loads the library, until the process exits.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is kept for the life of
+ *     the process: after cudaDeviceReset (or any teardown of the device's
+ *     primary context) it is stale, so this entry point must not be called
+ *     again in that process.
  *   - A batch whose scratch need (pkv_paged_attention_workspace_size) is
  *     above PKV_STATIC_SCRATCH_BYTES is rejected with PKV_ERR_WORKSPACE
  *     before anything is launched; num_splits == 1 needs no scratch.
@@ -289,7 +292,8 @@ pkv_status pkv_paged_attention_decode_static_scratch(
  *   block_mapping: int64 [num_pairs][2] = (src, dst), device-accessible memory.
  * Destination blocks must be distinct; out-of-range ids set
  * PKV_DEVERR_BAD_BLOCK and that pair is skipped.  Pointers that the device
- * cannot dereference are rejected with PKV_ERR_INVALID_ARG.
+ * cannot dereference are rejected with PKV_ERR_INVALID_ARG.  num_pairs < 2^30
+ * (PKV_ERR_OUT_OF_RANGE otherwise).
  */
 pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t src_num_blocks, void* dst_k,
                            void* dst_v, int32_t dst_num_blocks, const pkv_cache_desc* cache,

@@ -313,7 +313,8 @@ PKV_API pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache
     if (st != PKV_OK) return st;
     if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d < 0", num_pairs);
     if (num_pairs == 0) return PKV_OK;
-    if (num_pairs > (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d too large", num_pairs);
+    // one CTA per (pair, tensor): the grid of 2 * num_pairs CTAs must stay below 2^31
+    if (num_pairs >= (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d >= 2^30", num_pairs);
     if (!k_cache || !v_cache || !block_mapping) return fail(PKV_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(k_cache) || !aligned16(v_cache))
         return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
@@ -353,7 +354,7 @@ PKV_API pkv_status pkv_swap_blocks(const void* src_k, const void* src_v, int32_t
         return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_pairs=%d src_num_blocks=%d dst_num_blocks=%d)", num_pairs,
                     src_num_blocks, dst_num_blocks);
     if (num_pairs == 0) return PKV_OK;
-    if (num_pairs > (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d too large", num_pairs);
+    if (num_pairs >= (1 << 30)) return fail(PKV_ERR_OUT_OF_RANGE, "num_pairs %d >= 2^30", num_pairs);
     if (!src_k || !src_v || !dst_k || !dst_v || !block_mapping) return fail(PKV_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(src_k) || !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
         return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint8_t* __restrict__ 
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* mapping, int num_pairs, int num_blocks,
                                int64_t block_bytes, int32_t* err, cudaStream_t stream) {
-    copy_blocks_kernel<<<2 * num_pairs, 256, 0, stream>>>(static_cast<uint8_t*>(k_cache),
+    copy_blocks_kernel<<<2u * static_cast<unsigned>(num_pairs), 256, 0, stream>>>(static_cast<uint8_t*>(k_cache),
                                                          static_cast<uint8_t*>(v_cache), mapping, num_pairs,
                                                          num_blocks, block_bytes, err);
     return cudaGetLastError();
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(const uint8_t* __restr
 cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, int src_nb, void* dst_k, void* dst_v,
                                int dst_nb, const int64_t* mapping, int num_pairs, int64_t block_bytes, int32_t* err,
                                cudaStream_t stream) {
-    swap_blocks_kernel<<<2 * num_pairs, 256, 0, stream>>>(
+    swap_blocks_kernel<<<2u * static_cast<unsigned>(num_pairs), 256, 0, stream>>>(
         static_cast<const uint8_t*>(src_k), static_cast<const uint8_t*>(src_v), static_cast<uint8_t*>(dst_k),
         static_cast<uint8_t*>(dst_v), mapping, num_pairs, src_nb, dst_nb, block_bytes, err);
     return cudaGetLastError();

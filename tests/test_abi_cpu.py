@@ -93,6 +93,9 @@ def test_reshape_and_copy_host_checks():
     assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 16, 0, None, None) == 0
     assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 12, 3, None, None) == 1
     assert L.pkv_copy_blocks(None, 16, ctypes.byref(d), 16, 3, None, None) == 1
+    # one CTA per (pair, tensor): 2^30 pairs would overflow the grid
+    assert L.pkv_copy_blocks(16, 16, ctypes.byref(d), 16, 1 << 30, None, None) == 3
+    assert L.pkv_swap_blocks(16, 16, 4, 16, 16, 4, ctypes.byref(d), 16, 1 << 30, None, None) == 3
 
 
 def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):

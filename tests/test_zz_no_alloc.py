@@ -4,9 +4,10 @@ pkv_paged_attention_decode_static_scratch serves callers that cannot
 allocate device memory when they run attention (a fixed memory plan, a
 host that owns every allocation, a plain-C runtime without an allocator):
 it keeps the split-KV scratch in a static device array owned by the
-library.  These tests call it through the C ABI and check it against the
-workspace-taking entry point on two calls in a row, within the same
-tolerances as the other parity tests.  This file is collected last.
+library.  These tests call it through the C ABI and check it on two calls
+in a row against the workspace-taking entry point and against the fp64
+oracle, within the same tolerances as the other parity tests.  This file is
+collected last.
 """
 import numpy as np
 import pytest
@@ -18,7 +19,7 @@ from paged_kv_cache_71_gb300 import workload as wl
 from paged_kv_cache_71_gb300.block_manager import SequenceTables
 from paged_kv_cache_71_gb300.runner import DeviceStep
 
-from parity import TOL
+from parity import TOL, assert_close, oracle_step, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +62,7 @@ def test_static_scratch_matches_workspace_entry_point(name, make, num_splits):
     assert st.device_error() == 0
     ref = st.out.double().cpu().numpy()
     atol, rtol = TOL[w.kv_dtype]
+    _, _, oref = oracle_step(w)
     for call in range(2):
         out = torch.full_like(st.out, float("nan"))
         pkv.pkv_paged_attention_decode_static_scratch(out, st.q, st.k_cache, st.v_cache, st.cache, st.block_tables,
@@ -71,6 +73,8 @@ def test_static_scratch_matches_workspace_entry_point(name, make, num_splits):
         got = out.double().cpu().numpy()
         assert np.isfinite(got).all(), f"call {call}"
         assert (np.abs(got - ref) <= atol + rtol * np.abs(ref)).all(), f"call {call}: max diff {np.abs(got - ref).max()}"
+        # and independently of the other CUDA entry point: against the oracle
+        assert_close(w.kv_dtype, to_host(out), oref, f"{name} splits={num_splits} call {call} vs oracle")
 
 
 def test_static_scratch_rejects_batches_beyond_its_size():
