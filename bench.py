@@ -34,6 +34,9 @@ if ROOT not in sys.path:
 METRIC = "paged decode attn KV GB/s & % of GB300 HBM peak; seq-steps/sec per layer"
 UNIT = "seq-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+# GB300's L2 size, for the reference arm's `config` (it runs on the host and queries no device); the GPU arm reads
+# the size from the device
+REFERENCE_L2_BYTES = 126 * 2**20
 
 
 # ---------------------------------------------------------------- byte accounting
@@ -52,6 +55,61 @@ def decode_algorithmic_bytes(w) -> int:
     qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * elem_size(w.q_dtype)
     table = int(((L + w.block_size - 1) // w.block_size).sum()) * 4
     return kv + qo + table + 4 * w.num_seqs
+
+
+def decode_unique_bytes(w) -> int:
+    """decode_algorithmic_bytes with every physical block's K and V counted once, however many sequences' tables
+    name it (a shared prefix is read by every sequence that holds it; these are the bytes that must come from
+    DRAM at least once)."""
+    from paged_kv_cache_71_gb300.workload import elem_size
+    S = w.block_size
+    L = w.context_lens.astype(np.int64)
+    nb = (L + S - 1) // S
+    seq = np.repeat(np.arange(w.num_seqs), nb)
+    j = np.arange(int(nb.sum())) - np.repeat(np.cumsum(nb) - nb, nb)
+    blocks = w.block_tables[seq, j].astype(np.int64)
+    valid = np.minimum(S, L[seq] - j * S)
+    most = np.zeros(max(int(blocks.max()) + 1 if blocks.size else 1, 1), dtype=np.int64)
+    np.maximum.at(most, blocks, valid)
+    kv = int(most.sum()) * kv_bytes_per_token(1, w.num_kv_heads, w.head_dim, elem_size(w.kv_dtype))
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * elem_size(w.q_dtype)
+    return kv + qo + int(nb.sum()) * 4 + 4 * w.num_seqs
+
+
+def contiguous_layout(w):
+    """The same batch with every sequence's K/V in consecutive physical blocks in logical order (the contiguous
+    KV cache that paging replaces): (permutation new block -> old block, int32 tables [B, MB])."""
+    S = w.block_size
+    L = w.context_lens.astype(np.int64)
+    nb = (L + S - 1) // S
+    first = np.cumsum(nb) - nb
+    perm = np.concatenate([w.block_tables[s, : nb[s]] for s in range(w.num_seqs)]).astype(np.int64)
+    tables = np.full((w.num_seqs, max(int(nb.max()), 1)), -1, dtype=np.int32)
+    for s in range(w.num_seqs):
+        tables[s, : nb[s]] = first[s] + np.arange(nb[s])
+    return perm, tables
+
+
+def l2_plan(w, l2_bytes: int) -> str:
+    """How the timed steps keep L2 from serving K/V left by the previous step: a batch whose unique K/V bytes are
+    at least twice the L2 size evicts itself; a smaller one gets the L2 flushed (a 2x-L2 buffer written) before
+    every timed step, outside the events that time it."""
+    return "large" if decode_unique_bytes(w) >= 2 * l2_bytes else "flush"
+
+
+def line_config(w, num_splits: int, ws: int, l2: str) -> dict:
+    """The `config` of a bench line, identical for both arms on the same workload."""
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "kv_dtype": w.kv_dtype, "mean_context": float(w.context_lens.mean()), "num_splits": num_splits,
+            "parallelism": f"replicas{ws}", "l2": l2}
+
+
+def l2_note(w, plan: str) -> str:
+    if plan == "large":
+        return f"inputs larger than L2: {decode_algorithmic_bytes(w) / 1e9:.2f} GB of K/V read per step"
+    return (f"L2 flushed before every timed step (2x L2 written outside the timed events): the step's "
+            f"{decode_unique_bytes(w) / 1e6:.1f} MB of unique K/V would fit in L2")
 
 
 def prefill_flops(w) -> int:
@@ -194,6 +252,31 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle timing
 
+def time_oracle_one_core(w, max_seconds: float = 8.0, chunk: int = 8) -> dict:
+    """fp64 oracle on ONE host core: the step's cache write, then the decode of successive groups of `chunk`
+    sequences until the batch is done or `max_seconds` pass; seq-steps/s over the sequences done (the write's
+    time counted in proportion)."""
+    import oracle
+    oracle.build()
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    cache_dt = {"f32": oracle.F32, "bf16": oracle.BF16, "e4m3": oracle.E4M3, "i8": oracle.I8}[w.kv_dtype]
+    t0 = time.perf_counter()
+    oracle.reshape_and_cache(w.k_new, w.v_new, w.slot_mapping, kc, vc, cache_dtype=cache_dt,
+                             k_scale=w.k_scale, v_scale=w.v_scale)
+    t_write = time.perf_counter() - t0
+    done, t1 = 0, time.perf_counter()
+    while done < w.num_seqs and time.perf_counter() - t1 < max_seconds:
+        sel = np.arange(done, min(done + chunk, w.num_seqs))
+        oracle.paged_attention_decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, cache_dtype=cache_dt,
+                                      k_scale=w.k_scale, v_scale=w.v_scale, seqs=sel, threads=1)
+        done += len(sel)
+    t_dec = time.perf_counter() - t1
+    dt = t_dec + t_write * done / w.num_seqs
+    return {"value": round(done / dt, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"cache write of the whole {w.name} batch, then fp64 decode of its first {done} of "
+                      f"{w.num_seqs} sequences on one core, {dt:.1f} s"}
+
+
 def time_oracle(w, steps: int = 1, max_seconds: float = 20.0) -> dict:
     """fp64 oracle on the host cores: the step's cache write and decode over the whole batch,
     repeated up to `steps` times or until `max_seconds` pass."""
@@ -273,6 +356,7 @@ def main():
                     help="time the chained block content hashes of the Llama-3-8B batch's token ids")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-contiguous", action="store_true", help="skip the paged-vs-contiguous decode comparison")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -297,17 +381,22 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    from paged_kv_cache_71_gb300 import _binding as B
-    from paged_kv_cache_71_gb300.runner import DeviceStep, to_device
+    from paged_kv_cache_71_gb300.runner import DeviceStep
 
     # every rank serves its own batch (sequences shard across GPUs; no exchange)
     w = wl.make(args.config, **rank_workload_kwargs(args.config, rank, args.batch))
     st = DeviceStep(w, num_splits=args.num_splits)
     stream = torch.cuda.current_stream()
     launches_per_step = 2 + (1 if st.copy_pairs is not None else 0)
-
     has_prefill = st.pf_q is not None
     launches_per_step += 1 if has_prefill else 0
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or 126 * 2**20)
+    plan = l2_plan(w, l2_bytes)
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if plan == "flush" else None
+
+    def flush():
+        if flush_buf is not None:
+            flush_buf.fill_(1)
 
     def step():
         st.write(stream)
@@ -315,6 +404,7 @@ def main():
         st.prefill(stream)
 
     for _ in range(args.warmup):
+        flush()
         step()
     torch.cuda.synchronize()
     if st.device_error():
@@ -332,6 +422,7 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
+        flush()
         ev[i][0].record(stream)
         st.write(stream)
         ev[i][1].record(stream)
@@ -344,43 +435,18 @@ def main():
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     prefill_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)] if has_prefill else None
+    if plan == "flush":  # the steps alone, without the flushes between them
+        total_ms = sum(ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps))
+    else:
+        total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
     value = job_throughput(ws, w.num_seqs, ms_per_step)
 
-    # ---- end to end through the C ABI with host buffers
-    e2e = None
-    if not args.no_e2e:
-        host = {k: getattr(st, k).cpu().pin_memory() for k in
-                ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
-        out_host = torch.empty_like(st.out, device="cpu").pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_host.numel() * out_host.element_size()
-
-        def e2e_step():
-            for k, t in host.items():
-                getattr(st, k).copy_(t, non_blocking=True)
-            step()
-            out_host.copy_(st.out, non_blocking=True)
-
-        for _ in range(args.warmup):
-            e2e_step()
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dist, "cuda")
-        e2e = {"value": job_throughput(ws, w.num_seqs, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+    e2e = None if args.no_e2e else time_e2e(args, w, st, plan, flush, dist, ws)
 
     peak, peak_src = measured_peaks()
     alg = decode_algorithmic_bytes(w)
@@ -390,6 +456,10 @@ def main():
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": profiled_traffic(w.name, ksrc), "peak_source": peak_src,
             "kernel": kname, "algorithmic_bytes": alg, "avg_launch_us": round(dec_avg * 1e3, 2)}
+    uniq = decode_unique_bytes(w)
+    if uniq != alg:  # shared blocks: the logical bytes stay the headline, the unique bytes beside them
+        roof["unique_bytes"] = uniq
+        roof["unique_gbps"] = round(uniq / (dec_avg / 1e3) / 1e9, 1)
     # the binding ceiling of the CUDA-core form: reading the K/V at the HBM peak needs (flops per byte) x peak of
     # fp32 FMA work; where that exceeds the CUDA cores' FMA peak the kernel is bound by arithmetic instead (the
     # tensor-core form does its contractions on the tensor pipe, far below its peak, and stays HBM-bound)
@@ -402,22 +472,23 @@ def main():
                      "peak_source": "fp32 FMA peak from unit counts and clock", "algorithmic_flops": flops,
                      "hbm_gbs": round(achieved, 1), "hbm_frac": round(achieved / peak, 4)})
 
+    contig = None
+    if not args.no_contiguous and ws == 1:
+        contig = paged_vs_contiguous(args, w, st, flush, stream)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, steps=1000, max_seconds=12.0)
         cpu.pop("seconds", None)
         cpu.pop("steps", None)
+        cpu["one_core"] = time_oracle_one_core(w)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                       "kv_dtype": w.kv_dtype, "mean_context": float(w.context_lens.mean()),
-                       "num_splits": args.num_splits, "parallelism": f"replicas{ws}",
-                       "l2": f"inputs larger than L2: {alg / 1e9:.2f} GB of K/V read per step"},
+            "config": line_config(w, args.num_splits, ws, l2_note(w, plan)),
             "kv_gbps": round(achieved, 1), "pct_of_hbm_peak": round(100 * achieved / peak, 2),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
@@ -425,6 +496,8 @@ def main():
                         "reshape_and_cache_us": round(float(np.mean(write_ms)) * 1e3, 2),
                         "write_bytes": write_bytes(w)},
         }
+        if contig is not None:
+            line["paged_vs_contiguous"] = contig
         if has_prefill:
             pf_us = float(np.mean(prefill_ms)) * 1e3
             fl = prefill_flops(w)
@@ -434,6 +507,147 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_e2e(args, w, st, plan, flush, dist, ws) -> dict:
+    """The step through the C ABI from host buffers: each step's inputs (q, new K/V, slots, block tables,
+    lengths) are copied from pinned host memory and its output copied back, inside the timed region.  Two
+    device-side input/output sets alternate, so that a copy stream moves step i+1's inputs in and step i-1's
+    output out while the compute stream runs step i; the KV cache itself is device-resident state."""
+    import torch
+    from paged_kv_cache_71_gb300.runner import DeviceStep
+    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    outs = ("out",)
+    if st.copy_pairs is not None:  # the copy-on-write pairs of the step
+        names += ("copy_pairs",)
+    if st.pf_q is not None:  # the prefill chunk's queries in, its output out
+        names += ("pf_q",)
+        outs += ("pf_out",)
+    host = {k: getattr(st, k).cpu().pin_memory() for k in names}
+    out_host = [{k: torch.empty_like(getattr(st, k), device="cpu").pin_memory() for k in outs} for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host[0].values())
+    # slot 1: its own input and output buffers, the same caches, workspace and error word
+    other = DeviceStep.__new__(DeviceStep)
+    other.__dict__.update(st.__dict__)
+    for k in names + outs:
+        setattr(other, k, torch.empty_like(getattr(st, k)))
+    slots = (st, other)
+    comp = torch.cuda.current_stream()
+    cs = torch.cuda.Stream()
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+
+    def h2d_into(i):
+        d = slots[i % 2]
+        if i >= 2:
+            cs.wait_event(comp_done[i % 2])  # step i-2 has finished with these buffers
+        with torch.cuda.stream(cs):
+            for k in names:
+                getattr(d, k).copy_(host[k], non_blocking=True)
+        h2d_done[i % 2].record(cs)
+
+    def compute(i):
+        d = slots[i % 2]
+        comp.wait_event(h2d_done[i % 2])
+        d.write(comp)
+        d.attend(comp)
+        d.prefill(comp)
+        comp_done[i % 2].record(comp)
+
+    def d2h_from(i):
+        cs.wait_event(comp_done[i % 2])
+        with torch.cuda.stream(cs):
+            for k in outs:
+                out_host[i % 2][k].copy_(getattr(slots[i % 2], k), non_blocking=True)
+
+    def run(n, per_step_flush):
+        """n steps; returns the copy stream's (start, end) events around them."""
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if per_step_flush:  # flush, then time one whole step (copies in, compute, copy out) at a time
+            ms = 0.0
+            for i in range(n):
+                with torch.cuda.stream(cs):
+                    flush()
+                a.record(cs)
+                h2d_into(i)
+                compute(i)
+                d2h_from(i)
+                b.record(cs)
+                b.synchronize()
+                ms += a.elapsed_time(b)
+            return ms
+        a.record(cs)
+        h2d_into(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d_into(i + 1)
+            compute(i)
+            d2h_from(i)
+        b.record(cs)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    run(args.warmup, plan == "flush")
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = run(args.steps, plan == "flush")
+    e2e_ms = max_over_ranks(ms / args.steps, dist, "cuda")
+    return {"value": job_throughput(ws, w.num_seqs, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+            "overlap": "copies of step i+1 in and step i out on a copy stream beside step i"
+            if plan != "flush" else "one step at a time (L2 flushed between steps)"}
+
+
+def paged_vs_contiguous(args, w, st, flush, stream) -> dict:
+    """The decode kernel over the batch's scattered blocks beside the same kernel over a copy of the pool in which
+    every sequence's blocks are consecutive and in logical order (identity block tables: a contiguous KV cache).
+    Same values, same work split, so the outputs agree bit for bit; the time difference is what paging costs."""
+    import torch
+    from paged_kv_cache_71_gb300 import _binding as B
+    from paged_kv_cache_71_gb300.runner import to_device
+    perm, tables = contiguous_layout(w)
+    idx = torch.from_numpy(perm).to("cuda")
+    kc = st.k_cache.index_select(0, idx)
+    vc = st.v_cache.index_select(0, idx)
+    desc = B.CacheDesc.for_cache(kc, w.k_scale, w.v_scale)
+    dt = to_device(tables)
+    out_c = torch.empty_like(st.out)
+    ws_c = torch.zeros(max(B.pkv_paged_attention_workspace_size(desc, w.num_seqs, w.num_q_heads, st.num_splits), 16),
+                       dtype=torch.uint8, device="cuda")
+
+    def paged():
+        st.attend(stream)
+
+    def contiguous():
+        B.pkv_paged_attention_decode(out_c, st.q, kc, vc, desc, dt, st.context_lens, w.scale, st.num_splits,
+                                     st.max_context_len, ws_c, st.err, stream)
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return [x.elapsed_time(y) * 1e3 for x, y in ts]
+
+    timed(paged, 3)
+    timed(contiguous, 3)
+    tp, tc = [], []
+    for _ in range(3):  # interleaved rounds: both layouts see the same clocks
+        tp += timed(paged, args.steps)
+        tc += timed(contiguous, args.steps)
+    same = bool(torch.equal(out_c, st.out))
+    p_us, c_us = float(np.median(tp)), float(np.median(tc))
+    return {"paged_us": round(p_us, 2), "contiguous_us": round(c_us, 2),
+            "overhead_pct": round(100.0 * (p_us - c_us) / c_us, 2), "outputs_identical": same,
+            "contiguous": "each sequence's blocks consecutive and in logical order (shared blocks duplicated)",
+            "launches_each": 3 * args.steps}
 
 
 def run_prefill_only(args, local):
@@ -648,9 +862,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                       "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                       "kv_dtype": w.kv_dtype},
+            "config": line_config(w, args.num_splits, ws, l2_note(w, l2_plan(w, REFERENCE_L2_BYTES))),
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step = the full {w.name} batch ({w.num_seqs} sequences): cache "
                                        f"write + fp64 decode"},

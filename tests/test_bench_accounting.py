@@ -82,3 +82,53 @@ def test_decode_kernel_attribution_follows_the_library_policy():
     # the policy constants the attribution mirrors
     api = open(os.path.join(bench.ROOT, "paged_kv_cache_71_gb300", "csrc", "api.cu")).read()
     assert "#define PKV_BF16_MMA_MIN_G 8" in api
+
+
+def test_unique_bytes_count_shared_blocks_once():
+    """Prefix-sharing batch: 128 sequences of 1005 tokens whose first 800 (50 blocks) are one shared copy."""
+    w = wl.prefix_shared()
+    per_tok = 2 * 8 * 128 * 2                       # K and V, 8 kv heads, d = 128, bf16
+    qo = 2 * 128 * 32 * 128 * 2
+    table = 128 * 63 * 4 + 4 * 128
+    assert bench.decode_algorithmic_bytes(w) == 128 * 1005 * per_tok + qo + table
+    assert bench.decode_unique_bytes(w) == (800 + 128 * 205) * per_tok + qo + table
+    # no sharing: the two counts agree
+    t = wl.tiny()
+    assert bench.decode_unique_bytes(t) == bench.decode_algorithmic_bytes(t)
+
+
+def test_contiguous_layout_holds_the_same_tokens_in_order():
+    """Identity tables over a permuted copy of the pool read every sequence's tokens exactly as the scattered
+    tables do; each sequence's blocks are consecutive."""
+    import oracle
+    w = wl.tiny()
+    perm, tables = bench.contiguous_layout(w)
+    kc = w.k_cache[perm]
+    S = w.block_size
+    for s in range(w.num_seqs):
+        L = int(w.context_lens[s])
+        nb = -(-L // S)
+        row = tables[s, :nb]
+        assert (np.diff(row) == 1).all() and (tables[s, nb:] == -1).all()
+        for p in range(L):
+            b0, o0 = oracle.lookup(w.block_tables[s], p, S)
+            b1, o1 = oracle.lookup(tables[s], p, S)
+            assert o0 == o1 and (kc[b1, o1] == w.k_cache[b0, o0]).all()
+
+
+def test_l2_plan_and_reference_config():
+    """Batches whose unique K/V fits twice in L2 are timed with an L2 flush between steps; the reference arm prints
+    the same `config` as the GPU arm for the same workload, whichever of GB300's quoted L2 sizes the device gives."""
+    for name, plan in (("tiny", "flush"), ("prefix_shared", "flush"), ("llama3_8b_gqa", "large")):
+        w = wl.make(name)
+        for l2 in (bench.REFERENCE_L2_BYTES, 129 * 10**6, 132 * 2**20):
+            assert bench.l2_plan(w, l2) == plan, (name, l2)
+    w = wl.tiny()
+    cfg = bench.line_config(w, 0, 1, bench.l2_note(w, bench.l2_plan(w, bench.REFERENCE_L2_BYTES)))
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference", "--config",
+                        "tiny", "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"] == cfg
