@@ -50,17 +50,20 @@ constexpr int kKvHalf = kKeys * 128;           // 64 head dims of 64 keys, bytes
 constexpr int kStgSlot = kKeys * 128;          // one key tile of one-byte codes (128 head dims), bytes
 constexpr int kOffQ = 0;                       // tile A: 2 halves, tile B: 2 halves
 
-// Shared-memory plan per cache kind (NARROW: 0 bf16, 1 FP8 E4M3 codes, 2 INT8 codes).  One-byte caches
-// land in a two-slot staging ring per operand and are widened to f16 by the producer (and MMA) warps.
+// Shared-memory plan per cache kind (NARROW: 0 bf16, 1 FP8 E4M3 codes, 2 INT8 codes).  bf16 tiles and FP8 codes
+// go straight from TMA into the K and V rings that the MMAs read (FP8: one 128-byte line of codes per key, 8 KB
+// per 64-key stage).  INT8 codes land in a two-slot staging ring per operand and are widened to f16 by the
+// producer (and MMA) warps into the rings.
 template <int NARROW>
 struct Plan {
-    static constexpr int kStages = NARROW ? 3 : 4;                  // bf16 K and V ring depth
-    static constexpr int kOffK = kOffQ + 4 * kQHalf;                // kStages x 2 halves
-    static constexpr int kOffV = kOffK + kStages * 2 * kKvHalf;
-    static constexpr int kOffStg = kOffV + kStages * 2 * kKvHalf;   // K: 2 slots, then V: 2 slots
-    static constexpr int kOffMeta = kOffStg + (NARROW ? 4 * kStgSlot : 0);
+    static constexpr int kStages = NARROW == 0 ? 4 : NARROW == 1 ? 6 : 3;  // K and V ring depth
+    static constexpr int kStage = NARROW == 1 ? kStgSlot : 2 * kKvHalf;   // bytes of one ring stage
+    static constexpr int kOffK = kOffQ + 4 * kQHalf;
+    static constexpr int kOffV = kOffK + kStages * kStage;
+    static constexpr int kOffStg = kOffV + kStages * kStage;            // INT8: K 2 slots, then V 2 slots
+    static constexpr int kOffMeta = kOffStg + (NARROW == 2 ? 4 * kStgSlot : 0);
 };
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;     // + 128 * tile + 64 * buffer: scores (fp32, 64 keys); P over the first 32 columns
 constexpr int kColO = 256;   // + 128 * tile: output accumulator (fp32, 128 dims)
@@ -78,6 +81,12 @@ template <int NARROW>
 constexpr uint32_t kIdescS = NARROW ? idesc_f16_f32(128, kKeys, false) : idesc_bf16_f32(128, kKeys, false);
 template <int NARROW>
 constexpr uint32_t kIdescPV = NARROW ? idesc_f16_f32(128, 128, true) : idesc_bf16_f32(128, 128, true);
+// kind::f8f6f4 with E4M3 A and B (type fields 0): the same bit pattern as the f16 descriptor above
+constexpr uint32_t kIdescS8 = idesc_f16_f32(128, kKeys, false);
+constexpr uint32_t kIdescPV8 = idesc_f16_f32(128, 128, true);
+// FP8 caches: the running maximum is set 4 (log2 units) below a new row maximum, so that the probabilities reach
+// up to 2^4..2^8 and their two E4M3 parts keep full precision for smaller values
+constexpr float kP8Shift = 4.f;
 
 // mbarrier slots (8 bytes each); "tb" = 2 * tile + buffer
 constexpr int kBarKFull = 0;                         // + stage: K in the bf16 ring (copies landed / widened)
@@ -118,6 +127,22 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+// two E4M3 codes in the low 16 bits of w (low byte first) -> f16x2, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_u(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(w)));
+    return r;
+}
+
+// f16x2 -> two floats (exact)
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+    return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -130,12 +155,32 @@ __device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
     return r;
 }
 
-// Two E4M3 codes (low byte first) -> f16x2, exactly (every E4M3 value is an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t w) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(w));
+// f16x2 -> two E4M3 codes (low half to the low byte), round to nearest even, saturating to +-448
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
     return r;
 }
+
+// two floats -> two E4M3 codes (lo to the low byte), round to nearest even, saturating
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// A value x split into two E4M3 codes, hi = E4M3(x) and lo = E4M3(x - hi): hi + lo carries about 8 significant
+// bits (a bf16 value exactly, when lo stays in E4M3's normal range).  Four f16 values (two f16x2 words, lowest
+// first) give one 32-bit word of four hi codes and one of four lo codes.
+__device__ __forceinline__ void split_e4m3x4(uint32_t h01, uint32_t h23, uint32_t& hi, uint32_t& lo) {
+    const uint32_t a = f16x2_to_e4m3x2(h01), b = f16x2_to_e4m3x2(h23);
+    uint32_t ra, rb;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(ra) : "r"(h01), "r"(e4m3x2_to_f16x2_u(a)));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rb) : "r"(h23), "r"(e4m3x2_to_f16x2_u(b)));
+    hi = a | (b << 16);
+    lo = f16x2_to_e4m3x2(ra) | (f16x2_to_e4m3x2(rb) << 16);
+}
+
 
 // Signed bytes i0, i0 + 1 of w -> f16x2, exactly.  f = w ^ 0x80808080 holds u = byte + 128; u placed in the low
 // mantissa bits of 0x6400 (1024) reads 1024 + u, and one packed subtraction of 1152 leaves the byte's value.
@@ -155,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
     constexpr int kStages = Plan<NARROW>::kStages, kOffK = Plan<NARROW>::kOffK, kOffV = Plan<NARROW>::kOffV;
-    constexpr int kOffStg = Plan<NARROW>::kOffStg, kOffMeta = Plan<NARROW>::kOffMeta;
+    constexpr int kOffStg = Plan<NARROW>::kOffStg, kOffMeta = Plan<NARROW>::kOffMeta, kStage = Plan<NARROW>::kStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -254,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // producer widens every row, leaving the MMA warps to issue; in a varlen launch a CTA with tile A alone (a
     // decode token) has the MMA warps also widen half of the rows of the operand they consume.  Single-chunk
     // launches compile the producer-only form alone.
-    const bool split = NARROW != 0 && ADAPT && !has_b;
+    const bool split = NARROW == 2 && ADAPT && !has_b;
 
     if (tid == 0) {
         // the bf16 instance never waits on the staging-free barriers
@@ -278,13 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // One-byte caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into f16 stage st
-    // (exact: every E4M3 and INT8 code is an f16 value; the per-tensor or per-head scales go to the scores and the
+    // INT8 caches: widen rows rr * 32 + lane of key tile `slot` of the K (or V) staging ring into f16 stage st
+    // (exact: every INT8 code is an f16 value; the per-tensor or per-head scales go to the scores and the
     // output).  128 codes per key row, in 128-byte swizzled lines like the 16-bit halves.  With split widening
     // each of the two warps that serve an operand (its producer and its MMA warp) widens one half of the rows.
     auto widen_rows = [&](bool is_v, int slot, int st, int rr) {
         const uint8_t* src = smem + kOffStg + ((is_v ? 2 : 0) + slot) * kStgSlot;
-        uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * 2 * kKvHalf;
+        uint8_t* dstb = smem + (is_v ? kOffV : kOffK) + st * kStage;
         const int r = lane + 32 * rr, sw = r & 7;
         src += r * 128;
         uint8_t* dst = dstb + r * 128;
@@ -295,14 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if constexpr (NARROW == 2) {
-                    const uint32_t f = ws[i] ^ 0x80808080u;
-                    o[2 * i] = s8x2_to_f16x2(f, 0);
-                    o[2 * i + 1] = s8x2_to_f16x2(f, 2);
-                } else {
-                    o[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] & 0xffffu));
-                    o[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(ws[i] >> 16));
-                }
+                const uint32_t f = ws[i] ^ 0x80808080u;
+                o[2 * i] = s8x2_to_f16x2(f, 0);
+                o[2 * i + 1] = s8x2_to_f16x2(f, 2);
             }
             uint8_t* dh = dst + (c >> 2) * kKvHalf;
             const int lc = 2 * (c & 3);
@@ -354,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                      (j / kStages - 1) & 1, a.timeout_ns));
         };
         int issued = 0, staged = 0, widened = 0;
-        if constexpr (NARROW == 0) {
+        if constexpr (NARROW != 2) {
+            // bf16 tiles (two 64-dim halves per key) or FP8 codes (one 128-byte line per key) straight into the ring
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j % kStages;
                 const int row = tile_row(j);
@@ -364,13 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (__any_sync(kFull, *abort_flag != 0)) break;
                 const uint32_t fb = bar + 8 * (full + st);
-                if (lane == 0) mbar_arrive_expect_tx(fb, 2 * kKvHalf);
+                if (lane == 0) mbar_arrive_expect_tx(fb, kStage);
                 __syncwarp();
-                if (lane < blocks_per_tile)
+                if (lane < blocks_per_tile) {
+                    if constexpr (NARROW == 0) {
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d_nohint(dst0 + (2 * st + hf) * kKvHalf + lane * a.S * 128, map, hf * 64, h, row,
-                                           fb);
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d_nohint(dst0 + st * kStage + hf * kKvHalf + lane * a.S * 128, map, hf * 64, h,
+                                               row, fb);
+                    } else {
+                        tma_load_3d_nohint(dst0 + st * kStage + lane * a.S * 128, map, 0, h, row, fb);
+                    }
+                }
                 issued = j + 1;
             }
         } else {
@@ -454,13 +500,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S(j) of both query tiles into buffer j & 1, which P(j-2) was read from
             auto issue_s = [&](int t, int j) {
                 const uint64_t a0 = d_kmaj + ((kOffQ + 2 * t * kQHalf) >> 4);
-                const uint64_t b0 = d_kmaj + ((kOffK + 2 * (j % kStages) * kKvHalf) >> 4);
+                const uint64_t b0 = d_kmaj + ((kOffK + (j % kStages) * kStage) >> 4);
                 const uint32_t d = tmem + kColS + 128 * t + 64 * (j & 1);
+                if constexpr (NARROW == 1) {
+                    // E4M3: the query row's hi codes in the tile's first 16 KB, its lo codes in the second; the key
+                    // codes one 128-byte line per key; 32 head dims (32 bytes) per MMA
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off_a = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
-                    const uint32_t off_b = ((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4;
-                    tc_mma_f16_warp(d, a0 + off_a, b0 + off_b, kIdescS<NARROW>, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc_mma_f8_warp(d, a0 + 2 * kk, b0 + 2 * kk, kIdescS8, kk > 0);
+                        tc_mma_f8_warp(d, a0 + (kQHalf >> 4) + 2 * kk, b0 + 2 * kk, kIdescS8, 1u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off_a = ((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4;
+                        const uint32_t off_b = ((kk >> 2) * kKvHalf + (kk & 3) * 32) >> 4;
+                        tc_mma_f16_warp(d, a0 + off_a, b0 + off_b, kIdescS<NARROW>, kk > 0);
+                    }
                 }
                 tc_commit_warp(bar + 8 * (kBarSFull + 2 * t + (j & 1)));
             };
@@ -486,12 +542,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
             // P(j).V(j) of both query tiles once their softmax is done
             auto issue_pv = [&](int t, int j) {
-                const uint64_t b0 = d_v + ((kOffV + 2 * (j % kStages) * kKvHalf) >> 4);
+                const uint64_t b0 = d_v + ((kOffV + (j % kStages) * kStage) >> 4);
                 const uint32_t d = tmem + kColO + 128 * t, p = tmem + kColS + 128 * t + 64 * (j & 1);
                 const uint32_t acc0 = j > 0;
+                if constexpr (NARROW == 1) {
+                    // E4M3: P's hi codes of the 64 keys in 16 columns (four per column), its lo codes in the next
+                    // 16; V codes N-major, 128 head dims per 128-byte line, 32 keys (four 1024-byte groups) per MMA
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk)
-                    tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV<NARROW>, kk > 0 ? 1u : acc0);
+                    for (int kc = 0; kc < kKeys / 32; ++kc) {
+                        tc_mma_f8_ts_warp(d, p + 8 * kc, b0 + ((kc * 4096) >> 4), kIdescPV8, kc > 0 ? 1u : acc0);
+                        tc_mma_f8_ts_warp(d, p + 16 + 8 * kc, b0 + ((kc * 4096) >> 4), kIdescPV8, 1u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        tc_mma_f16_ts_warp(d, p + 8 * kk, b0 + ((kk * 2048) >> 4), kIdescPV<NARROW>,
+                                           kk > 0 ? 1u : acc0);
+                }
                 tc_commit_warp(bar + 8 * (kBarPVDone + 2 * t + (j & 1)));
             };
             if (split) ok = widen_half(true, 0);
@@ -528,11 +595,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         int done = 0;
         const bool active = t == 0 || has_b;
         // score scale (log2 units) and output factor of this KV head: per-head scales when given
-        const float sm_log2 = a.k_head ? a.sm_base * __ldg(a.k_head + h) : a.sm_log2;
+        float sm_log2 = a.k_head ? a.sm_base * __ldg(a.k_head + h) : a.sm_log2;
         const float out_mul = a.v_head ? __ldg(a.v_head + h) : a.out_mul;
         bool s_ready = false;  // the next tile's scores were seen complete ahead of time
-        if constexpr (NARROW != 0) {
-            // one-byte caches: the MMAs run on f16 operands, so Q (bf16, landed by TMA) is converted in place, each
+        if constexpr (NARROW == 1) {
+            // FP8 caches: the S MMAs run on E4M3 operands.  This thread's query row r (bf16, landed by TMA: dims
+            // 0-63 in the tile's first 16 KB, 64-127 in the second) is scaled by 2^e, e chosen so that its largest
+            // magnitude lies in [128, 256), and split into hi = E4M3(x) and lo = E4M3(x - hi), written over the row
+            // (hi codes in the first 16 KB, lo codes in the second, 128 codes per 128-byte swizzled line); hi + lo
+            // is the scaled bf16 value exactly for elements within 2^-10 of the row's largest.  The scores are
+            // multiplied back by 2^-e.  Non-finite query values raise Q_RANGE.
+            bool ok_q = !active || __all_sync(kFull, mbar_spin_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns));
+            if (!ok_q) *abort_flag = 1;
+            if (active && ok_q) {
+                uint8_t* qt = smem + kOffQ + 2 * t * kQHalf + r * 128;
+                const int sw = r & 7;
+                auto chunk = [&](int hf, int k) -> uint4 {  // bf16 dims 64 hf + 8k .. + 7
+                    return *reinterpret_cast<const uint4*>(qt + hf * kQHalf + ((k ^ sw) << 4));
+                };
+                auto amax4 = [](uint32_t m, const uint4& x) {  // |value| bits: ordered like the values
+                    const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) m = max(m, max((ws[i] << 17) >> 1, ((ws[i] >> 16) & 0x7fffu) << 16));
+                    return m;
+                };
+                // dims 64..127 are kept in registers: the lo codes of dims 0..63 are written over them
+                uint4 w1[8];
+                uint32_t amax_bits = 0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    w1[k] = chunk(1, k);
+                    amax_bits = amax4(amax4(amax_bits, w1[k]), chunk(0, k));
+                }
+                if (amax_bits >= 0x7f800000u) raise_error(a.err, PKV_DEVERR_Q_RANGE);  // inf or NaN
+                const int ex = static_cast<int>(amax_bits >> 23) - 127;        // floor(log2(max |x|))
+                const int e = min(126, max(-126, 7 - ex));
+                const float up = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+                sm_log2 *= __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // output chunk c: head dims 16c .. 16c + 15
+                    // bf16 chunks 2c, 2c + 1; for c < 4 read here (chunks 0 .. 2c - 1 of that half are consumed,
+                    // and the chunk-c slots written below hold chunks already read or kept in w1)
+                    const uint4 s0 = c < 4 ? chunk(0, 2 * c) : w1[2 * c - 8];
+                    const uint4 s1 = c < 4 ? chunk(0, 2 * c + 1) : w1[2 * c - 7];
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {  // dims 16c + 4i .. 16c + 4i + 3
+                        const uint4 src = (i >> 1) ? s1 : s0;
+                        const uint32_t x01 = (i & 1) ? src.z : src.x, x23 = (i & 1) ? src.w : src.y;
+                        const float2 f01 = bf16x2_to_float2(x01), f23 = bf16x2_to_float2(x23);
+                        const float q0 = f01.x * up, q1 = f01.y * up, q2 = f23.x * up, q3 = f23.y * up;
+                        const uint32_t h01 = f32x2_to_e4m3x2(q0, q1), h23 = f32x2_to_e4m3x2(q2, q3);
+                        const float2 b01 = f16x2_to_float2(e4m3x2_to_f16x2_u(h01));
+                        const float2 b23 = f16x2_to_float2(e4m3x2_to_f16x2_u(h23));
+                        hw[i] = h01 | (h23 << 16);
+                        lw[i] = f32x2_to_e4m3x2(q0 - b01.x, q1 - b01.y) | (f32x2_to_e4m3x2(q2 - b23.x, q3 - b23.y) << 16);
+                    }
+                    *reinterpret_cast<uint4*>(qt + ((c ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(qt + kQHalf + ((c ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                fence_proxy_async_smem();  // the S MMAs (async proxy) read what was written
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * kBarQConv);
+        }
+        if constexpr (NARROW == 2) {
+            // INT8 caches: the MMAs run on f16 operands, so Q (bf16, landed by TMA) is converted in place, each
             // query tile by its own four warps; exact for |q| in [2^-14, 65504], larger values raise Q_RANGE
             bool ok_q = !active || __all_sync(kFull, mbar_spin_bounded(bar + 8 * kBarQFull, 0, a.timeout_ns));
             if (!ok_q) *abort_flag = 1;
@@ -588,14 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool need = mt > m_ref + 8.f;
             // O is rescaled (below) only when some row of the warp needs it; rows that do not keep alpha = 1
             const bool rescale = j > 0 && __any_sync(kFull, need);
-            const float m_new = need ? mt : m_ref;
+            const float m_new = need ? (NARROW == 1 ? mt - kP8Shift : mt) : m_ref;
             const float alpha = ex2_approx(m_ref - m_new);
             m_ref = m_new;
             // exponent arguments and running sums on packed fp32 pairs (two elements per instruction); the
             // masked form (edge tiles only) is a separate instance so the common path carries no selects
             const float2 sc2 = make_float2(sm_log2, sm_log2), nm2 = make_float2(-m_ref, -m_ref);
             float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t pk[32];
+            uint32_t pk[32];  // bf16 / f16 pairs; FP8: 16 words of four hi codes, then 16 of four lo codes
             auto exp_pack = [&](auto with_mask) {
 #pragma unroll
                 for (int i = 0; i < 64; i += 2) {
@@ -609,6 +737,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ls2[(i >> 1) & 1] = __fadd2_rn(ls2[(i >> 1) & 1], make_float2(p0, p1));
                     if constexpr (NARROW != 0) pk[i / 2] = f16x2_rn(p0, p1);
                     else pk[i / 2] = bf16x2_rn(p0, p1);
+                }
+                if constexpr (NARROW == 1) {
+                    // the f16 probabilities (at most 2^8) split into two E4M3 parts for the 8-bit P.V MMAs
+                    uint32_t hl[32];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) split_e4m3x4(pk[2 * k], pk[2 * k + 1], hl[k], hl[16 + k]);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) pk[k] = hl[k];
                 }
             };
             if (masked) exp_pack(std::true_type{});
@@ -644,9 +780,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                for (int idx = tid; idx < (kKeys - nvalid) * 16; idx += kSoftmax / 2) {
-                    const int row = nvalid + idx / 16, hf = (idx / 8) & 1, ch = idx & 7;
-                    *reinterpret_cast<uint4*>(smem + kOffV + (2 * st + hf) * kKvHalf + row * 128 + ch * 16) = z;
+                if constexpr (NARROW == 1) {  // one 128-byte line of codes per key
+                    for (int idx = tid; idx < (kKeys - nvalid) * 8; idx += kSoftmax / 2) {
+                        const int row = nvalid + idx / 8, ch = idx & 7;
+                        *reinterpret_cast<uint4*>(smem + kOffV + st * kStage + row * 128 + ch * 16) = z;
+                    }
+                } else {
+                    for (int idx = tid; idx < (kKeys - nvalid) * 16; idx += kSoftmax / 2) {
+                        const int row = nvalid + idx / 16, hf = (idx / 8) & 1, ch = idx & 7;
+                        *reinterpret_cast<uint4*>(smem + kOffV + st * kStage + hf * kKvHalf + row * 128 + ch * 16) = z;
+                    }
                 }
                 fence_proxy_async_smem();
             }
@@ -701,7 +844,9 @@ static size_t ws_smem_bytes() {
     return static_cast<size_t>(Plan<NARROW>::kOffMeta) + kMetaCount + 4 * (kMaxSeqs + 1) + 1024;
 }
 
-size_t prefill_ws_smem_bytes(int narrow) { return narrow ? ws_smem_bytes<1>() : ws_smem_bytes<0>(); }
+size_t prefill_ws_smem_bytes(int narrow) {
+    return narrow == 2 ? ws_smem_bytes<2>() : narrow == 1 ? ws_smem_bytes<1>() : ws_smem_bytes<0>();
+}
 
 int prefill_ws_max_seqs() { return kMaxSeqs; }
 
@@ -709,7 +854,7 @@ template <int NARROW>
 static cudaError_t launch_ws(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              const PrefillArgs& a, cudaStream_t stream) {
     const size_t smem = ws_smem_bytes<NARROW>();
-    constexpr bool kAdapt = NARROW != 0;
+    constexpr bool kAdapt = NARROW == 2;
     const bool adapt = kAdapt && a.cu_q != nullptr;
     cudaError_t e = cudaFuncSetAttribute(
         adapt ? paged_prefill_ws_kernel<NARROW, kAdapt> : paged_prefill_ws_kernel<NARROW, false>,

@@ -277,20 +277,24 @@ def test_prefill_chunk_edge_shapes(NQ, q_start, Hq, Hkv, S):
     assert_close("bf16", got, ref, f"prefill NQ={NQ} q_start={q_start} G={Hq // Hkv} S={S}")
 
 
-@pytest.mark.parametrize("kv", ["e4m3", "i8"])
-def test_prefill_one_byte_cache_query_out_of_f16_range_is_flagged(kv):
-    """One-byte caches run the tile's products on f16 operands: a query value the f16 range cannot hold raises
-    PKV_DEVERR_Q_RANGE (0x10); the other rows still match the oracle."""
+@pytest.mark.parametrize("kv,bits,flagged", [
+    ("i8", 0x47C8, True),     # 102400: INT8 caches run the products on f16 operands, which cannot hold it
+    ("e4m3", 0x47C8, False),  # FP8 caches scale each query row by a power of two first: any finite value is fine
+    ("e4m3", 0x7F80, True),   # +inf is flagged on FP8 caches
+])
+def test_prefill_one_byte_cache_query_range(kv, bits, flagged):
+    """A query value the tile's operands cannot carry raises PKV_DEVERR_Q_RANGE (0x10): beyond the f16 range for
+    INT8 caches, non-finite for FP8 caches.  The rows without that value match the oracle either way."""
     q, kc, vc, table, kv_len = _chunk_case(40, 100, 8, 1, 16, seed=13, kv=kv)
     q = q.copy()
-    q[5, 3, 7] = 0x47C8  # bf16 bits of 102400
+    q[5, 3, 7] = bits
     dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
     out = torch.empty_like(dq)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     pkv.pkv_paged_prefill_chunk(out, dq, 100, dk, dv, B.CacheDesc.for_cache(dk, 0.25, 0.5), to_device(table),
                                 kv_len, 1 / np.sqrt(128), err)
     torch.cuda.synchronize()
-    assert err.item() & 0x10
+    assert bool(err.item() & 0x10) == flagged
     code = {"e4m3": oracle.E4M3, "i8": oracle.I8}[kv]
     rows = [0, 1, 20, 39]
     ref = oracle.paged_prefill_chunk(q, 100, kc, vc, table, kv_len, 1 / np.sqrt(128), rows=rows, cache_dtype=code,
@@ -299,8 +303,9 @@ def test_prefill_one_byte_cache_query_out_of_f16_range_is_flagged(kv):
 
 
 def test_fp8_prefill_query_rows_of_wide_range():
-    """Query rows mixing values from 2^-12 to 2^6 (and exact zeros) over an FP8 cache: the tile takes q to f16,
-    which holds every one of them exactly, so the chunk matches the oracle."""
+    """Query rows mixing values from 2^-12 to 2^6 (and exact zeros) over an FP8 cache: the tile scales each row by a
+    power of two and splits it into two E4M3 parts, exact for values within 2^-10 of the row's largest and within
+    2^-18 of it in absolute terms below that, so the chunk matches the oracle."""
     q, kc, vc, table, kv_len = _chunk_case(70, 250, 16, 2, 16, seed=17, kv="e4m3")
     rng = np.random.default_rng(5)
     mag = np.exp2(rng.integers(-12, 7, size=q.shape)).astype(np.float32)
