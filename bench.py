@@ -316,7 +316,7 @@ def rank_workload_kwargs(config: str, rank: int, batch: int = 0) -> dict:
     kw = {"seed": wl.CONFIG_SEEDS[config] + 1000 * rank} if config != "llama70b_mixed_fp8" else {}
     if config == "llama70b_mixed_fp8" and rank:
         kw["seed"] = wl.CONFIG_SEEDS[config] + 1000 * rank
-    if batch and config in ("llama3_8b_gqa", "llama70b_mixed_bf16", "llama70b_mixed_fp8"):
+    if batch and config in ("llama3_8b_gqa", "llama3_8b_gqa_int8", "llama70b_mixed_bf16", "llama70b_mixed_fp8"):
         kw["batch"] = batch
     return kw
 

@@ -66,8 +66,9 @@ typedef enum {
 #define PKV_DEVERR_BAD_BLOCK 0x2    /* block id < 0 or >= num_blocks where one must be read */
 #define PKV_DEVERR_BAD_LENGTH 0x4   /* context_len < 0 or > max_blocks_per_seq * block_size */
 #define PKV_DEVERR_TIMEOUT 0x8      /* a bounded wait on an async copy gave up */
-#define PKV_DEVERR_Q_RANGE 0x10     /* a query value beyond the f16 range (|q| >= 65520) in a prefill or decode
-                                       over an FP8 or INT8 cache, whose tensor-core products run on f16 operands */
+#define PKV_DEVERR_Q_RANGE 0x10     /* a query value the tensor-core operands cannot carry: beyond the f16 range
+                                       (|q| >= 65520) in a decode over an FP8 or INT8 cache or a prefill over an
+                                       INT8 cache (f16 operands); non-finite in a prefill over an FP8 cache */
 
 /* Description of one layer's K and V cache pools. */
 typedef struct {
@@ -176,16 +177,25 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
  * q_start_pos + i) and query head hq (KV head hq / G) attend causally:
  *   out[i][hq] = softmax(scale * q[i][hq] . K[0 .. q_start_pos + i]^T) V[0 .. q_start_pos + i]
  * with K/V gathered through block_table (one sequence, ceil(kv_len / S)
- * entries).  Runs on the tensor cores: bf16 inputs, fp32 accumulation, the
- * softmax weights rounded to bf16 for the P.V product.  An FP8 or INT8 cache
- * is widened to f16 on chip (exactly), the queries are taken to f16 (exact for
- * |q| in [2^-14, 65504]; a value of 65520 or more sets PKV_DEVERR_Q_RANGE), the
- * softmax weights are rounded to f16, and the per-tensor or per-head scales
- * are applied to the scores and the output.
+ * entries).  Runs on the tensor cores with fp32 accumulation:
+ *   - bf16 cache: bf16 inputs, the softmax weights rounded to bf16 for P.V.
+ *   - FP8 cache: 8-bit (E4M3) products on the cached codes as they are.  Each
+ *     query row is scaled by a power of two (its largest magnitude to
+ *     [128, 256)) and split into two E4M3 parts, hi + lo, which carry it
+ *     exactly for elements within 2^-10 of the row's largest and to 2^-18 of
+ *     that largest below; the softmax weights are split the same way (about
+ *     8 significant bits, like bf16).  A non-finite query value sets
+ *     PKV_DEVERR_Q_RANGE.
+ *   - INT8 cache: the codes are widened to f16 on chip (exactly), the queries
+ *     are taken to f16 (exact for |q| in [2^-14, 65504]; a value of 65520 or
+ *     more sets PKV_DEVERR_Q_RANGE), the softmax weights rounded to f16.
+ *   The per-tensor or per-head scales are applied to the scores and the output.
  *   q, out: [num_q_tokens][num_q_heads][128] bf16.
  * scale must be positive.
- * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
- *   G = num_q_heads / num_kv_heads dividing 128.  No workspace.
+ * Supported (narrower than the decode call): bf16 queries, bf16, FP8 or INT8
+ *   cache, head_dim 128 only, block_size 8/16/32 only (a 64-key tile is copied
+ *   as whole blocks), G = num_q_heads / num_kv_heads dividing 128; other shapes
+ *   return PKV_ERR_UNSUPPORTED.  No workspace.
  */
 pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,
                                    int32_t q_start_pos, const void* k_cache, const void* v_cache,
@@ -211,12 +221,11 @@ pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, in
  * total_q_tokens, kv_len too short, more table entries than max_blocks_per_seq)
  * sets PKV_DEVERR_BAD_LENGTH and leaves that chunk's rows unwritten; a table
  * entry outside the pool sets PKV_DEVERR_BAD_BLOCK.
- * An FP8 or INT8 cache is widened to f16 on chip (exactly), with f16 queries
- * and softmax weights and its scales applied to the scores and the output, as
- * in pkv_paged_prefill_chunk.
+ * The arithmetic per cache type is that of pkv_paged_prefill_chunk.
  * scale must be positive.
- * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128, block_size 8/16/32,
- *   G dividing 128, num_seqs <= 2048.  No workspace.
+ * Supported (narrower than the decode call): bf16 queries, bf16, FP8 or INT8
+ *   cache, head_dim 128 only, block_size 8/16/32 only, G dividing 128,
+ *   num_seqs <= 2048; other shapes return PKV_ERR_UNSUPPORTED.  No workspace.
  */
 pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
                                     const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,

@@ -32,6 +32,22 @@ PKV_EXTERN_ALL(KvI8, KvBF16)
 #undef PKV_EXTERN_ALL
 #undef PKV_EXTERN_GD
 #undef PKV_EXTERN
+// The tensor-core form's instantiations live in decode_mma_{bf16,fp8,i8}_s{4,8,16,32}.cu.
+#define PKV_EXTERN_MMA(S_, KV_, G_, HP_)                                                                    \
+    extern template cudaError_t launch_paged_decode_mma<G_, S_, KV_, HP_>(                                  \
+        const CUtensorMap&, const CUtensorMap&, const DecodeArgs&, int, int, size_t, cudaStream_t);
+#define PKV_EXTERN_MMA_GH(S_, KV_)                                                                          \
+    PKV_EXTERN_MMA(S_, KV_, 1, 1) PKV_EXTERN_MMA(S_, KV_, 2, 1) PKV_EXTERN_MMA(S_, KV_, 4, 1)                \
+    PKV_EXTERN_MMA(S_, KV_, 8, 1) PKV_EXTERN_MMA(S_, KV_, 1, 2) PKV_EXTERN_MMA(S_, KV_, 2, 2)                \
+    PKV_EXTERN_MMA(S_, KV_, 4, 2) PKV_EXTERN_MMA(S_, KV_, 8, 2)
+#define PKV_EXTERN_MMA_ALL(KV_)                                                                             \
+    PKV_EXTERN_MMA_GH(4, KV_) PKV_EXTERN_MMA_GH(8, KV_) PKV_EXTERN_MMA_GH(16, KV_) PKV_EXTERN_MMA_GH(32, KV_)
+PKV_EXTERN_MMA_ALL(KvBF16)
+PKV_EXTERN_MMA_ALL(KvE4M3)
+PKV_EXTERN_MMA_ALL(KvI8)
+#undef PKV_EXTERN_MMA_ALL
+#undef PKV_EXTERN_MMA_GH
+#undef PKV_EXTERN_MMA
 
 // ------------------------------------------------------------------ error detail
 
