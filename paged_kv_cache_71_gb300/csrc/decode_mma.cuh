@@ -281,6 +281,137 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     };
 
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+    // The query rows of the pair whose first block follows stream position x, when the metadata window holds it:
+    // prefetched into L2 (HP G rows of 256 bytes, contiguous), so that the next segment's own loads hit L2 instead
+    // of waiting on DRAM behind the K/V stream.
+    auto prefetch_next_q = [&](int x) {
+        const unsigned f0 = __ballot_sync(kFull, (cur.c & kMetaFirst) && wbase + lane > x);
+        const unsigned f1 = __ballot_sync(kFull, (nxt.c & kMetaFirst) && wbase + 32 + lane > x);
+        if ((f0 | f1) == 0) return;
+        const int sl = f0 ? __ffs(f0) - 1 : __ffs(f1) - 1;
+        const int na = __shfl_sync(kFull, f0 ? cur.a : nxt.a, sl);
+        if (lane < HP * G * 2) {
+            const uint8_t* q0 = reinterpret_cast<const uint8_t*>(a.q) +
+                                (static_cast<size_t>(na >> 10) * a.Hq + static_cast<size_t>(na & 1023) * HP * G) * D * 2;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(q0 + lane * 128));
+        }
+    };
+    // A cut pair's ticket: the atomic's result is read only at the next segment's end (or at the end of the
+    // share), so that its round trip does not stall the stream; the last finisher then merges the pair.
+    int pend_s = -1, pend_u = 0, pend_blocks = 0, pend_old = 0;
+
+    // the 32 output dims of thread (g, t), in runs of 16 contiguous dims: one-byte caches 32t .. 32t+31; bf16
+    // caches 16t .. 16t+15 and 64+16t .. 64+16t+15 (output tile n, column 2t / 2t+1 is dim 8 (2t) + n / 8 (2t+1)
+    // + n for n < 8, and 64 + the same for tile 8 + n)
+    auto dim_of = [&](int i) { return B16 ? (i < 16 ? 16 * t + i : 64 + 16 * t + i - 16) : 32 * t + i; };
+    // head hh's O in dim_of order
+    auto o_row = [&](const float (&o)[16][4], int hh, float (&v)[32]) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            if constexpr (B16) {
+                v[n] = o[n][2 * hh];
+                v[8 + n] = o[n][2 * hh + 1];
+                v[16 + n] = o[8 + n][2 * hh];
+                v[24 + n] = o[8 + n][2 * hh + 1];
+            } else {
+                v[n] = o[n][2 * hh];
+                v[8 + n] = o[8 + n][2 * hh];
+                v[16 + n] = o[n][2 * hh + 1];
+                v[24 + n] = o[8 + n][2 * hh + 1];
+            }
+        }
+    };
+    // out[s][query head (u HP + hh) G + g][dim_of(i)], bf16
+    auto store_row = [&](int s, int u, int hh, const float (&x)[32], float inv) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            wv[i] = static_cast<uint32_t>(float_to_bf16_bits(x[2 * i] * inv)) |
+                    (static_cast<uint32_t>(float_to_bf16_bits(x[2 * i + 1] * inv)) << 16);
+        uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                        (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(u * HP + hh) * G + g) * D * 2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(orow + dim_of(8 * i) * 2) =
+                make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+    };
+    auto out_mul = [&](int u, int hh) { return a.v_head ? __ldg(a.v_head + u * HP + hh) : a.o_mul; };
+    const size_t rec_floats = static_cast<size_t>(GU) * (D + 2);
+
+    // Merge of pair (s, u) by its last finisher: the shares that hold a segment of it are found 32 workers at a
+    // time (one per lane; shares are contiguous in worker order), and their records are combined in stream order
+    // with each record's loads issued before the previous one is combined.
+    auto merge_pair = [&](int s, int u) {
+        __threadfence();
+        const int nb = P[s + 1] - P[s];
+        const int U0 = Hu * P[s] + u * nb;
+        const int U1 = U0 + nb;
+        int w_first = 0;  // the last worker at or before w whose share starts at or before the pair
+        for (int base = w;; base -= 32) {
+            const int cand = base - lane;
+            const unsigned okm = __ballot_sync(kFull, cand < 0 || split.start(cand) <= U0);
+            if (okm) {
+                w_first = max(0, base - (__ffs(okm) - 1));
+                break;
+            }
+        }
+#pragma unroll 1
+        for (int hh = 0; hh < HP; ++hh) {  // one head at a time: 32 accumulators live
+            const int row = hh * G + g;
+            float Mx = -INFINITY, Ls = 0.f, acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+            for (int base = w_first; base < W; base += 32) {
+                // lane i: worker base + i, whether its (non-empty) share holds a segment of the pair, and which slot
+                const int cand = base + lane;
+                const int c0 = cand < W ? split.start(cand) : T;
+                const int c1 = cand < W ? split.start(cand + 1) : T;
+                const unsigned cm = __ballot_sync(kFull, cand < W && c0 < U1 && c1 > c0);
+                const int slot_l = c0 >= U0 ? 0 : 1;
+                const unsigned long long rec_l = reinterpret_cast<unsigned long long>(
+                    a.partials + (static_cast<size_t>(cand < W ? cand : 0) * 2 + slot_l) * rec_floats);
+                for (unsigned m = cm; m != 0; m &= m - 1) {
+                    const float* r = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
+                    if (g < G) {
+                        const float mr = __ldcg(r + GU * D + row);
+                        const float lr = __ldcg(r + GU * D + GU + row);
+                        float4 ov[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            if constexpr (GU % 2 == 0) {
+                                ov[i] = __ldcg(reinterpret_cast<const float4*>(r + row * D + dim_of(4 * i)));
+                            } else {
+                                const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)));
+                                const float2 o23 =
+                                    __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)) + 1);
+                                ov[i] = make_float4(o01.x, o01.y, o23.x, o23.y);
+                            }
+                        }
+                        const float mn = fmaxf(Mx, mr);
+                        const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
+                        const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
+                        Ls = Ls * fo + lr * fr;
+                        Mx = mn;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            acc[4 * i] = acc[4 * i] * fo + ov[i].x * fr;
+                            acc[4 * i + 1] = acc[4 * i + 1] * fo + ov[i].y * fr;
+                            acc[4 * i + 2] = acc[4 * i + 2] * fo + ov[i].z * fr;
+                            acc[4 * i + 3] = acc[4 * i + 3] * fo + ov[i].w * fr;
+                        }
+                    }
+                }
+                if (!(__ballot_sync(kFull, cand < W && c1 < U1) >> 31 & 1u)) break;  // the pair ends in this round
+            }
+            if (g < G) store_row(s, u, hh, acc, Ls > 0.f ? out_mul(u, hh) / Ls : 0.f);
+        }
+    };
+    auto resolve_pending = [&]() {
+        if (pend_s < 0) return;
+        const int old = __shfl_sync(kFull, pend_old, 0);
+        if (old + pend_blocks == P[pend_s + 1] - P[pend_s]) merge_pair(pend_s, pend_u);
+        pend_s = -1;
+    };
     int k = 0;
     int st = 0;       // stage of stream index k (k % depth)
     uint32_t ph = 0;  // its phase parity ((k / depth) & 1)
@@ -440,9 +571,10 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
             if (!wait_stage(k, st, ph)) return;
             const uint32_t sp = wreg_u32 + static_cast<uint32_t>(st) * a.stage_bytes;
             if (first) {
-                // Q of this (s, unit) from global memory: for each head hh of the unit, row g, the head dims this
-                // thread's K operand holds, in the same permuted k order (one-byte caches: dims 32t .. 32t+31,
-                // bf16 -> f16; bf16 caches: dims 16t .. 16t+15 and 64+16t .. 64+16t+15 as they are)
+                // Q of this (s, unit): for each head hh of the unit, row g, the head dims this thread's K operand
+                // holds, in the same permuted k order (one-byte caches: dims 32t .. 32t+31, bf16 -> f16; bf16
+                // caches: dims 16t .. 16t+15 and 64+16t .. 64+16t+15 as they are)
+                prefetch_next_q(x);
                 seg_first = mc & kMetaFirst;
                 bool in_range = true;
 #pragma unroll
@@ -527,42 +659,6 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         // ------------------------------------------------ end of segment
         const int s = ma >> 10, u = ma & 1023;
         const int nb = P[s + 1] - P[s];
-        // the 32 output dims of thread (g, t), in runs of 16 contiguous dims: one-byte caches 32t .. 32t+31; bf16
-        // caches 16t .. 16t+15 and 64+16t .. 64+16t+15 (output tile n, column 2t / 2t+1 is dim 8 (2t) + n / 8 (2t+1)
-        // + n for n < 8, and 64 + the same for tile 8 + n)
-        auto dim_of = [&](int i) { return B16 ? (i < 16 ? 16 * t + i : 64 + 16 * t + i - 16) : 32 * t + i; };
-        // head hh's O in dim_of order
-        auto o_row = [&](int hh, float (&v)[32]) {
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                if constexpr (B16) {
-                    v[n] = o[n][2 * hh];
-                    v[8 + n] = o[n][2 * hh + 1];
-                    v[16 + n] = o[8 + n][2 * hh];
-                    v[24 + n] = o[8 + n][2 * hh + 1];
-                } else {
-                    v[n] = o[n][2 * hh];
-                    v[8 + n] = o[8 + n][2 * hh];
-                    v[16 + n] = o[n][2 * hh + 1];
-                    v[24 + n] = o[8 + n][2 * hh + 1];
-                }
-            }
-        };
-        // out[s][query head (u HP + hh) G + g][dim_of(i)], bf16
-        auto store_row = [&](int hh, const float (&x)[32], float inv) {
-            uint32_t wv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                wv[i] = static_cast<uint32_t>(float_to_bf16_bits(x[2 * i] * inv)) |
-                        (static_cast<uint32_t>(float_to_bf16_bits(x[2 * i + 1] * inv)) << 16);
-            uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
-                            (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(u * HP + hh) * G + g) * D * 2;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint4*>(orow + dim_of(8 * i) * 2) =
-                    make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
-        };
-        auto out_mul = [&](int hh) { return a.v_head ? __ldg(a.v_head + u * HP + hh) : a.o_mul; };
 #pragma unroll
         for (int hh = 0; hh < HP; ++hh) {
             l_run[hh] += __shfl_xor_sync(kFull, l_run[hh], 1);
@@ -574,16 +670,16 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
 #pragma unroll
                 for (int hh = 0; hh < HP; ++hh) {
                     float v[32];
-                    o_row(hh, v);
-                    store_row(hh, v, l_run[hh] > 0.f ? out_mul(hh) / l_run[hh] : 0.f);
+                    o_row(o, hh, v);
+                    store_row(s, u, hh, v, l_run[hh] > 0.f ? out_mul(u, hh) / l_run[hh] : 0.f);
                 }
             }
+            resolve_pending();
             continue;
         }
         // partial record of this segment: O[GU][D], m[GU], l[GU] (row hh G + g for head hh).  A record is
         // GU * (D + 2) floats, so records are 16-byte aligned for even GU and only 8-byte aligned for GU = 1: the O
         // runs move as float4 or as float2 pairs.
-        const size_t rec_floats = static_cast<size_t>(GU) * (D + 2);
         {
             const int slot = (seg_x0 == A0) ? 0 : 1;
             float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
@@ -591,7 +687,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
 #pragma unroll
                 for (int hh = 0; hh < HP; ++hh) {
                     float v[32];
-                    o_row(hh, v);
+                    o_row(o, hh, v);
                     const int row = hh * G + g;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -611,63 +707,16 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                 }
             }
         }
+        resolve_pending();  // the previous cut pair, whose ticket result has long arrived
         __threadfence();
         __syncwarp();
-        int old = 0;
-        const int seg_blocks = x_last - seg_x0 + 1;
-        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hu + u], seg_blocks);
-        old = __shfl_sync(kFull, old, 0);
-        if (old + seg_blocks != nb) continue;
-
-        // last finisher of pair (s, unit): merge its segments in stream order
-        __threadfence();
-        const int U0 = Hu * P[s] + u * nb;
-        const int U1 = U0 + nb;
-#pragma unroll
-        for (int hh = 0; hh < HP; ++hh) {
-            const int row = hh * G + g;
-            float Mx = -INFINITY, Ls = 0.f;
-            float acc[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            int wq = w, ys = A0;
-            while (ys > U0 && wq > 0) ys = split.start(--wq);
-            while (ys < U1 && wq < W) {
-                const int ye = split.start(wq + 1);
-                if (ye > ys && g < G) {  // a non-empty share holds one segment of the pair
-                    const int sl = (ys >= U0) ? 0 : 1;
-                    const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
-                    const float mr = __ldcg(r + GU * D + row);
-                    const float lr = __ldcg(r + GU * D + GU + row);
-                    const float mn = fmaxf(Mx, mr);
-                    const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
-                    const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
-                    Ls = Ls * fo + lr * fr;
-                    Mx = mn;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float4 ov;
-                        if constexpr (GU % 2 == 0) {
-                            ov = __ldcg(reinterpret_cast<const float4*>(r + row * D + dim_of(4 * i)));
-                        } else {
-                            const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)));
-                            const float2 o23 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)) + 1);
-                            ov = make_float4(o01.x, o01.y, o23.x, o23.y);
-                        }
-                        acc[4 * i] = acc[4 * i] * fo + ov.x * fr;
-                        acc[4 * i + 1] = acc[4 * i + 1] * fo + ov.y * fr;
-                        acc[4 * i + 2] = acc[4 * i + 2] * fo + ov.z * fr;
-                        acc[4 * i + 3] = acc[4 * i + 3] * fo + ov.w * fr;
-                    }
-                }
-                ++wq;
-                ys = ye;
-            }
-            if (g < G) store_row(hh, acc, Ls > 0.f ? out_mul(hh) / Ls : 0.f);
-        }
+        pend_s = s;
+        pend_u = u;
+        pend_blocks = x_last - seg_x0 + 1;
+        if (lane == 0) pend_old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hu + u], pend_blocks);
     }
+    resolve_pending();
 }
-
 // Host-side launch for one instantiation (defined in decode_mma_*.cu).
 template <int G, int S, class KV, int HP>
 cudaError_t launch_paged_decode_mma(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,
