@@ -159,10 +159,11 @@ DECODE_SOURCES = ("decode.cuh", "pkv_device.cuh", "decode_bf16_s16.cu")
 
 def decode_kernel(w) -> tuple[str, tuple]:
     """The decode kernel a workload runs on, and the sources its profile digest covers: FP8 / INT8 caches with
-    128-dim heads, and bf16 caches of 128-dim heads in GQA groups of 8, take the tensor-core form, everything else
-    the CUDA-core form."""
+    128-dim heads, and bf16 caches of 128-dim heads in GQA groups of 8 (or any group when the batch shares blocks
+    and takes the shared-block form), take the tensor-core form, everything else the CUDA-core form."""
     G = w.num_q_heads // w.num_kv_heads
-    if w.head_dim == 128 and (w.kv_dtype in ("e4m3", "i8") or (w.kv_dtype == "bf16" and G >= 8)):
+    shared = bool(w.notes.get("shared_blocks"))
+    if w.head_dim == 128 and (w.kv_dtype in ("e4m3", "i8") or (w.kv_dtype == "bf16" and (G >= 8 or shared))):
         tag = {"e4m3": "fp8", "i8": "i8", "bf16": "bf16"}[w.kv_dtype]
         return "paged_decode_mma_kernel", ("decode_mma.cuh", "decode.cuh", "pkv_device.cuh",
                                            f"decode_mma_{tag}_s{w.block_size}.cu")
@@ -620,9 +621,11 @@ def paged_vs_contiguous(args, w, st, flush, stream) -> dict:
     def paged():
         st.attend(stream)
 
-    def contiguous():
-        B.pkv_paged_attention_decode(out_c, st.q, kc, vc, desc, dt, st.context_lens, w.scale, st.num_splits,
-                                     st.max_context_len, ws_c, st.err, stream)
+    fn = B.pkv_paged_attention_decode_shared if st.shared else B.pkv_paged_attention_decode
+
+    def contiguous():  # the same decode form as the paged launch
+        fn(out_c, st.q, kc, vc, desc, dt, st.context_lens, w.scale, st.num_splits, st.max_context_len, ws_c, st.err,
+           stream)
 
     def timed(fn, n):
         ts = []

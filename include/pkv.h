@@ -170,6 +170,34 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype,
                                       void* stream);
 
 /*
+ * Paged decode attention over a batch whose sequences share physical blocks:
+ * forked samples or beams, or sequences with a common prompt prefix, whose
+ * tables name the same blocks ("3.3 批处理与内存管理", section "共享与写时复制":
+ * blocks with a reference count above one).  Same arguments, result,
+ * workspace and errors as pkv_paged_attention_decode (the size returned by
+ * pkv_paged_attention_workspace_size is enough for this call).  A caller whose
+ * block manager knows that the batch shares blocks calls this form.
+ *
+ * Every sequence still reads each of its blocks through its own table.  A
+ * shared block is fetched from DRAM once and re-read from L2 by the other
+ * sequences that hold it, so the K/V arrive faster than HBM delivers them and
+ * the instruction cost per byte becomes the bound.  For bf16 caches of 128-dim
+ * heads this form therefore runs the tensor-core kernel (one KV head per work
+ * unit) at every GQA group, where pkv_paged_attention_decode keeps groups
+ * below 8 on the CUDA cores, which stream DRAM-resident blocks slightly
+ * faster.  For every other cache it is identical to pkv_paged_attention_decode.
+ */
+pkv_status pkv_paged_attention_decode_shared(void* out, const void* q, int32_t q_dtype,
+                                             const void* k_cache, const void* v_cache,
+                                             const pkv_cache_desc* cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens, int32_t num_seqs,
+                                             int32_t num_q_heads, float scale, int32_t num_splits,
+                                             int32_t max_context_len, void* workspace,
+                                             size_t workspace_bytes, int32_t* device_error,
+                                             void* stream);
+
+/*
  * One chunk of a chunked prefill ("3.3 批处理与内存管理", section "分块预填充":
  * the chunk's queries attend to a KV cache that already holds the earlier
  * chunks).  The chunk's own K/V must already be written (pkv_reshape_and_cache),

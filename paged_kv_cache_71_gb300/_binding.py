@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
     L.pkv_reshape_and_cache.argtypes = [P, P, i32, P, i32, P, P, D, P, P]
     L.pkv_paged_attention_workspace_size.argtypes = [D, i32, i32, i32, ctypes.POINTER(sz)]
     L.pkv_paged_attention_decode.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32, P, sz, P, P]
+    L.pkv_paged_attention_decode_shared.argtypes = L.pkv_paged_attention_decode.argtypes
     L.pkv_copy_blocks.argtypes = [P, P, D, P, i32, P, P]
     L.pkv_paged_attention_decode_static_scratch.argtypes = [P, P, i32, P, P, D, P, i32, P, i32, i32, f32, i32, i32,
                                                             P, P]
@@ -149,6 +150,20 @@ def pkv_paged_attention_decode(out, q, k_cache, v_cache, cache: CacheDesc, block
                                             int(num_splits), int(max_context_len), _ptr(workspace), ws_bytes,
                                             _ptr(device_error), _stream(stream)),
            "pkv_paged_attention_decode")
+
+
+def pkv_paged_attention_decode_shared(out, q, k_cache, v_cache, cache: CacheDesc, block_tables, context_lens,
+                                      scale: float, num_splits: int = 0, max_context_len: int = 0, workspace=None,
+                                      device_error=None, stream=None) -> None:
+    """pkv_paged_attention_decode for a batch whose tables share physical blocks (same arguments)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_attention_decode_shared(_ptr(out), _ptr(q), _dtype(q), _ptr(k_cache), _ptr(v_cache),
+                                                   ctypes.byref(cache), _ptr(block_tables),
+                                                   int(block_tables.shape[1]), _ptr(context_lens), int(q.shape[0]),
+                                                   int(q.shape[1]), float(scale), int(num_splits),
+                                                   int(max_context_len), _ptr(workspace), ws_bytes,
+                                                   _ptr(device_error), _stream(stream)),
+           "pkv_paged_attention_decode_shared")
 
 
 def pkv_paged_attention_decode_static_scratch(out, q, k_cache, v_cache, cache: CacheDesc, block_tables,

@@ -221,19 +221,24 @@ static int policy_warps(int G, int D) {
 #endif
 
 // Which decode form runs: the tensor-core form for FP8 / INT8 caches and bf16 caches from PKV_BF16_MMA_MIN_G up
-// (128-dim heads), the CUDA-core form otherwise.
-static bool uses_tensor_core(int dtype, int G, int D) {
-    return D == 128 && (narrow(dtype) || (dtype == PKV_BF16 && G >= PKV_BF16_MMA_MIN_G));
+// (128-dim heads), the CUDA-core form otherwise.  The shared-block form (batches whose tables share physical
+// blocks, re-read from L2) takes every bf16 cache of 128-dim heads to the tensor-core form, with one KV head per
+// work unit (its 8 KB stages keep 8 warps per SM; a bf16 head pair's 16 KB stages leave room for 4).
+static bool uses_tensor_core(int dtype, int G, int D, bool shared = false) {
+    return D == 128 && (narrow(dtype) || (dtype == PKV_BF16 && (shared || G >= PKV_BF16_MMA_MIN_G)));
 }
-static int mma_heads_per_unit(int G, int Hkv) { return (G <= PKV_MMA_PAIR_MAX_G && Hkv % 2 == 0) ? 2 : 1; }
+static int mma_heads_per_unit(int G, int Hkv, int dtype, bool shared = false) {
+    if (shared && dtype == PKV_BF16) return 1;
+    return (G <= PKV_MMA_PAIR_MAX_G && Hkv % 2 == 0) ? 2 : 1;
+}
 
 // Split-KV scratch: one completion counter per (sequence, KV head), then two partial (O, m, l) records per worker
 // warp, each over the query heads of one work unit (G, or 2G when the tensor-core form pairs KV heads).
-static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D, int dtype) {
+static size_t workspace_bytes_for(int sms, int B, int Hkv, int G, int D, int dtype, bool shared = false) {
     const size_t tickets = ((static_cast<size_t>(B) * Hkv * 4 + 255) / 256) * 256;
-    const bool tc = uses_tensor_core(dtype, G, D);
+    const bool tc = uses_tensor_core(dtype, G, D, shared);
     const size_t W = static_cast<size_t>(sms) * (tc ? kMmaWarps : policy_warps(G, D));
-    const size_t rows = static_cast<size_t>(G) * (tc ? mma_heads_per_unit(G, Hkv) : 1);
+    const size_t rows = static_cast<size_t>(G) * (tc ? mma_heads_per_unit(G, Hkv, dtype, shared) : 1);
     return tickets + W * 2 * rows * (D + 2) * 4;
 }
 
@@ -441,10 +446,10 @@ static cudaError_t dispatch_mma(int S, int G, int HP, const CUtensorMap& km, con
 // PKV_BF16_MMA_MIN_G up, 128-dim heads.  Its stages hold 128-byte swizzled K and V tiles only (two 64-dim halves per
 // bf16 row), each half starting on a 1024-byte boundary; `a` arrives with everything but the shared-memory plan.
 static pkv_status decode_tensor_core(DecodeArgs a, const pkv_cache_desc& c, int G, int num_seqs, const void* k_cache,
-                                     const void* v_cache, const DeviceInfo& di, cudaStream_t s) {
+                                     const void* v_cache, const DeviceInfo& di, bool shared, cudaStream_t s) {
     const int S = c.block_size, Hkv = c.num_kv_heads;
     const bool b16 = c.dtype == PKV_BF16;
-    const int HP = mma_heads_per_unit(G, Hkv);  // KV heads per work unit
+    const int HP = mma_heads_per_unit(G, Hkv, c.dtype, shared);  // KV heads per work unit
     const uint32_t tile = static_cast<uint32_t>((b16 ? 2 : 1) * std::max(S * 128, 1024));
     a.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));  // one K (or V) tile of one head
     a.q_bytes = 0;  // the query rows are read straight into registers
@@ -507,13 +512,12 @@ PKV_API pkv_status pkv_paged_attention_workspace_size(const pkv_cache_desc* cach
     return PKV_OK;
 }
 
-PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype, const void* k_cache,
-                                              const void* v_cache, const pkv_cache_desc* cache,
-                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                                              float scale, int32_t num_splits, int32_t max_context_len,
-                                              void* workspace, size_t workspace_bytes, int32_t* device_error,
-                                              void* stream) {
+// The decode entry points: `shared` selects the shared-block form (pkv_paged_attention_decode_shared).
+static pkv_status decode_entry(void* out, const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+                               const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                               const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, float scale,
+                               int32_t num_splits, int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                               int32_t* device_error, void* stream, bool shared) {
     g_detail[0] = 0;
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
@@ -562,7 +566,7 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     int32_t* tickets = nullptr;
     float* partials = nullptr;
     if (num_splits != 1) {
-        const size_t need = workspace_bytes_for(di.sms, num_seqs, Hkv, G, D, cache->dtype);
+        const size_t need = workspace_bytes_for(di.sms, num_seqs, Hkv, G, D, cache->dtype, shared);
         if (!workspace || workspace_bytes < need)
             return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                         workspace ? workspace_bytes : static_cast<size_t>(0));
@@ -600,8 +604,9 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
     a.stage_bytes = ((2 * a.kv_bytes + a.q_bytes + 127) / 128) * 128;
     a.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_seqs) + 1) * 4 + 127) / 128 * 128);
     a.timeout_ns = 2000000000ull;
-    if (uses_tensor_core(cache->dtype, G, D))
-        return decode_tensor_core(a, *cache, G, num_seqs, k_cache, v_cache, di, static_cast<cudaStream_t>(stream));
+    if (uses_tensor_core(cache->dtype, G, D, shared))
+        return decode_tensor_core(a, *cache, G, num_seqs, k_cache, v_cache, di, shared,
+                                  static_cast<cudaStream_t>(stream));
     const size_t budget = static_cast<size_t>(di.smem_optin) - 256;  // static shared memory of the kernel
     int nw = policy_warps(G, D), depth = 0;
     while (nw >= 1) {
@@ -639,6 +644,30 @@ PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t 
         e = dispatch_s<KvI8, KvBF16>(S, D, G, km, vm, a, di.sms, nw * 32, smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_attention_decode launch");
     return PKV_OK;
+}
+
+PKV_API pkv_status pkv_paged_attention_decode(void* out, const void* q, int32_t q_dtype, const void* k_cache,
+                                              const void* v_cache, const pkv_cache_desc* cache,
+                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                              float scale, int32_t num_splits, int32_t max_context_len,
+                                              void* workspace, size_t workspace_bytes, int32_t* device_error,
+                                              void* stream) {
+    return decode_entry(out, q, q_dtype, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_q_heads, scale, num_splits, max_context_len, workspace, workspace_bytes,
+                        device_error, stream, false);
+}
+
+PKV_API pkv_status pkv_paged_attention_decode_shared(void* out, const void* q, int32_t q_dtype, const void* k_cache,
+                                                     const void* v_cache, const pkv_cache_desc* cache,
+                                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                     const int32_t* context_lens, int32_t num_seqs,
+                                                     int32_t num_q_heads, float scale, int32_t num_splits,
+                                                     int32_t max_context_len, void* workspace, size_t workspace_bytes,
+                                                     int32_t* device_error, void* stream) {
+    return decode_entry(out, q, q_dtype, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, num_q_heads, scale, num_splits, max_context_len, workspace, workspace_bytes,
+                        device_error, stream, true);
 }
 
 PKV_API pkv_status pkv_paged_prefill_chunk(void* out, const void* q, int32_t q_dtype, int32_t num_q_tokens,

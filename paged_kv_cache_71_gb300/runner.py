@@ -27,9 +27,12 @@ def to_device(a: np.ndarray, dtype: str | None = None, device="cuda") -> torch.T
 class DeviceStep:
     """Device copies of a workload's inputs plus output / workspace buffers."""
 
-    def __init__(self, w: Workload, num_splits: int = 0, device="cuda"):
+    def __init__(self, w: Workload, num_splits: int = 0, device="cuda", shared=None):
         self.w = w
         self.num_splits = num_splits
+        # a batch whose tables share physical blocks takes the shared-block decode form (the host block manager
+        # knows: the workload records its shared blocks)
+        self.shared = bool(w.notes.get("shared_blocks")) if shared is None else bool(shared)
         self.k_cache = to_device(w.k_cache, device=device)
         self.v_cache = to_device(w.v_cache, device=device)
         self.q = to_device(w.q, device=device)
@@ -58,9 +61,9 @@ class DeviceStep:
                                 self.err, stream)
 
     def attend(self, stream=None) -> None:
-        B.pkv_paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache, self.cache, self.block_tables,
-                                     self.context_lens, self.w.scale, self.num_splits, self.max_context_len,
-                                     self.workspace, self.err, stream)
+        fn = B.pkv_paged_attention_decode_shared if self.shared else B.pkv_paged_attention_decode
+        fn(self.out, self.q, self.k_cache, self.v_cache, self.cache, self.block_tables, self.context_lens,
+           self.w.scale, self.num_splits, self.max_context_len, self.workspace, self.err, stream)
 
     def prefill(self, stream=None) -> None:
         if self.pf_q is None:

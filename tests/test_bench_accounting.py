@@ -64,12 +64,13 @@ def test_decode_ceiling_switches_to_fma_where_arithmetic_binds():
 
 def test_decode_kernel_attribution_follows_the_library_policy():
     """The benchmark names the decode kernel a workload runs on as the library dispatches it: the tensor-core form
-    for FP8 / INT8 caches with 128-dim heads and for bf16 caches of 128-dim heads in GQA groups of 8, the CUDA-core
-    form otherwise; only the CUDA-core form is ever reported against the fp32 FMA ceiling."""
+    for FP8 / INT8 caches with 128-dim heads, for bf16 caches of 128-dim heads in GQA groups of 8, and for the
+    prefix-sharing batch (shared-block form), the CUDA-core form otherwise; only the CUDA-core form is ever reported
+    against the fp32 FMA ceiling."""
     import bench
     from paged_kv_cache_71_gb300 import workload as wl
     expect = {"tiny": "paged_decode_kernel", "llama2_7b": "paged_decode_kernel",
-              "llama3_8b_gqa": "paged_decode_kernel", "prefix_shared": "paged_decode_kernel",
+              "llama3_8b_gqa": "paged_decode_kernel", "prefix_shared": "paged_decode_mma_kernel",
               "llama3_8b_gqa_int8": "paged_decode_mma_kernel", "llama70b_mixed_bf16": "paged_decode_mma_kernel",
               "llama70b_mixed_fp8": "paged_decode_mma_kernel"}
     for name, kernel in expect.items():
