@@ -475,6 +475,114 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
         return false;
     };
 
+    const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
+    // out[s][h G + g], this lane's dims, scaled by inv (lanes with tp == 0 store)
+    auto store_rows = [&](int s, int h, const float2 (&o)[G][HP], const float (&inv)[G]) {
+        if (tp != 0) return;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                            (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                float v[EPC];
+#pragma unroll
+                for (int e = 0; e < EPC / 2; ++e) {
+                    v[2 * e] = o[g][c * (EPC / 2) + e].x * inv[g];
+                    v[2 * e + 1] = o[g][c * (EPC / 2) + e].y * inv[g];
+                }
+                store_out<QT, EPC>(orow + static_cast<size_t>((c * LPT + lg) * EPC) * QT::es, v);
+            }
+        }
+    };
+    // Merge of pair (s, h) by its last finisher: the shares that hold a segment of it are found 32 workers at a
+    // time (one per lane; shares are contiguous in worker order) and their records combined in stream order.
+    // Every lane works on the merge: lane (head g, part c) owns dims [c MDP, (c + 1) MDP) of query head h G + g,
+    // and the loads of two records are in flight together.
+    auto merge_pair = [&](int s, int h) {
+        constexpr int MLR = 32 / G;   // lanes per query head
+        constexpr int MDP = D / MLR;  // dims per lane (8-byte pairs: records of one head are 8-byte aligned only)
+        const int r_g = lane / MLR, d0 = (lane % MLR) * MDP;
+        __threadfence();
+        const int nb = P[s + 1] - P[s];
+        const int U0 = Hkv * P[s] + h * nb;
+        const int U1 = U0 + nb;
+        int w_first = 0;  // the last worker at or before w whose share starts at or before the pair
+        for (int base = w;; base -= 32) {
+            const int cand = base - lane;
+            const unsigned okm = __ballot_sync(kFull, cand < 0 || split.start(cand) <= U0);
+            if (okm) {
+                w_first = max(0, base - (__ffs(okm) - 1));
+                break;
+            }
+        }
+        float Mx = -INFINITY, Ls = 0.f, acc[MDP];
+#pragma unroll
+        for (int i = 0; i < MDP; ++i) acc[i] = 0.f;
+        auto load_rec = [&](const float* r, float& m, float& l, float2 (&ov)[MDP / 2]) {
+            m = __ldcg(r + G * D + r_g);
+            l = __ldcg(r + G * D + G + r_g);
+#pragma unroll
+            for (int i = 0; i < MDP / 2; ++i) ov[i] = __ldcg(reinterpret_cast<const float2*>(r + r_g * D + d0) + i);
+        };
+        auto combine = [&](float m, float l, const float2 (&ov)[MDP / 2]) {
+            const float mn = fmaxf(Mx, m);
+            const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
+            const float fr = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            Ls = Ls * fo + l * fr;
+            Mx = mn;
+#pragma unroll
+            for (int i = 0; i < MDP / 2; ++i) {
+                acc[2 * i] = acc[2 * i] * fo + ov[i].x * fr;
+                acc[2 * i + 1] = acc[2 * i + 1] * fo + ov[i].y * fr;
+            }
+        };
+        for (int base = w_first; base < W; base += 32) {
+            const int cand = base + lane;
+            const int c0 = cand < W ? split.start(cand) : T;
+            const int c1 = cand < W ? split.start(cand + 1) : T;
+            const unsigned cm = __ballot_sync(kFull, cand < W && c0 < U1 && c1 > c0);
+            const int slot_l = c0 >= U0 ? 0 : 1;
+            const unsigned long long rec_l = reinterpret_cast<unsigned long long>(
+                a.partials + (static_cast<size_t>(cand < W ? cand : 0) * 2 + slot_l) * rec_floats);
+            unsigned m = cm;
+            while (m != 0) {
+                const float* r0 = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
+                m &= m - 1;
+                float m0, l0;
+                float2 o0[MDP / 2];
+                load_rec(r0, m0, l0, o0);
+                if (m != 0) {
+                    const float* r1 = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
+                    m &= m - 1;
+                    float m1, l1;
+                    float2 o1[MDP / 2];
+                    load_rec(r1, m1, l1, o1);
+                    combine(m0, l0, o0);
+                    combine(m1, l1, o1);
+                } else {
+                    combine(m0, l0, o0);
+                }
+            }
+            if (!(__ballot_sync(kFull, cand < W && c1 < U1) >> 31 & 1u)) break;  // the pair ends in this round
+        }
+        const float inv = (Ls > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / Ls : 0.f;
+#pragma unroll
+        for (int i = 0; i < MDP; ++i) acc[i] *= inv;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                        (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + r_g) * D * QT::es;
+        store_out<QT, MDP>(orow + static_cast<size_t>(d0) * QT::es, acc);
+    };
+    // A cut pair's ticket: the atomic's result is read only at the next segment's end (or at the end of the
+    // share), so that its round trip does not stall the stream; the last finisher then merges the pair.
+    int pend_s = -1, pend_h = 0, pend_blocks = 0, pend_old = 0;
+    auto resolve_pending = [&]() {
+        if (pend_s < 0) return;
+        const int old = __shfl_sync(kFull, pend_old, 0);
+        if (old + pend_blocks == P[pend_s + 1] - P[pend_s]) merge_pair(pend_s, pend_h);
+        pend_s = -1;
+    };
+
     int k = 0;
     while (k < n_blocks) {
         // ------------------------------------------------ one segment: consecutive blocks of one (s, h) pair
@@ -649,31 +757,17 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
         const int nb = P[s + 1] - P[s];
         const bool whole = seg_first && (mc & kMetaLast) && (x_last - seg_x0 + 1 == nb);
         if (whole) {
-            float l_all[G];
+            float inv[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) l_all[g] = __shfl_sync(kFull, l_run, g * DUP);
-            if (tp == 0) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float inv = (l_all[g] > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / l_all[g] : 0.f;
-                    uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
-                                    (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        float v[EPC];
-#pragma unroll
-                        for (int e = 0; e < EPC / 2; ++e) {
-                            v[2 * e] = o2[g][c * (EPC / 2) + e].x * inv;
-                            v[2 * e + 1] = o2[g][c * (EPC / 2) + e].y * inv;
-                        }
-                        store_out<QT, EPC>(orow + static_cast<size_t>((c * LPT + lg) * EPC) * QT::es, v);
-                    }
-                }
+            for (int g = 0; g < G; ++g) {
+                const float l_all = __shfl_sync(kFull, l_run, g * DUP);
+                inv[g] = (l_all > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / l_all : 0.f;
             }
+            store_rows(s, h, o2, inv);
+            resolve_pending();
             continue;
         }
         // partial record of this segment: O[G][D], m[G], l[G]
-        const size_t rec_floats = static_cast<size_t>(G) * (D + 2);
         {
             const int slot = (seg_x0 == A0) ? 0 : 1;
             float* rec = a.partials + (static_cast<size_t>(w) * 2 + slot) * rec_floats;
@@ -692,78 +786,15 @@ __global__ void __launch_bounds__(32 * DecodePolicy<G, D>::warps, 1)
                 rec[G * D + G + gl] = l_run;
             }
         }
+        resolve_pending();  // the previous cut pair, whose ticket result has long arrived
         __threadfence();
         __syncwarp();
-        int old = 0;
-        const int seg_blocks = x_last - seg_x0 + 1;
-        if (lane == 0) old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], seg_blocks);
-        old = __shfl_sync(kFull, old, 0);
-        if (old + seg_blocks != nb) continue;
-
-        // last finisher of pair (s, h): merge its segments in stream order
-        __threadfence();
-        const int U0 = Hkv * P[s] + h * nb;
-        const int U1 = U0 + nb;
-        float Mx[G], Ls[G];
-        float2 acc[G][HP];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            Mx[g] = -INFINITY;
-            Ls[g] = 0.f;
-#pragma unroll
-            for (int i = 0; i < HP; ++i) acc[g][i] = make_float2(0.f, 0.f);
-        }
-        // the workers that cut this pair are consecutive: step down from this one to the first
-        int wq = w, ys = A0;
-        while (ys > U0 && wq > 0) ys = split.start(--wq);
-        while (ys < U1 && wq < W) {
-            const int ye = split.start(wq + 1);
-            if (ye > ys) {  // a non-empty share holds one segment of the pair
-                const int sl = (ys >= U0) ? 0 : 1;
-                const float* r = a.partials + (static_cast<size_t>(wq) * 2 + sl) * rec_floats;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float mr = __ldcg(r + G * D + g);
-                    const float lr = __ldcg(r + G * D + G + g);
-                    const float mn = fmaxf(Mx[g], mr);
-                    const float fo = (Mx[g] == -INFINITY) ? 0.f : ex2_approx(Mx[g] - mn);
-                    const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
-                    Ls[g] = Ls[g] * fo + lr * fr;
-                    Mx[g] = mn;
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c)
-#pragma unroll
-                        for (int e = 0; e < EPC / 2; ++e) {
-                            const float2 ov =
-                                __ldcg(reinterpret_cast<const float2*>(r + g * D + (c * LPT + lg) * EPC + 2 * e));
-                            float2& ac = acc[g][c * (EPC / 2) + e];
-                            ac.x = ac.x * fo + ov.x * fr;
-                            ac.y = ac.y * fo + ov.y * fr;
-                        }
-                }
-            }
-            ++wq;
-            ys = ye;
-        }
-        if (tp == 0) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float inv = (Ls[g] > 0.f) ? (a.v_head ? __ldg(a.v_head + h) : a.o_mul) / Ls[g] : 0.f;
-                uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
-                                (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(h) * G + g) * D * QT::es;
-#pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                    float v[EPC];
-#pragma unroll
-                    for (int e = 0; e < EPC / 2; ++e) {
-                        v[2 * e] = acc[g][c * (EPC / 2) + e].x * inv;
-                        v[2 * e + 1] = acc[g][c * (EPC / 2) + e].y * inv;
-                    }
-                    store_out<QT, EPC>(orow + static_cast<size_t>((c * LPT + lg) * EPC) * QT::es, v);
-                }
-            }
-        }
+        pend_s = s;
+        pend_h = h;
+        pend_blocks = x_last - seg_x0 + 1;
+        if (lane == 0) pend_old = atomicAdd(&a.tickets[static_cast<size_t>(s) * Hkv + h], pend_blocks);
     }
+    resolve_pending();
 }
 
 // Host-side launch for one instantiation (defined in the per-dtype .cu files).

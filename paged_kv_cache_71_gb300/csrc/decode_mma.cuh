@@ -339,9 +339,15 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     const size_t rec_floats = static_cast<size_t>(GU) * (D + 2);
 
     // Merge of pair (s, u) by its last finisher: the shares that hold a segment of it are found 32 workers at a
-    // time (one per lane; shares are contiguous in worker order), and their records are combined in stream order
-    // with each record's loads issued before the previous one is combined.
+    // time (one per lane; shares are contiguous in worker order), and their records are combined in stream order.
+    // Every lane works on the merge: lane (row r, part c) owns dims [c DPL, (c + 1) DPL) of record row r (query
+    // head u GU + r), and the loads of two records are in flight together.
     auto merge_pair = [&](int s, int u) {
+        constexpr int LPR = 32 / GU;    // lanes per record row
+        constexpr int DPL = D / LPR;    // dims per lane
+        constexpr int NV = DPL / 4;     // 16-byte runs per lane (8-byte pairs when GU is odd)
+        constexpr int NBATCH = DPL <= 32 ? 2 : 1;
+        const int r_row = lane / LPR, d0 = (lane % LPR) * DPL;
         __threadfence();
         const int nb = P[s + 1] - P[s];
         const int U0 = Hu * P[s] + u * nb;
@@ -355,55 +361,84 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
                 break;
             }
         }
-#pragma unroll 1
-        for (int hh = 0; hh < HP; ++hh) {  // one head at a time: 32 accumulators live
-            const int row = hh * G + g;
-            float Mx = -INFINITY, Ls = 0.f, acc[32];
+        float Mx = -INFINITY, Ls = 0.f, acc[DPL];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int base = w_first; base < W; base += 32) {
-                // lane i: worker base + i, whether its (non-empty) share holds a segment of the pair, and which slot
-                const int cand = base + lane;
-                const int c0 = cand < W ? split.start(cand) : T;
-                const int c1 = cand < W ? split.start(cand + 1) : T;
-                const unsigned cm = __ballot_sync(kFull, cand < W && c0 < U1 && c1 > c0);
-                const int slot_l = c0 >= U0 ? 0 : 1;
-                const unsigned long long rec_l = reinterpret_cast<unsigned long long>(
-                    a.partials + (static_cast<size_t>(cand < W ? cand : 0) * 2 + slot_l) * rec_floats);
-                for (unsigned m = cm; m != 0; m &= m - 1) {
-                    const float* r = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
-                    if (g < G) {
-                        const float mr = __ldcg(r + GU * D + row);
-                        const float lr = __ldcg(r + GU * D + GU + row);
-                        float4 ov[8];
+        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+        auto load_rec = [&](const float* r, float& m, float& l, float4 (&ov)[NV]) {
+            m = __ldcg(r + GU * D + r_row);
+            l = __ldcg(r + GU * D + GU + r_row);
+            const float* o = r + r_row * D + d0;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            if constexpr (GU % 2 == 0) {
-                                ov[i] = __ldcg(reinterpret_cast<const float4*>(r + row * D + dim_of(4 * i)));
-                            } else {
-                                const float2 o01 = __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)));
-                                const float2 o23 =
-                                    __ldcg(reinterpret_cast<const float2*>(r + row * D + dim_of(4 * i)) + 1);
-                                ov[i] = make_float4(o01.x, o01.y, o23.x, o23.y);
-                            }
-                        }
-                        const float mn = fmaxf(Mx, mr);
-                        const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
-                        const float fr = (mr == -INFINITY) ? 0.f : ex2_approx(mr - mn);
-                        Ls = Ls * fo + lr * fr;
-                        Mx = mn;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            acc[4 * i] = acc[4 * i] * fo + ov[i].x * fr;
-                            acc[4 * i + 1] = acc[4 * i + 1] * fo + ov[i].y * fr;
-                            acc[4 * i + 2] = acc[4 * i + 2] * fo + ov[i].z * fr;
-                            acc[4 * i + 3] = acc[4 * i + 3] * fo + ov[i].w * fr;
-                        }
-                    }
+            for (int i = 0; i < NV; ++i) {
+                if constexpr (GU % 2 == 0) {
+                    ov[i] = __ldcg(reinterpret_cast<const float4*>(o) + i);
+                } else {
+                    const float2 a01 = __ldcg(reinterpret_cast<const float2*>(o) + 2 * i);
+                    const float2 a23 = __ldcg(reinterpret_cast<const float2*>(o) + 2 * i + 1);
+                    ov[i] = make_float4(a01.x, a01.y, a23.x, a23.y);
                 }
-                if (!(__ballot_sync(kFull, cand < W && c1 < U1) >> 31 & 1u)) break;  // the pair ends in this round
             }
-            if (g < G) store_row(s, u, hh, acc, Ls > 0.f ? out_mul(u, hh) / Ls : 0.f);
+        };
+        auto combine = [&](float m, float l, const float4 (&ov)[NV]) {
+            const float mn = fmaxf(Mx, m);
+            const float fo = (Mx == -INFINITY) ? 0.f : ex2_approx(Mx - mn);
+            const float fr = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+            Ls = Ls * fo + l * fr;
+            Mx = mn;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                acc[4 * i] = acc[4 * i] * fo + ov[i].x * fr;
+                acc[4 * i + 1] = acc[4 * i + 1] * fo + ov[i].y * fr;
+                acc[4 * i + 2] = acc[4 * i + 2] * fo + ov[i].z * fr;
+                acc[4 * i + 3] = acc[4 * i + 3] * fo + ov[i].w * fr;
+            }
+        };
+        for (int base = w_first; base < W; base += 32) {
+            // lane i: worker base + i, whether its (non-empty) share holds a segment of the pair, and which slot
+            const int cand = base + lane;
+            const int c0 = cand < W ? split.start(cand) : T;
+            const int c1 = cand < W ? split.start(cand + 1) : T;
+            const unsigned cm = __ballot_sync(kFull, cand < W && c0 < U1 && c1 > c0);
+            const int slot_l = c0 >= U0 ? 0 : 1;
+            const unsigned long long rec_l = reinterpret_cast<unsigned long long>(
+                a.partials + (static_cast<size_t>(cand < W ? cand : 0) * 2 + slot_l) * rec_floats);
+            unsigned m = cm;
+            while (m != 0) {
+                const float* r0 = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
+                m &= m - 1;
+                float m0, l0;
+                float4 o0[NV];
+                load_rec(r0, m0, l0, o0);
+                if (NBATCH == 2 && m != 0) {
+                    const float* r1 = reinterpret_cast<const float*>(__shfl_sync(kFull, rec_l, __ffs(m) - 1));
+                    m &= m - 1;
+                    float m1, l1;
+                    float4 o1[NV];
+                    load_rec(r1, m1, l1, o1);
+                    combine(m0, l0, o0);
+                    combine(m1, l1, o1);
+                } else {
+                    combine(m0, l0, o0);
+                }
+            }
+            if (!(__ballot_sync(kFull, cand < W && c1 < U1) >> 31 & 1u)) break;  // the pair ends in this round
+        }
+        // out[s][query head u GU + r_row][d0 .. d0 + DPL), bf16
+        const int hh = r_row / G;
+        const float inv = Ls > 0.f ? out_mul(u, hh) / Ls : 0.f;
+        uint8_t* orow = reinterpret_cast<uint8_t*>(a.out) +
+                        (static_cast<size_t>(s) * a.Hq + static_cast<size_t>(u) * GU + r_row) * D * 2 + d0 * 2;
+        uint32_t wv[DPL / 2];
+#pragma unroll
+        for (int e = 0; e < DPL / 2; ++e)
+            wv[e] = static_cast<uint32_t>(float_to_bf16_bits(acc[2 * e] * inv)) |
+                    (static_cast<uint32_t>(float_to_bf16_bits(acc[2 * e + 1] * inv)) << 16);
+        if constexpr (DPL >= 8) {
+#pragma unroll
+            for (int i = 0; i < DPL / 8; ++i)
+                *reinterpret_cast<uint4*>(orow + i * 16) = make_uint4(wv[4 * i], wv[4 * i + 1], wv[4 * i + 2], wv[4 * i + 3]);
+        } else {  // one query head per unit (GU = 1): 4 dims per lane
+            *reinterpret_cast<uint2*>(orow) = make_uint2(wv[0], wv[1]);
         }
     };
     auto resolve_pending = [&]() {
