@@ -351,8 +351,9 @@ def main():
     ap.add_argument("--swap-only", action="store_true",
                     help="time swap_blocks between the device pool and pinned host memory (Llama-3-8B block geometry)")
     ap.add_argument("--varlen", action="store_true",
-                    help="the Llama-70B mixed step (48 decode tokens + one 512-token chunk) as one varlen prefill "
-                         "launch, timed beside the decode + chunk kernels")
+                    help="the Llama-70B mixed step (48 decode tokens + one 512-token chunk) as one launch "
+                         "(pkv_paged_attention_mixed), timed beside the decode + chunk kernels and beside the "
+                         "all-tile varlen launch")
     ap.add_argument("--hash-only", action="store_true",
                     help="time the chained block content hashes of the Llama-3-8B batch's token ids")
     ap.add_argument("--no-e2e", action="store_true")
@@ -734,10 +735,17 @@ def run_varlen(args, local):
     tables[B_, : pf.block_table.shape[0]] = pf.block_table
     q_all = torch.cat([st.q, st.pf_q], dim=0).contiguous()
     out_all = torch.empty_like(q_all)
+    out_tile = torch.empty_like(q_all)
     d_cu, d_qs, d_kv, d_tab = to_device(cu), to_device(q_starts), to_device(kv_lens), to_device(tables)
+    ws_mixed = torch.zeros(max(B.pkv_paged_attention_mixed_workspace_size(st.cache, B_, w.num_q_heads), 16),
+                           dtype=torch.uint8, device="cuda")
 
-    def one_launch():
-        B.pkv_paged_prefill_varlen(out_all, q_all, d_cu, d_qs, d_kv, st.k_cache, st.v_cache, st.cache, d_tab,
+    def one_launch():  # the mixed-step launch: decode tokens through the decode's work split, chunk on the tile
+        B.pkv_paged_attention_mixed(out_all, q_all, d_cu, d_qs, d_kv, st.k_cache, st.v_cache, st.cache, d_tab, B_,
+                                    w.scale, ws_mixed, st.err)
+
+    def tile_launch():  # every chunk, decode tokens included, on the prefill tile
+        B.pkv_paged_prefill_varlen(out_tile, q_all, d_cu, d_qs, d_kv, st.k_cache, st.v_cache, st.cache, d_tab,
                                    w.scale, st.err)
 
     def two_kernels():
@@ -756,16 +764,23 @@ def run_varlen(args, local):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / args.steps * 1e3
 
-    us_one = time_it(one_launch)
-    us_two = time_it(two_kernels)
+    us_one, us_two, us_tile = [], [], []
+    for _ in range(3):  # interleaved rounds: the three forms see the same clocks
+        us_one.append(time_it(one_launch))
+        us_two.append(time_it(two_kernels))
+        us_tile.append(time_it(tile_launch))
+    us_one, us_two, us_tile = (float(np.median(x)) for x in (us_one, us_two, us_tile))
     if st.device_error():
         raise RuntimeError(f"device error word {st.device_error():#x}")
     ref = torch.cat([st.out, st.pf_out], dim=0).float()
     diff = float((out_all.float() - ref).abs().max())
-    print(json.dumps({"metric": "mixed step (48 decode tokens + 512-token chunk) in one varlen launch",
+    diff_tile = float((out_tile.float() - ref).abs().max())
+    print(json.dumps({"metric": "mixed step (48 decode tokens + 512-token chunk) in one launch",
                       "value": round(B_ / (us_one * 1e-6), 1), "unit": "seq-steps/s", "us": round(us_one, 1),
-                      "two_kernel_us": round(us_two, 1), "kv_dtype": w.kv_dtype, "steps": args.steps,
-                      "max_abs_diff_vs_two_kernel_path": round(diff, 5), "config": {"workload": name}}), flush=True)
+                      "two_kernel_us": round(us_two, 1), "varlen_tile_us": round(us_tile, 1),
+                      "kv_dtype": w.kv_dtype, "steps": args.steps,
+                      "max_abs_diff_vs_two_kernel_path": round(diff, 5),
+                      "varlen_tile_max_abs_diff": round(diff_tile, 5), "config": {"workload": name}}), flush=True)
 
 
 def run_swap_only(args, local, nblocks: int = 2048):

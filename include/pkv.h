@@ -263,6 +263,38 @@ pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, i
                                     int32_t* device_error, void* stream);
 
 /*
+ * One launch for a mixed serving step: the decode tokens and the prefill chunks
+ * of a step, of different sequences ("从 PagedAttention 到 Chunked Prefill"
+ * §3.2: chunked prefill and decode share one batch; "3.3 批处理与内存管理",
+ * section "分块预填充").  The chunks are described as for
+ * pkv_paged_prefill_varlen (cu_q, q_starts, kv_lens, block_tables rows); the
+ * first num_decode chunks are decode tokens: one query each (cu_q[s] = s for
+ * s <= num_decode) at position kv_lens[s] - 1, computing what
+ * pkv_paged_attention_decode computes for it (a violation sets
+ * PKV_DEVERR_BAD_LENGTH).  The remaining chunks compute what
+ * pkv_paged_prefill_chunk computes for them.
+ *
+ * One CTA per SM: each first runs its share of the prefill tiles, then works
+ * through the decode tokens' K/V with the tensor-core decode (split-KV with
+ * merges, one KV head per work unit); the decode stream is cut so that CTAs
+ * that spent time on prefill tiles take less of it.
+ *   workspace: >= pkv_paged_attention_mixed_workspace_size bytes (0 without
+ *   decode tokens), 16-byte aligned; concurrent calls must not share it.
+ * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128,
+ *   block_size 16, G in {1, 2, 4, 8}, num_seqs <= 2048, num_decode <= 8192.
+ */
+pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
+                                     const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,
+                                     const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t num_seqs,
+                                     int32_t num_decode, int32_t num_q_heads, float scale, void* workspace,
+                                     size_t workspace_bytes, int32_t* device_error, void* stream);
+
+/* Bytes of device workspace pkv_paged_attention_mixed needs (on the current device). */
+pkv_status pkv_paged_attention_mixed_workspace_size(const pkv_cache_desc* cache, int32_t num_decode,
+                                                    int32_t num_q_heads, size_t* bytes);
+
+/*
  * Copy whole physical blocks, for copy-on-write of shared blocks
  * ("3.3 批处理与内存管理", section "共享与写时复制": before a sequence writes
  * into a block whose reference count is above one, the engine copies the

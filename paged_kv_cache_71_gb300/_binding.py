@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
                                                             P, P]
     L.pkv_paged_prefill_chunk.argtypes = [P, P, i32, i32, i32, P, P, D, P, i32, i32, f32, P, P]
     L.pkv_paged_prefill_varlen.argtypes = [P, P, i32, i32, P, P, P, P, P, D, P, i32, i32, i32, f32, P, P]
+    L.pkv_paged_attention_mixed.argtypes = [P, P, i32, i32, P, P, P, P, P, D, P, i32, i32, i32, i32, f32, P, sz,
+                                            P, P]
+    L.pkv_paged_attention_mixed_workspace_size.argtypes = [D, i32, i32, ctypes.POINTER(sz)]
     L.pkv_swap_blocks.argtypes = [P, P, i32, P, P, i32, D, P, i32, P, P]
     L.pkv_block_hashes.argtypes = [P, P, i32, i32, P, P, ctypes.c_int64, P, P]
     for name in ("pkv_reshape_and_cache", "pkv_paged_attention_workspace_size", "pkv_paged_attention_decode",
@@ -184,6 +187,27 @@ def pkv_paged_prefill_chunk(out, q, q_start: int, k_cache, v_cache, cache: Cache
                                          int(kv_len), int(q.shape[1]), float(scale), _ptr(device_error),
                                          _stream(stream)),
            "pkv_paged_prefill_chunk")
+
+
+def pkv_paged_attention_mixed_workspace_size(cache: CacheDesc, num_decode: int, num_q_heads: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().pkv_paged_attention_mixed_workspace_size(ctypes.byref(cache), int(num_decode), int(num_q_heads),
+                                                          ctypes.byref(out)),
+           "pkv_paged_attention_mixed_workspace_size")
+    return int(out.value)
+
+
+def pkv_paged_attention_mixed(out, q, cu_q, q_starts, kv_lens, k_cache, v_cache, cache: CacheDesc, block_tables,
+                              num_decode: int, scale: float, workspace=None, device_error=None, stream=None) -> None:
+    """A mixed step in one launch: chunks [0, num_decode) are decode tokens, the rest prefill chunks (varlen arrays
+    on the device, q/out [total_q_tokens][Hq][128])."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().pkv_paged_attention_mixed(_ptr(out), _ptr(q), _dtype(q), int(q.shape[0]), _ptr(cu_q),
+                                           _ptr(q_starts), _ptr(kv_lens), _ptr(k_cache), _ptr(v_cache),
+                                           ctypes.byref(cache), _ptr(block_tables), int(block_tables.shape[1]),
+                                           int(kv_lens.shape[0]), int(num_decode), int(q.shape[1]), float(scale),
+                                           _ptr(workspace), ws_bytes, _ptr(device_error), _stream(stream)),
+           "pkv_paged_attention_mixed")
 
 
 def pkv_paged_prefill_varlen(out, q, cu_q, q_starts, kv_lens, k_cache, v_cache, cache: CacheDesc, block_tables,

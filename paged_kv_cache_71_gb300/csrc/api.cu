@@ -11,6 +11,7 @@
 #include "cache_ops.cuh"
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "mixed.cuh"
 #include "prefill.cuh"
 
 namespace pkv {
@@ -48,6 +49,18 @@ PKV_EXTERN_MMA_ALL(KvI8)
 #undef PKV_EXTERN_MMA_ALL
 #undef PKV_EXTERN_MMA_GH
 #undef PKV_EXTERN_MMA
+// The mixed-step kernel's instantiations live in mixed_{bf16,fp8,i8}.cu.
+#define PKV_EXTERN_MIX(N_, KV_, G_)                                                                         \
+    extern template cudaError_t launch_paged_mixed<N_, G_, KV_>(const CUtensorMap&, const CUtensorMap&,        \
+                                                                const CUtensorMap&, const PrefillArgs&,         \
+                                                                const DecodeArgs&, const MixedArgs&, int,       \
+                                                                size_t, cudaStream_t);
+#define PKV_EXTERN_MIX_G(N_, KV_) PKV_EXTERN_MIX(N_, KV_, 1) PKV_EXTERN_MIX(N_, KV_, 2) PKV_EXTERN_MIX(N_, KV_, 4) PKV_EXTERN_MIX(N_, KV_, 8)
+PKV_EXTERN_MIX_G(0, KvBF16)
+PKV_EXTERN_MIX_G(1, KvE4M3)
+PKV_EXTERN_MIX_G(2, KvI8)
+#undef PKV_EXTERN_MIX_G
+#undef PKV_EXTERN_MIX
 
 // ------------------------------------------------------------------ error detail
 
@@ -804,5 +817,190 @@ PKV_API pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_
     a.kv_lens = kv_lens;
     cudaError_t e = launch_paged_prefill_ws(qm, km, vm, a, nk, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "paged_prefill_varlen launch");
+    return PKV_OK;
+}
+
+// ------------------------------------------------------------------ mixed step
+
+// Split-KV scratch of the mixed step's decode: one completion counter per (decode token, KV head), then two partial
+// records per worker warp (8 per SM, one KV head per work unit).
+static size_t mixed_workspace_bytes(int sms, int num_decode, int Hkv, int G) {
+    if (num_decode == 0) return 0;
+    const size_t tickets = ((static_cast<size_t>(num_decode) * Hkv * 4 + 255) / 256) * 256;
+    return tickets + static_cast<size_t>(sms) * kMmaWarps * 2 * G * (128 + 2) * 4;
+}
+
+PKV_API pkv_status pkv_paged_attention_mixed_workspace_size(const pkv_cache_desc* cache, int32_t num_decode,
+                                                            int32_t num_q_heads, size_t* bytes) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (!bytes) return fail(PKV_ERR_INVALID_ARG, "bytes is NULL");
+    if (num_decode < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes (num_decode=%d num_q_heads=%d)", num_decode, num_q_heads);
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    *bytes = mixed_workspace_bytes(di.sms, num_decode, cache->num_kv_heads, num_q_heads / cache->num_kv_heads);
+    return PKV_OK;
+}
+
+template <int N, class KV>
+static cudaError_t dispatch_mixed(int G, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                                  const PrefillArgs& pa, const DecodeArgs& da, const MixedArgs& ma, int grid,
+                                  size_t smem, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_paged_mixed<N, 1, KV>(qm, km, vm, pa, da, ma, grid, smem, s);
+        case 2: return launch_paged_mixed<N, 2, KV>(qm, km, vm, pa, da, ma, grid, smem, s);
+        case 4: return launch_paged_mixed<N, 4, KV>(qm, km, vm, pa, da, ma, grid, smem, s);
+        case 8: return launch_paged_mixed<N, 8, KV>(qm, km, vm, pa, da, ma, grid, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+PKV_API pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
+                                             const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,
+                                             const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             int32_t num_seqs, int32_t num_decode, int32_t num_q_heads, float scale,
+                                             void* workspace, size_t workspace_bytes, int32_t* device_error,
+                                             void* stream) {
+    g_detail[0] = 0;
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    const int Hkv = cache->num_kv_heads, D = cache->head_dim, S = cache->block_size;
+    if (total_q_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_decode < 0 ||
+        num_decode > num_seqs || num_decode > total_q_tokens)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "bad sizes (total_q_tokens=%d num_seqs=%d num_decode=%d num_q_heads=%d max_blocks_per_seq=%d)",
+                    total_q_tokens, num_seqs, num_decode, num_q_heads, max_blocks_per_seq);
+    if (num_q_heads % Hkv != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", num_q_heads, Hkv);
+    const int G = num_q_heads / Hkv;
+    if (q_dtype != PKV_BF16 || (cache->dtype != PKV_BF16 && !narrow(cache->dtype)))
+        return fail(PKV_ERR_UNSUPPORTED, "the mixed step supports bf16 queries with a bf16, FP8 or INT8 cache");
+    if (D != 128 || S != 16) return fail(PKV_ERR_UNSUPPORTED, "the mixed step supports head_dim 128, block_size 16");
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_ERR_UNSUPPORTED, "GQA group size %d (supported: 1, 2, 4, 8)", G);
+    if (num_seqs > prefill_ws_max_seqs())
+        return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > %d chunks per call", num_seqs, prefill_ws_max_seqs());
+    if (num_decode > 8192) return fail(PKV_ERR_UNSUPPORTED, "num_decode %d > 8192", num_decode);
+    if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * Hkv > INT32_MAX - 64)
+        return fail(PKV_ERR_OUT_OF_RANGE, "num_seqs * max_blocks_per_seq * num_kv_heads must stay below 2^31");
+    if (num_seqs == 0 || total_q_tokens == 0) return PKV_OK;
+    if (!out || !q || !cu_q || !q_starts || !kv_lens || !k_cache || !v_cache || !block_tables)
+        return fail(PKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PKV_ERR_INVALID_ARG, "q, out and the caches must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(q_starts) |
+         reinterpret_cast<uintptr_t>(kv_lens) | reinterpret_cast<uintptr_t>(block_tables)) & 3u)
+        return fail(PKV_ERR_INVALID_ARG, "index arrays must be 4-byte aligned");
+    if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
+    DeviceInfo di;
+    if ((st = device_info(&di)) != PKV_OK) return st;
+    const size_t need = mixed_workspace_bytes(di.sms, num_decode, Hkv, G);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : static_cast<size_t>(0));
+    if (need > 0 && !aligned16(workspace)) return fail(PKV_ERR_WORKSPACE, "workspace must be 16-byte aligned");
+    const bool fp8 = narrow(cache->dtype);
+    const int nk = cache->dtype == PKV_INT8 ? 2 : fp8 ? 1 : 0;
+    const bool b16 = cache->dtype == PKV_BF16;
+    const float kLog2e = 1.4426950408889634f;
+
+    // ---- prefill chunks: [num_decode, num_seqs)
+    PrefillArgs pa;
+    pa.out = out;
+    pa.block_table = block_tables;
+    pa.err = device_error;
+    pa.NQ = total_q_tokens;
+    pa.q_start = 0;
+    pa.kv_len = 0;
+    pa.Hq = num_q_heads;
+    pa.Hkv = Hkv;
+    pa.G = G;
+    pa.S = S;
+    pa.NB = cache->num_blocks;
+    pa.n_table = max_blocks_per_seq;
+    pa.sm_log2 = scale * kLog2e * (fp8 ? cache->k_scale : 1.f);
+    pa.out_mul = fp8 ? cache->v_scale : 1.f;
+    pa.sm_base = scale * kLog2e;
+    pa.k_head = cache->k_head_scales;
+    pa.v_head = cache->v_head_scales;
+    pa.timeout_ns = 2000000000ull;
+    pa.nseq = num_seqs;
+    pa.MB = max_blocks_per_seq;
+    pa.cu_q = cu_q;
+    pa.q_starts = q_starts;
+    pa.kv_lens = kv_lens;
+    pa.first_chunk = num_decode;
+    const int cta_q = 2 * (128 / G);
+    MixedArgs ma;
+    ma.num_decode = num_decode;
+    ma.slots_x = num_seqs > num_decode ? (total_q_tokens - num_decode) / cta_q + (num_seqs - num_decode) : 0;
+    ma.item_bytes = S * 128 * (b16 ? 2 : 1) * 2;
+
+    // ---- decode tokens: chunks [0, num_decode), one query each at position kv_len - 1 (the tensor-core decode, one
+    // KV head per work unit)
+    DecodeArgs da;
+    da.out = out;
+    da.q = q;
+    da.block_tables = block_tables;
+    da.context_lens = kv_lens;
+    da.err = device_error;
+    da.B = num_decode;
+    da.Hq = num_q_heads;
+    da.Hkv = Hkv;
+    da.S = S;
+    da.MB = max_blocks_per_seq;
+    da.NB = cache->num_blocks;
+    da.part_blocks = 1;
+    da.q_mul = scale * kLog2e * (fp8 ? cache->k_scale : 1.f);
+    da.o_mul = fp8 ? cache->v_scale : 1.f;
+    da.q_base = scale * kLog2e;
+    da.k_head = cache->k_head_scales;
+    da.v_head = cache->v_head_scales;
+    da.timeout_ns = 2000000000ull;
+    da.tickets = nullptr;
+    da.partials = nullptr;
+    if (need > 0) {
+        da.tickets = static_cast<int32_t*>(workspace);
+        const size_t tb = ((static_cast<size_t>(num_decode) * Hkv * 4 + 255) / 256) * 256;
+        da.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + tb);
+    }
+    const uint32_t tile = static_cast<uint32_t>((b16 ? 2 : 1) * std::max(S * 128, 1024));
+    da.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));
+    da.q_bytes = 0;
+    da.stage_bytes = 2 * tile;
+    da.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_decode) + 1) * 4 + 1023) / 1024 * 1024);
+    const size_t cost_bytes = ((2 * static_cast<size_t>(di.sms) + 1) * 4 + 1023) / 1024 * 1024;
+    const size_t budget = static_cast<size_t>(di.smem_optin) - 1024 - 1024 - cost_bytes;  // static smem, slack
+    const size_t per_warp = budget > da.prefix_bytes ? (budget - da.prefix_bytes) / kMmaWarps : 0;
+    int depth = 6;
+    while (depth >= 2 && (static_cast<size_t>(depth) * da.stage_bytes + 8 * depth + 1023) / 1024 * 1024 > per_warp)
+        --depth;
+    if (depth < 2) return fail(PKV_ERR_UNSUPPORTED, "shared memory too small for the mixed step's decode");
+    da.depth = depth;
+    da.warp_bytes = static_cast<uint32_t>((static_cast<size_t>(depth) * da.stage_bytes + 8 * depth + 1023) / 1024 * 1024);
+    ma.cost_off = static_cast<uint32_t>(da.prefix_bytes + static_cast<size_t>(kMmaWarps) * da.warp_bytes);
+    const size_t smem_dec = ma.cost_off + cost_bytes + 1024;
+    const size_t smem = std::max(smem_dec, prefill_ws_smem_bytes(nk));
+    if (smem > static_cast<size_t>(di.smem_optin) - 1024)
+        return fail(PKV_ERR_UNSUPPORTED, "device shared memory too small for the mixed step");
+
+    CUtensorMap qm, km, vm;
+    if ((st = tensor_map_sw128(&qm, q, false, 128, num_q_heads, total_q_tokens, G, 128 / G)) != PKV_OK) return st;
+    const uint64_t rows = static_cast<uint64_t>(cache->num_blocks) * S;
+    if ((st = tensor_map_sw128(&km, k_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    if ((st = tensor_map_sw128(&vm, v_cache, fp8, 128, Hkv, rows, 1, S)) != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (da.tickets) {
+        cudaError_t e = cudaMemsetAsync(da.tickets, 0, static_cast<size_t>(num_decode) * Hkv * 4, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing split-KV counters");
+    }
+    const cudaError_t e =
+        nk == 0   ? dispatch_mixed<0, KvBF16>(G, qm, km, vm, pa, da, ma, di.sms, smem, s)
+        : nk == 1 ? dispatch_mixed<1, KvE4M3>(G, qm, km, vm, pa, da, ma, di.sms, smem, s)
+                  : dispatch_mixed<2, KvI8>(G, qm, km, vm, pa, da, ma, di.sms, smem, s);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_attention_mixed launch");
     return PKV_OK;
 }

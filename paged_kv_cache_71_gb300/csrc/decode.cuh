@@ -245,9 +245,13 @@ __device__ __forceinline__ int find_seq(const int* P, int B, int key) {
 // the next allowed cut (a pair boundary, or a multiple of C blocks inside a pair).  All
 // arithmetic is 32-bit: T < 2^31 is checked on the host, and floor(w * T / W) is formed as
 // w * (T / W) + floor(w * (T % W) / W) with w * (T % W) < W^2.
+// Optional weighting (a mixed step, where some CTAs start on the stream late): cb[c] .. cb[c + 1] is CTA c's part
+// of the stream before snapping, split evenly among its NWc workers.
 struct WorkSplit {
     const int* P;
     int B, Hkv, T, C, W, tq, tr;
+    const int* cb = nullptr;
+    int NWc = 1;
 
     __device__ __forceinline__ int snap(int x) const {
         if (x >= T) return T;
@@ -261,6 +265,11 @@ struct WorkSplit {
     }
     __device__ __forceinline__ int start(int w) const {
         if (w >= W) return T;
+        if (cb != nullptr) {
+            const int c = w / NWc, i = w - c * NWc;
+            const int x = cb[c] + static_cast<int>((static_cast<long long>(cb[c + 1] - cb[c]) * i) / NWc);
+            return snap(x < 0 ? 0 : x);
+        }
         return snap(w * tq + (w * tr) / W);
     }
 };

@@ -118,10 +118,22 @@ struct MmaStage {
 // second half of each S quad and its output the second half of each O quad.  The MMA count per byte is the same,
 // the per-block work of the pipeline (waits, refills, metadata, softmax reductions) is shared by two heads, and the
 // two heads' rows of a token, adjacent in the cache, are fetched together.
-template <int G, int S, class KV, int HP>
-__global__ void __launch_bounds__(32 * kMmaWarps, 1)
-    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                            const DecodeArgs a) {
+// Barrier over the first nthreads threads of the CTA (all of them: __syncthreads; fewer, when the rest of the CTA
+// does other work or has left: named barrier 1).
+__device__ __forceinline__ void threads_sync(int nthreads) {
+    if (nthreads == static_cast<int>(blockDim.x)) __syncthreads();
+    else asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// The decode, run by the first nthreads threads of a CTA (nthreads / 32 worker warps) as CTA cta of ncta CTAs that
+// share the work stream; smem_raw is the dynamic shared memory the plan in `a` describes.  pcost (nullable, ncta
+// entries) weights the split for CTAs that join the stream late: CTA c is taken to have pcost[c] stream items of
+// other work before its decode starts, and the stream is cut so that every CTA finishes together (the cut points go
+// to cb, ncta + 1 ints of shared memory); WEIGHTED selects this form at compile time.
+template <int G, int S, class KV, int HP, bool WEIGHTED>
+__device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
+                                                uint8_t* smem_raw, int cta, int ncta, int nthreads,
+                                                const int* pcost, int* cb) {
     constexpr int D = 128;
     constexpr int TS = S < 16 ? S : 16;   // tokens of a block per 16-row MMA tile
     constexpr int NT = S / TS;            // tiles per block
@@ -131,11 +143,10 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     static_assert(G <= 8 && (HP == 1 || HP == 2), "query rows of one MMA tile");
     static_assert(KV::es <= 2, "one-byte or bf16 caches");
 
-    extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int NW = blockDim.x >> 5;
+    const int NW = nthreads >> 5;
     const int B = a.B, Hkv = a.Hkv;
     const int g = lane >> 2, t = lane & 3;  // fragment row (query head) and column pair
     // this thread's operand offsets inside a K or V half: K rows g and 8 + g (1024 bytes further, same swizzle),
@@ -150,14 +161,14 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     // ---- 1. per-sequence block counts and their prefix sum (P[s] = blocks before s)
     int* P = reinterpret_cast<int*>(smem);
     {
-        const int per = (B + blockDim.x - 1) / blockDim.x;
+        const int per = (B + nthreads - 1) / nthreads;
         const int s0 = tid * per;
         const int s1 = min(B, s0 + per);
         int local = 0;
         for (int s = s0; s < s1; ++s) {
             int L = a.context_lens[s];
             if (L < 0 || L > a.MB * S) {
-                if (blockIdx.x == 0) raise_error(a.err, PKV_DEVERR_BAD_LENGTH);
+                if (cta == 0) raise_error(a.err, PKV_DEVERR_BAD_LENGTH);
                 L = 0;
             }
             local += (L + S - 1) / S;
@@ -170,7 +181,7 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
         }
         __shared__ int warp_tot[32];
         if (lane == 31) warp_tot[warp] = incl;
-        __syncthreads();
+        threads_sync(nthreads);
         int wbase = 0;
         for (int i = 0; i < warp; ++i) wbase += warp_tot[i];
         int run = wbase + incl - local;
@@ -180,19 +191,19 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
             if (L < 0 || L > a.MB * S) L = 0;
             run += (L + S - 1) / S;
         }
-        if (tid == blockDim.x - 1) {
+        if (tid == nthreads - 1) {
             int tot = 0;
             for (int i = 0; i < NW; ++i) tot += warp_tot[i];
             P[B] = tot;
         }
-        __syncthreads();
+        threads_sync(nthreads);
     }
 
     // ---- 2. empty sequences get zero rows (spread over the CTAs)
-    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+    for (int s = cta; s < B; s += ncta) {
         if (P[s + 1] != P[s]) continue;
         const int n = a.Hq * D;
-        for (int i = tid; i < n; i += blockDim.x) reinterpret_cast<uint16_t*>(a.out)[static_cast<size_t>(s) * n + i] = 0;
+        for (int i = tid; i < n; i += nthreads) reinterpret_cast<uint16_t*>(a.out)[static_cast<size_t>(s) * n + i] = 0;
     }
 
     // ---- 3. this warp's stages and barriers, and its share of the work stream
@@ -209,9 +220,50 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     const int Hu = Hkv / HP;  // work units per block: KV heads taken HP at a time
     const int T = Hu * P[B];
     if (T == 0) return;
-    const int W = min(static_cast<int>(gridDim.x) * NW, T);
-    const int w = blockIdx.x * NW + warp;
-    const WorkSplit split{P, B, Hu, T, a.part_blocks, W, T / W, T % W};
+    const int W = WEIGHTED ? ncta * NW : min(ncta * NW, T);
+    const int w = cta * NW + warp;
+    if constexpr (WEIGHTED) {
+        // CTA c's part of the stream: E - pcost[c] items, E chosen so that the parts add up to T (CTAs whose other
+        // work alone reaches E get none).  The levelling runs in 1/1024 items, so that a stream shorter than the
+        // CTA count still spreads over the idle CTAs; one thread per CTA computes the same cut points.
+        if (warp == 0 && lane == 0) {
+            const long long Ts = static_cast<long long>(T) << 10;
+            long long tot = Ts;
+            for (int c = 0; c < ncta; ++c) tot += static_cast<long long>(pcost[c]) << 10;
+            long long E = tot / ncta;
+            for (int it = 0; it < 4; ++it) {  // drop CTAs above E and re-level (converges in a few steps)
+                long long t2 = Ts;
+                int n2 = 0;
+                for (int c = 0; c < ncta; ++c) {
+                    const long long pc = static_cast<long long>(pcost[c]) << 10;
+                    if (pc < E) {
+                        t2 += pc;
+                        ++n2;
+                    }
+                }
+                E = n2 ? t2 / n2 : E;
+            }
+            long long acc = 0, given = 0;
+            for (int c = 0; c < ncta; ++c) {
+                const long long pc = static_cast<long long>(pcost[c]) << 10;
+                acc += pc < E ? E - pc : 0;
+            }
+            cb[0] = 0;
+            for (int c = 0; c < ncta; ++c) {
+                const long long pc = static_cast<long long>(pcost[c]) << 10;
+                given += pc < E ? E - pc : 0;
+                // monotone in c (given never falls), and exactly T at the last CTA
+                const double f = acc > 0 ? static_cast<double>(given) / static_cast<double>(acc) : 1.0;
+                cb[c + 1] = c + 1 == ncta ? T : min(T, static_cast<int>(f * static_cast<double>(T)));
+            }
+        }
+        threads_sync(nthreads);  // every worker reads the cut points
+    }
+    WorkSplit split{P, B, Hu, T, a.part_blocks, W, T / W, T % W};
+    if constexpr (WEIGHTED) {
+        split.cb = cb;
+        split.NWc = NW;
+    }
     const int A0 = split.start(w);
     const int A1 = split.start(w + 1);
     if (A0 >= A1) return;
@@ -752,6 +804,15 @@ __global__ void __launch_bounds__(32 * kMmaWarps, 1)
     }
     resolve_pending();
 }
+template <int G, int S, class KV, int HP>
+__global__ void __launch_bounds__(32 * kMmaWarps, 1)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                            const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    decode_mma_body<G, S, KV, HP, false>(kmap, vmap, a, smem_raw, blockIdx.x, gridDim.x, blockDim.x, nullptr,
+                                         nullptr);
+}
+
 // Host-side launch for one instantiation (defined in decode_mma_*.cu).
 template <int G, int S, class KV, int HP>
 cudaError_t launch_paged_decode_mma(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a, int grid,

@@ -12,6 +12,7 @@ struct PrefillArgs {
     int NQ, q_start, kv_len, Hq, Hkv, G, S, NB, n_table;
     // varlen (cu_q set): per-chunk query offsets / start positions / key counts, device arrays
     int nseq = 1, MB = 0;
+    int first_chunk = 0;         // chunks below it are not prefill chunks (a mixed step's decode tokens)
     const int32_t* cu_q = nullptr;
     const int32_t* q_starts = nullptr;
     const int32_t* kv_lens = nullptr;
