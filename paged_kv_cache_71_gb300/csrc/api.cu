@@ -897,6 +897,7 @@ PKV_API pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q
     if (!(scale > 0.f && scale < 3.0e38f)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite and positive");
     DeviceInfo di;
     if ((st = device_info(&di)) != PKV_OK) return st;
+    if (di.sms > 256) return fail(PKV_ERR_UNSUPPORTED, "the mixed step's work split takes at most 256 SMs");
     const size_t need = mixed_workspace_bytes(di.sms, num_decode, Hkv, G);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -937,7 +938,8 @@ PKV_API pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q
     MixedArgs ma;
     ma.num_decode = num_decode;
     ma.slots_x = num_seqs > num_decode ? (total_q_tokens - num_decode) / cta_q + (num_seqs - num_decode) : 0;
-    ma.item_bytes = S * 128 * (b16 ? 2 : 1) * 2;
+    // a prefill key tile's weight in decode stream items (one block of one KV head, K and V)
+    ma.tile_cost = kDecodeBytesPerKeyTile * kCostUnit / (S * 128 * (b16 ? 2 : 1) * 2);
 
     // ---- decode tokens: chunks [0, num_decode), one query each at position kv_len - 1 (the tensor-core decode, one
     // KV head per work unit)
@@ -971,7 +973,10 @@ PKV_API pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q
     da.kv_bytes = static_cast<uint32_t>(S * 128 * (b16 ? 2 : 1));
     da.q_bytes = 0;
     da.stage_bytes = 2 * tile;
-    da.prefix_bytes = static_cast<uint32_t>(((static_cast<size_t>(num_decode) + 1) * 4 + 1023) / 1024 * 1024);
+    // the sequence prefix of the decode tokens, and before it the slot prefix of the prefill chunks
+    const size_t n_prefix = static_cast<size_t>(std::max(num_decode, num_seqs - num_decode)) + 1;
+    da.prefix_bytes = static_cast<uint32_t>((n_prefix * 4 + 1023) / 1024 * 1024);
+    // CTA costs and cut points of the weighted split
     const size_t cost_bytes = ((2 * static_cast<size_t>(di.sms) + 1) * 4 + 1023) / 1024 * 1024;
     const size_t budget = static_cast<size_t>(di.smem_optin) - 1024 - 1024 - cost_bytes;  // static smem, slack
     const size_t per_warp = budget > da.prefix_bytes ? (budget - da.prefix_bytes) / kMmaWarps : 0;

@@ -246,12 +246,12 @@ __device__ __forceinline__ int find_seq(const int* P, int B, int key) {
 // arithmetic is 32-bit: T < 2^31 is checked on the host, and floor(w * T / W) is formed as
 // w * (T / W) + floor(w * (T % W) / W) with w * (T % W) < W^2.
 // Optional weighting (a mixed step, where some CTAs start on the stream late): cb[c] .. cb[c + 1] is CTA c's part
-// of the stream before snapping, split evenly among its NWc workers.
+// of the stream, split evenly among its 2^nw_shift workers before snapping.
 struct WorkSplit {
     const int* P;
     int B, Hkv, T, C, W, tq, tr;
     const int* cb = nullptr;
-    int NWc = 1;
+    int nw_shift = 0;
 
     __device__ __forceinline__ int snap(int x) const {
         if (x >= T) return T;
@@ -266,9 +266,10 @@ struct WorkSplit {
     __device__ __forceinline__ int start(int w) const {
         if (w >= W) return T;
         if (cb != nullptr) {
-            const int c = w / NWc, i = w - c * NWc;
-            const int x = cb[c] + static_cast<int>((static_cast<long long>(cb[c + 1] - cb[c]) * i) / NWc);
-            return snap(x < 0 ? 0 : x);
+            const int c = w >> nw_shift, i = w - (c << nw_shift);
+            const int span = cb[c + 1] - cb[c];
+            const float f = static_cast<float>(i) * (1.0f / static_cast<float>(1 << nw_shift));  // exact
+            return snap(cb[c] + min(span, static_cast<int>(static_cast<float>(span) * f)));
         }
         return snap(w * tq + (w * tr) / W);
     }

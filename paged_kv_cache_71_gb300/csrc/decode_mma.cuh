@@ -128,8 +128,11 @@ __device__ __forceinline__ void threads_sync(int nthreads) {
 // The decode, run by the first nthreads threads of a CTA (nthreads / 32 worker warps) as CTA cta of ncta CTAs that
 // share the work stream; smem_raw is the dynamic shared memory the plan in `a` describes.  pcost (nullable, ncta
 // entries) weights the split for CTAs that join the stream late: CTA c is taken to have pcost[c] stream items of
-// other work before its decode starts, and the stream is cut so that every CTA finishes together (the cut points go
-// to cb, ncta + 1 ints of shared memory); WEIGHTED selects this form at compile time.
+// other work before its decode starts (in 1/kCostUnit items), and the stream is cut so that every CTA finishes
+// together; cb is shared memory for the cut points (ncta + 1 ints, ncta <= 256, nthreads / 32 a power of two).
+// WEIGHTED selects this form at compile time.
+constexpr int kCostUnit = 16;  // the weighted split's CTA costs are in 1/16 stream items
+
 template <int G, int S, class KV, int HP, bool WEIGHTED>
 __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeArgs& a,
                                                 uint8_t* smem_raw, int cta, int ncta, int nthreads,
@@ -224,45 +227,81 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
     const int w = cta * NW + warp;
     if constexpr (WEIGHTED) {
         // CTA c's part of the stream: E - pcost[c] items, E chosen so that the parts add up to T (CTAs whose other
-        // work alone reaches E get none).  The levelling runs in 1/1024 items, so that a stream shorter than the
-        // CTA count still spreads over the idle CTAs; one thread per CTA computes the same cut points.
-        if (warp == 0 && lane == 0) {
-            const long long Ts = static_cast<long long>(T) << 10;
-            long long tot = Ts;
-            for (int c = 0; c < ncta; ++c) tot += static_cast<long long>(pcost[c]) << 10;
-            long long E = tot / ncta;
-            for (int it = 0; it < 4; ++it) {  // drop CTAs above E and re-level (converges in a few steps)
-                long long t2 = Ts;
+        // work alone reaches E get none).  Warp 0 of every CTA computes the same cut points, each lane over a run of
+        // up to 8 CTAs held in registers, in fp32 (GB300 has little FP64 throughput, and a 64-bit division goes
+        // through it): E by levelling, then every CTA's part rounded to whole items and an exact integer prefix over
+        // the parts, so that the cuts are monotone; the last is T.
+        if (warp == 0) {
+            constexpr int kPer = 8;  // CTAs per lane: ncta <= 256
+            const int per = (ncta + 31) / 32;
+            const int c_lo = lane * per;
+            float pv[kPer];  // this lane's CTAs' costs in items (-1: no CTA)
+#pragma unroll
+            for (int k = 0; k < kPer; ++k)
+                pv[k] = (k < per && c_lo + k < ncta) ? static_cast<float>(pcost[c_lo + k]) * (1.0f / kCostUnit) : -1.f;
+            const float Tf = static_cast<float>(T);
+            auto wsum = [](float v) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+                return v;
+            };
+            float own = 0.f;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) own += fmaxf(pv[k], 0.f);
+            float E = (Tf + wsum(own)) / static_cast<float>(ncta);
+            int n_prev = ncta;
+            for (int it = 0; it < 4; ++it) {  // drop CTAs at or above E and re-level (a few steps at most)
+                float t2 = 0.f;
                 int n2 = 0;
-                for (int c = 0; c < ncta; ++c) {
-                    const long long pc = static_cast<long long>(pcost[c]) << 10;
-                    if (pc < E) {
-                        t2 += pc;
+#pragma unroll
+                for (int k = 0; k < kPer; ++k)
+                    if (pv[k] >= 0.f && pv[k] < E) {
+                        t2 += pv[k];
                         ++n2;
                     }
-                }
-                E = n2 ? t2 / n2 : E;
+                n2 = __reduce_add_sync(kFull, n2);
+                t2 = wsum(t2);
+                if (n2 == 0 || n2 == n_prev) break;  // uniform across the warp
+                n_prev = n2;
+                E = (Tf + t2) / static_cast<float>(n2);
             }
-            long long acc = 0, given = 0;
-            for (int c = 0; c < ncta; ++c) {
-                const long long pc = static_cast<long long>(pcost[c]) << 10;
-                acc += pc < E ? E - pc : 0;
+            float mine_f = 0.f;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) mine_f += pv[k] >= 0.f ? fmaxf(E - pv[k], 0.f) : 0.f;
+            const float acc = wsum(mine_f);
+            const float inv = acc > 0.f ? Tf / acc : 0.f;
+            int part[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k)
+                part[k] = pv[k] < 0.f ? 0
+                          : acc > 0.f ? static_cast<int>(rintf(fmaxf(E - pv[k], 0.f) * inv))
+                                      : (c_lo + k == 0 ? T : 0);
+            // exact prefix sums (64-bit adds: rounding may take the total a few items past T), clamped only where
+            // written
+            long long mine = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) mine += part[k];
+            long long incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
             }
-            cb[0] = 0;
-            for (int c = 0; c < ncta; ++c) {
-                const long long pc = static_cast<long long>(pcost[c]) << 10;
-                given += pc < E ? E - pc : 0;
-                // monotone in c (given never falls), and exactly T at the last CTA
-                const double f = acc > 0 ? static_cast<double>(given) / static_cast<double>(acc) : 1.0;
-                cb[c + 1] = c + 1 == ncta ? T : min(T, static_cast<int>(f * static_cast<double>(T)));
+            long long run = incl - mine;
+            if (lane == 0) cb[0] = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int c = c_lo + k;
+                run += part[k];
+                if (k < per && c < ncta) cb[c + 1] = c + 1 == ncta ? T : static_cast<int>(min(static_cast<long long>(T), run));
             }
         }
-        threads_sync(nthreads);  // every worker reads the cut points
+        threads_sync(nthreads);
     }
     WorkSplit split{P, B, Hu, T, a.part_blocks, W, T / W, T % W};
     if constexpr (WEIGHTED) {
         split.cb = cb;
-        split.NWc = NW;
+        split.nw_shift = 31 - __clz(NW);  // NW is a power of two (8)
     }
     const int A0 = split.start(w);
     const int A1 = split.start(w + 1);
