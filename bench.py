@@ -167,7 +167,8 @@ def decode_kernel(w) -> tuple[str, tuple]:
         tag = {"e4m3": "fp8", "i8": "i8", "bf16": "bf16"}[w.kv_dtype]
         return "paged_decode_mma_kernel", ("decode_mma.cuh", "decode.cuh", "pkv_device.cuh",
                                            f"decode_mma_{tag}_s{w.block_size}.cu")
-    return "paged_decode_kernel", DECODE_SOURCES
+    tag = {"f32": "f32", "bf16": "bf16", "e4m3": "fp8", "i8": "i8"}[w.kv_dtype]
+    return "paged_decode_kernel", ("decode.cuh", "pkv_device.cuh", f"decode_{tag}_s{w.block_size}.cu")
 
 
 def kernel_digest(files) -> str:
