@@ -44,11 +44,15 @@ def _mixed_case(decode_lens, chunks, Hq, Hkv, seed, kv="bf16", tail_rows=2):
     return q, kc, vc, tables, cu, q_starts, kv_lens
 
 
-def _run(case, num_decode, kv):
+def _run(case, num_decode, kv, head_scales=None):
     q, kc, vc, tables, cu, q_starts, kv_lens = case
     ks, vs = SCALES[kv]
     dq, dk, dv = to_device(q), to_device(kc), to_device(vc)
-    desc = B.CacheDesc.for_cache(dk, ks, vs)
+    if head_scales is None:
+        desc = B.CacheDesc.for_cache(dk, ks, vs)
+    else:
+        dks, dvs = (torch.from_numpy(x).cuda() for x in head_scales)
+        desc = B.CacheDesc.for_cache(dk, 1.0, 1.0, dks, dvs)
     out = torch.full_like(dq, float("nan"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     need = pkv.pkv_paged_attention_mixed_workspace_size(desc, num_decode, q.shape[1])
@@ -59,18 +63,19 @@ def _run(case, num_decode, kv):
     return to_host(out), int(err.item())
 
 
-def _check_all(case, num_decode, kv, what):
+def _check_all(case, num_decode, kv, what, head_scales=None):
     q, kc, vc, tables, cu, q_starts, kv_lens = case
-    got, err = _run(case, num_decode, kv)
+    got, err = _run(case, num_decode, kv, head_scales)
     assert err == 0, hex(err)
     ks, vs = SCALES[kv]
+    scales = dict(k_scale=ks, v_scale=vs) if head_scales is None else \
+        dict(k_head_scales=head_scales[0], v_head_scales=head_scales[1])
     for s in range(len(kv_lens)):
         if cu[s + 1] == cu[s]:
             continue
         n_tab = -(-int(kv_lens[s]) // 16)
         ref = oracle.paged_prefill_chunk(q[cu[s]:cu[s + 1]], int(q_starts[s]), kc, vc, tables[s, :n_tab],
-                                         int(kv_lens[s]), 1 / np.sqrt(128), cache_dtype=CODE[kv], k_scale=ks,
-                                         v_scale=vs)
+                                         int(kv_lens[s]), 1 / np.sqrt(128), cache_dtype=CODE[kv], **scales)
         assert_close(kv, got[cu[s]:cu[s + 1]], ref, f"{what}: chunk {s} (q_start {q_starts[s]}, kv_len {kv_lens[s]})")
     assert np.isnan(got[cu[-1]:]).all(), "rows outside every chunk were written"
     return got
@@ -85,6 +90,25 @@ CHUNKS = [(0, 200), (1000, 57), (129, 0), (5, 33), (128, 128)]
 def test_mixed_step_matches_oracle(kv, Hq, Hkv):
     case = _mixed_case(DECODE, CHUNKS, Hq, Hkv, seed=Hq + Hkv, kv=kv)
     _check_all(case, len(DECODE), kv, f"{kv} G={Hq // Hkv}")
+
+
+@pytest.mark.parametrize("kv", ["e4m3", "i8"])
+def test_mixed_step_per_head_scales(kv):
+    """One-byte caches with one scale per KV head (replacing the per-tensor scale for both the decode tokens and the
+    prefill chunks of the step)."""
+    case = _mixed_case(DECODE, CHUNKS, 64, 8, seed=31, kv=kv)
+    rng = np.random.default_rng(32)
+    base = SCALES[kv]
+    head = (np.float32(base[0]) * rng.uniform(0.5, 2.0, 8).astype(np.float32),
+            np.float32(base[1]) * rng.uniform(0.5, 2.0, 8).astype(np.float32))
+    _check_all(case, len(DECODE), kv, f"{kv} per-head scales", head_scales=head)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_mixed_step_odd_kv_head_count(kv):
+    """Three KV heads in groups of two: the decode's work units and the tile slots run per KV head, at any count."""
+    case = _mixed_case([5, 2000, 33], [(0, 70), (400, 9)], 6, 3, seed=33, kv=kv)
+    _check_all(case, 3, kv, f"{kv} Hkv=3")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
