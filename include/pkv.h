@@ -280,8 +280,10 @@ pkv_status pkv_paged_prefill_varlen(void* out, const void* q, int32_t q_dtype, i
  * that spent time on prefill tiles take less of it.
  *   workspace: >= pkv_paged_attention_mixed_workspace_size bytes (0 without
  *   decode tokens), 16-byte aligned; concurrent calls must not share it.
+ * Per-tensor or per-head scales apply as in the decode and prefill calls.
  * Supported: bf16 queries, bf16, FP8 or INT8 cache, head_dim 128,
- *   block_size 16, G in {1, 2, 4, 8}, num_seqs <= 2048, num_decode <= 8192.
+ *   block_size 16, G in {1, 2, 4, 8}, num_seqs <= 2048, num_decode <= 8192,
+ *   devices of at most 256 SMs; other cases return PKV_ERR_UNSUPPORTED.
  */
 pkv_status pkv_paged_attention_mixed(void* out, const void* q, int32_t q_dtype, int32_t total_q_tokens,
                                      const int32_t* cu_q, const int32_t* q_starts, const int32_t* kv_lens,
