@@ -79,6 +79,15 @@ def test_decode_host_checks_before_any_device_work():
     assert call(args(scale=float("nan"))) == 1
     assert call(args(B=9000)) == 2
     assert call(args(B=0)) == 0              # empty batch is a no-op
+    # the shared-block form takes the same arguments and the same checks
+    shared = lambda a: L.pkv_paged_attention_decode_shared(a["out"], a["q"], a["q_dtype"], a["k"], a["v"],
+                                                           ctypes.byref(d), a["bt"], a["mb"], a["cl"], a["B"],
+                                                           a["Hq"], a["scale"], a["splits"], a["maxlen"], a["ws"],
+                                                           a["wsb"], None, None)
+    assert shared(args(Hq=30)) == 1
+    assert shared(args(Hq=8 * 3)) == 2
+    assert shared(args(q=24)) == 1
+    assert shared(args(B=0)) == 0
 
 
 def test_reshape_and_copy_host_checks():
@@ -114,3 +123,33 @@ def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
         pkv.pkv_paged_attention_decode(q.clone(), q, torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16),
                                        torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16), desc,
                                        torch.zeros(2, 1, dtype=torch.int32), torch.ones(2, dtype=torch.int32), 0.1)
+
+
+def test_mixed_step_host_checks_before_any_device_work():
+    """pkv_paged_attention_mixed rejects bad steps on the host, before it asks for the device."""
+    L = pkv.lib()
+
+    def call(desc=None, **o):
+        a = dict(out=16, q=16, q_dtype=B.PKV_BF16, total=40, cu=16, qs=16, kl=16, k=16, v=16, bt=16, mb=4, n=3,
+                 nd=2, Hq=64, scale=0.1, ws=16, wsb=1 << 20)
+        a.update(o)
+        d = desc or _desc()
+        return L.pkv_paged_attention_mixed(a["out"], a["q"], a["q_dtype"], a["total"], a["cu"], a["qs"], a["kl"],
+                                           a["k"], a["v"], ctypes.byref(d), a["bt"], a["mb"], a["n"], a["nd"],
+                                           a["Hq"], a["scale"], a["ws"], a["wsb"], None, None)
+    assert call(nd=4) == 1                           # more decode tokens than chunks
+    assert call(nd=-1) == 1
+    assert call(total=1) == 1                        # fewer query tokens than decode tokens
+    assert call(Hq=60) == 1                          # not a multiple of the KV heads
+    assert call(Hq=8 * 16) == 2                      # G = 16
+    assert call(Hq=8 * 3) == 2                       # G = 3
+    assert call(q_dtype=B.PKV_F32) == 2
+    assert call(desc=_desc(block_size=8)) == 2       # block_size 16 only
+    assert call(desc=_desc(head_dim=64)) == 2        # head_dim 128 only
+    assert call(desc=_desc(dtype=B.PKV_F32)) == 2    # bf16, FP8 or INT8 caches
+    assert call(n=4096, nd=2) == 2                   # more chunks than one launch takes
+    assert call(n=0, nd=0) == 0                      # an empty step is a no-op
+    assert call(total=0, nd=0) == 0
+    out = ctypes.c_size_t(1)
+    assert L.pkv_paged_attention_mixed_workspace_size(ctypes.byref(_desc()), -1, 64, ctypes.byref(out)) == 1
+    assert L.pkv_paged_attention_mixed_workspace_size(ctypes.byref(_desc()), 4, 60, ctypes.byref(out)) == 1
