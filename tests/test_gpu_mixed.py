@@ -169,10 +169,12 @@ def test_decode_token_not_at_the_last_position_is_flagged():
     assert err & B.DEVERR_BAD_LENGTH
 
 
-def test_llama70b_mixed_step_fp8():
+@pytest.mark.parametrize("name", ["llama70b_mixed_fp8", "llama70b_mixed_bf16"])
+def test_llama70b_mixed_step(name):
     """The Llama-70B mixed step (48 decode tokens over 4096..32768 keys, the 512-token chunk at 8192..8703) in one
     launch: every decode token and 64 sampled chunk rows against the oracle."""
-    w = wl.make("llama70b_mixed_fp8")
+    w = wl.make(name)
+    kind = "e4m3" if w.kv_dtype == "e4m3" else "bf16"
     st = DeviceStep(w)
     st.write()
     torch.cuda.synchronize()
@@ -196,8 +198,8 @@ def test_llama70b_mixed_step_fp8():
     assert st.device_error() == 0
     got = to_host(out)
     kc, vc, ref = oracle_step(w)
-    assert_close("e4m3", got[:nd], ref, "Llama-70B mixed step, decode tokens")
+    assert_close(kind, got[:nd], ref, f"{name}: decode tokens")
     rows = np.random.default_rng(1).choice(pf.q.shape[0], 64, replace=False)
     pref = oracle.paged_prefill_chunk(pf.q, pf.q_start, kc, vc, pf.block_table, pf.kv_len, w.scale, rows=rows,
-                                      cache_dtype=oracle.E4M3, k_scale=w.k_scale, v_scale=w.v_scale)
-    assert_close("e4m3", got[nd + rows], pref, "Llama-70B mixed step, chunk rows")
+                                      cache_dtype=CODE[kind], k_scale=w.k_scale, v_scale=w.v_scale)
+    assert_close(kind, got[nd + rows], pref, f"{name}: chunk rows")
