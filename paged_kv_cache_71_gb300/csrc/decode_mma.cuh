@@ -37,6 +37,15 @@ constexpr int kMmaWarps = 8;
 // one m16n8k16 MMA, f16 (or bf16: B16) operands, fp32 accumulate in place.  The operands are whole register quads
 // (rows 8-15 of A are zero registers of the quad and rows 8-15 of C accumulate nothing of use), so no copies are
 // needed around it.
+// two INT8 codes (low bytes first, or the high half when HI) -> f16x2 of 1152 + code, exactly (one byte permute).
+// The key operand takes the codes in this biased form: q.(1152 + k) = q.k + 1152 sum(q), and the decode subtracts
+// 1152 sum(q) (one value per query row and segment) from the fp32 scores, which saves the f16 subtraction per two
+// key codes; the cancellation costs about 2^-20 of the scores' magnitude.
+template <bool HI>
+__device__ __forceinline__ uint32_t s8x2_to_biased_f16x2(uint32_t w) {
+    return __byte_perm(w ^ 0x80808080u, 0x64646464u, HI ? 0x7362u : 0x5140u);
+}
+
 template <bool B16>
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     if constexpr (B16)
@@ -549,7 +558,8 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
         uint32_t qa[8][4];
         // O[g][dim] of head 0 in elements 0, 1 and of head 1 in elements 2, 3 of output tile n (dims: dim_of below)
         float o[16][4];
-        float m_ref[HP], l_run[HP], qm[HP];  // per head: running max of row g (log2 units), this thread's share of
+        float m_ref[HP], l_run[HP], qm[HP];
+        float qoff[HP];  // INT8: 1152 times the row's query sum, taken off the scores of the biased key codes  // per head: running max of row g (log2 units), this thread's share of
                                              // the running sum, score scale
         int ma = 0, mc = 0, seg_first = 0;
         bool first = true;
@@ -582,8 +592,13 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
                     const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
-                        kf[ks][0] = codes2_to_f16x2<KV, false>(w[ks]);
-                        kf[ks][1] = codes2_to_f16x2<KV, true>(w[ks]);
+                        if constexpr (KV::code == PKV_INT8) {
+                            kf[ks][0] = s8x2_to_biased_f16x2<false>(w[ks]);
+                            kf[ks][1] = s8x2_to_biased_f16x2<true>(w[ks]);
+                        } else {
+                            kf[ks][0] = codes2_to_f16x2<KV, false>(w[ks]);
+                            kf[ks][1] = codes2_to_f16x2<KV, true>(w[ks]);
+                        }
                     }
                 }
             };
@@ -618,6 +633,12 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
                     }
                 }
                 // ---- online softmax of head hh's row g over the tile's tokens
+                if constexpr (KV::code == PKV_INT8) {
+                    s0[2 * hh] -= qoff[hh];
+                    s0[2 * hh + 1] -= qoff[hh];
+                    s1[2 * hh] -= qoff[hh];
+                    s1[2 * hh + 1] -= qoff[hh];
+                }
                 const float sc0 = (t0 < lim) ? s0[2 * hh] * qm[hh] : -INFINITY;
                 const float sc1 = (t0 + 1 < lim) ? s0[2 * hh + 1] * qm[hh] : -INFINITY;
                 const float sc2 = (t2 < lim) ? s1[2 * hh] * qm[hh] : -INFINITY;
@@ -714,6 +735,7 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
                     const uint4* qrow = reinterpret_cast<const uint4*>(
                         reinterpret_cast<const uint8_t*>(a.q) +
                         (static_cast<size_t>(ma >> 10) * a.Hq + static_cast<size_t>(hk) * G + g) * D * 2);
+                    float qsum = 0.f;  // INT8: this thread's dims of row g
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int qi = B16 ? (i < 2 ? 2 * t + i : 8 + 2 * t + i - 2) : 4 * t + i;  // 16-byte units
@@ -734,6 +756,8 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
                             f[1] = pack2<false>(f1.x, f1.y);
                             f[2] = pack2<false>(f2.x, f2.y);
                             f[3] = pack2<false>(f3.x, f3.y);
+                            if constexpr (KV::code == PKV_INT8)
+                                qsum += ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
                         }
                         // dims d, d+1 go to the k 2t register of the quad, d+2, d+3 to the k 2t+8 register; head 0
                         // in rows g (elements 0, 2), head 1 in rows g + 8 (elements 1, 3)
@@ -741,6 +765,11 @@ __device__ __forceinline__ void decode_mma_body(const CUtensorMap& kmap, const C
                         qa[2 * i][2 + hh] = f[1];
                         qa[2 * i + 1][hh] = f[2];
                         qa[2 * i + 1][2 + hh] = f[3];
+                    }
+                    if constexpr (KV::code == PKV_INT8) {  // the row's sum over the 4 lanes that hold it
+                        qsum += __shfl_xor_sync(kFull, qsum, 1);
+                        qsum += __shfl_xor_sync(kFull, qsum, 2);
+                        qoff[hh] = 1152.f * qsum;
                     }
                 }
                 if (!in_range) raise_error(a.err, PKV_DEVERR_Q_RANGE);
